@@ -1,0 +1,396 @@
+"""Pins that tie the fp64 oracle to facts fixed outside itself.
+
+Every pin takes an ``Oracle`` instance and raises ``AssertionError`` when the
+oracle disagrees with a closed form, an invariant, a library special case or a
+finite difference.  ``test_oracle.py`` runs them against the real oracle and
+``test_oracle_mutants.py`` runs them against copies of the oracle with one
+plausible mistake planted each, to show that every such mistake is caught.
+
+None of the expected values here come from the oracle or from the CUDA path:
+they are closed forms written with numpy, torch's fp64 CPU reference
+attention, or central differences.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+NONE, TOP_LEFT, BOTTOM_RIGHT = 0, 1, 2
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def cu(lengths):
+    out = [0]
+    for n in lengths:
+        out.append(out[-1] + int(n))
+    return np.array(out, np.int32)
+
+
+def row_count(kind, i, nq, nk):
+    """Closed-form number of allowed keys of zero-based query row i."""
+    if kind == NONE:
+        return nk
+    if kind == TOP_LEFT:
+        return min(i + 1, nk)
+    return max(0, min(i + nk - nq + 1, nk))
+
+
+def allowed_interval(kind, lq, lk):
+    """[(token, key_start, key_end)] for every packed query token: under every
+    rule the allowed keys of a row are a prefix of its own sequence."""
+    out = []
+    cq, ck = cu(lq), cu(lk)
+    for s, (nq, nk) in enumerate(zip(lq, lk)):
+        for i in range(nq):
+            c = row_count(kind, i, nq, nk)
+            out.append((cq[s] + i, ck[s], ck[s] + c))
+    return out
+
+
+def rand_case(rng, lq, lk, hq, hkv, d):
+    tq, tk = sum(lq), sum(lk)
+    q = rng.standard_normal((tq, hq, d))
+    k = rng.standard_normal((tk, hkv, d))
+    v = rng.standard_normal((tk, hkv, d))
+    return q, k, v
+
+
+SHAPES = [  # (lq, lk, hq, hkv, d, kind)
+    ((5, 1, 7), (5, 1, 7), 4, 2, 8, TOP_LEFT),
+    ((3, 6), (8, 2), 2, 1, 4, BOTTOM_RIGHT),  # Nq<Nk and Nq>Nk (empty rows)
+    ((6, 4), (4, 6), 3, 3, 5, TOP_LEFT),      # Nq>Nk top-left
+    ((4, 0, 3), (4, 0, 3), 2, 2, 4, NONE),    # a zero-length segment
+    ((2, 5), (9, 3), 4, 1, 3, BOTTOM_RIGHT),
+]
+
+
+# --------------------------------------------------------------------------
+# mask
+# --------------------------------------------------------------------------
+def pin_token_meta(orc):
+    sid, pos = orc.token_meta(np.array([0, 3, 3, 7], np.int32), 7)
+    assert list(sid) == [0, 0, 0, 2, 2, 2, 2]
+    assert list(pos) == [0, 1, 2, 0, 1, 2, 3]
+
+
+def pin_mask_intervals(orc):
+    """The materialised mask equals, bit for bit, the prefix interval that the
+    closed form of each rule gives, with nothing across sequences."""
+    for lq, lk, _, _, _, kind in SHAPES:
+        for k2 in (NONE, TOP_LEFT, BOTTOM_RIGHT):
+            m = orc.mask(cu(lq), cu(lk), sum(lq), sum(lk), k2)
+            ref = np.zeros_like(m)
+            for t, a, b in allowed_interval(k2, lq, lk):
+                ref[t, a:b] = 1
+            assert np.array_equal(m, ref), (lq, lk, k2)
+
+
+def pin_golden_mask_counts(orc):
+    with open(os.path.join(GOLDEN, "mask_counts.json")) as f:
+        cases = json.load(f)["cases"]
+    kinds = {"top_left": TOP_LEFT, "bottom_right": BOTTOM_RIGHT, "none": NONE}
+    for c in cases:
+        lq, lk = c["seqlens_q"], c["seqlens_k"]
+        m = orc.mask(cu(lq), cu(lk), sum(lq), sum(lk), kinds[c["mask"]])
+        assert int(m.sum(dtype=np.int64)) == c["pairs_per_head"], c["name"]
+        assert int((m.sum(axis=1) == 0).sum()) == c["empty_rows_per_head"], c["name"]
+
+
+# --------------------------------------------------------------------------
+# forward: hand cases ("attention-algorithm-error-and-complexity-tests",
+# first paragraph)
+# --------------------------------------------------------------------------
+def pin_uniform_logits(orc):
+    """Q = 0: every allowed logit is 0, so O_i is the mean of the allowed V
+    rows and lse_i = ln |A_i|; empty rows give exact zeros and -inf."""
+    rng = np.random.default_rng(1)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        q[:] = 0.0
+        o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), 0.37, kind)
+        g = hq // hkv
+        for t, a, b in allowed_interval(kind, lq, lk):
+            for h in range(hq):
+                if b == a:
+                    assert np.all(o[t, h] == 0.0) and lse[h, t] == -math.inf
+                else:
+                    ref = v[a:b, h // g].mean(axis=0)
+                    np.testing.assert_allclose(o[t, h], ref, rtol=1e-12, atol=1e-12)
+                    assert abs(lse[h, t] - math.log(b - a)) < 1e-12
+
+
+def _dominant_case(n_keys, big, d=4, scale=0.5):
+    """One query whose score against key jstar is ``big`` and 0 against the
+    others (orthogonal keys)."""
+    rng = np.random.default_rng(2)
+    q = np.zeros((1, 1, d))
+    q[0, 0, 0] = 1.0
+    k = rng.standard_normal((n_keys, 1, d))
+    k[:, 0, 0] = 0.0
+    jstar = n_keys // 2
+    k[jstar, 0, 0] = big / scale
+    v = rng.standard_normal((n_keys, 1, d))
+    return q, k, v, jstar, scale
+
+
+def pin_single_dominant_score(orc):
+    """One score L above the rest: O = (e^L v* + sum_other v) / (e^L + n - 1).
+    L = 800 overflows exp in fp64 unless the row max is subtracted first."""
+    for big in (3.0, 800.0):
+        n = 6
+        q, k, v, js, scale = _dominant_case(n, big)
+        o, lse = orc.fwd(q, k, v, cu([1]), cu([n]), scale, NONE)
+        w = math.exp(-big)  # weights relative to e^L
+        others = [j for j in range(n) if j != js]
+        ref = (v[js, 0] + w * v[others, 0].sum(axis=0)) / (1.0 + (n - 1) * w)
+        np.testing.assert_allclose(o[0, 0], ref, rtol=1e-12, atol=1e-12)
+        assert abs(lse[0, 0] - (big + math.log1p((n - 1) * w))) < 1e-12
+
+
+def pin_masked_dominant_score(orc):
+    """A huge score on a masked key (a future key under top-left, or a key of
+    another packed sequence) must be excluded before the max and the
+    denominator: the row stays the uniform mean of its allowed keys."""
+    d, scale = 4, 0.5
+    rng = np.random.default_rng(3)
+    lq = lk = (4, 5)
+    q = np.zeros((9, 1, d))
+    q[:, 0, 0] = 1.0
+    k = rng.standard_normal((9, 1, d))
+    k[:, 0, 0] = 0.0
+    v = rng.standard_normal((9, 1, d))
+    k[3, 0, 0] = 1000.0 / scale  # last key of sequence 0: future for rows 0..2
+    k[8, 0, 0] = 1000.0 / scale  # last key of sequence 1
+    o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), scale, TOP_LEFT)
+    for t, a, b in allowed_interval(TOP_LEFT, lq, lk):
+        if t in (3, 8):
+            continue  # these rows do see the dominant key
+        np.testing.assert_allclose(o[t, 0], v[a:b, 0].mean(axis=0), rtol=1e-12, atol=1e-12)
+        assert abs(lse[0, t] - math.log(b - a)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# forward: invariants (third paragraph of the same page)
+# --------------------------------------------------------------------------
+def pin_row_shift(orc):
+    """K + 1 w^T adds scale * q_i . w to every logit of row i: O unchanged,
+    lse shifted by exactly that amount."""
+    rng = np.random.default_rng(4)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        w = rng.standard_normal(d)
+        scale = 0.41
+        o0, l0 = orc.fwd(q, k, v, cu(lq), cu(lk), scale, kind)
+        o1, l1 = orc.fwd(q, k + w, v, cu(lq), cu(lk), scale, kind)
+        np.testing.assert_allclose(o1, o0, rtol=1e-9, atol=1e-10)
+        shift = scale * np.einsum("thd,d->ht", q, w)
+        fin = np.isfinite(l0)
+        assert np.array_equal(fin, np.isfinite(l1))
+        np.testing.assert_allclose(l1[fin], l0[fin] + shift[fin], rtol=1e-10, atol=1e-10)
+
+
+def pin_permutation_noncausal(orc):
+    """Permuting keys and values together inside each sequence leaves every
+    noncausal row unchanged."""
+    rng = np.random.default_rng(5)
+    lq, lk = (3, 6), (7, 5)
+    q, k, v = rand_case(rng, lq, lk, 2, 1, 6)
+    ck = cu(lk)
+    perm = np.concatenate([ck[s] + rng.permutation(n) for s, n in enumerate(lk)])
+    o0, l0 = orc.fwd(q, k, v, cu(lq), ck, 0.3, NONE)
+    o1, l1 = orc.fwd(q, k[perm], v[perm], cu(lq), ck, 0.3, NONE)
+    np.testing.assert_allclose(o1, o0, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(l1, l0, rtol=1e-12, atol=1e-12)
+
+
+def pin_gqa_vs_repeat(orc):
+    """Shared KV heads equal K/V explicitly repeated by the contiguous
+    grouping h -> h // (Hq/Hkv), forward and gradients (dK, dV summed over
+    each group)."""
+    rng = np.random.default_rng(6)
+    lq = lk = (5, 3)
+    hq, hkv, d = 6, 2, 4
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    do = rng.standard_normal(q.shape)
+    g = hq // hkv
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    a = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, TOP_LEFT)
+    b = orc.bwd(q, kr, vr, do, cu(lq), cu(lk), 0.5, TOP_LEFT)
+    np.testing.assert_allclose(a[3], b[3], rtol=1e-12, atol=1e-12)  # O
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-10, atol=1e-12)  # dQ
+    dk_sum = b[1].reshape(-1, hkv, g, d).sum(axis=2)
+    dv_sum = b[2].reshape(-1, hkv, g, d).sum(axis=2)
+    np.testing.assert_allclose(a[1], dk_sum, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(a[2], dv_sum, rtol=1e-10, atol=1e-12)
+
+
+def pin_packed_vs_separate(orc):
+    """A packed batch equals each sequence run alone, outputs and gradients
+    gathered back to packed storage order ("causal-mask-and-ragged-sequence-
+    layouts", second and fifth paragraphs)."""
+    rng = np.random.default_rng(7)
+    for kind in (TOP_LEFT, BOTTOM_RIGHT):
+        lq, lk = (4, 2, 5), (6, 2, 3)
+        q, k, v = rand_case(rng, lq, lk, 2, 1, 4)
+        do = rng.standard_normal(q.shape)
+        packed = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.6, kind)
+        cq, ck = cu(lq), cu(lk)
+        for s in range(len(lq)):
+            qs, ks = slice(cq[s], cq[s + 1]), slice(ck[s], ck[s + 1])
+            one = orc.bwd(q[qs], k[ks], v[ks], do[qs], cu([lq[s]]), cu([lk[s]]), 0.6, kind)
+            np.testing.assert_allclose(packed[3][qs], one[3], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(packed[4][:, qs], one[4], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(packed[0][qs], one[0], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(packed[1][ks], one[1], rtol=1e-11, atol=1e-13)
+            np.testing.assert_allclose(packed[2][ks], one[2], rtol=1e-11, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# library special case: torch's fp64 CPU reference attention with an explicit
+# boolean mask ("causal-mask-and-ragged-sequence-layouts", fourth paragraph)
+# --------------------------------------------------------------------------
+def pin_torch_sdpa_fp64(orc):
+    rng = np.random.default_rng(8)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        scale = 1.0 / math.sqrt(d)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind)
+        g = hq // hkv
+        cq, ck = cu(lq), cu(lk)
+        for s, (nq, nk) in enumerate(zip(lq, lk)):
+            if nq == 0:
+                continue
+            rows = [i for i in range(nq) if row_count(kind, i, nq, nk) > 0]
+            mask = np.zeros((nq, nk), bool)
+            for i in range(nq):
+                mask[i, :row_count(kind, i, nq, nk)] = True
+            qs = torch.tensor(q[cq[s]:cq[s + 1]].transpose(1, 0, 2), requires_grad=True)
+            ks = torch.tensor(k[ck[s]:ck[s + 1]].transpose(1, 0, 2), requires_grad=True)
+            vs = torch.tensor(v[ck[s]:ck[s + 1]].transpose(1, 0, 2), requires_grad=True)
+            kr = ks.repeat_interleave(g, dim=0)
+            vr = vs.repeat_interleave(g, dim=0)
+            if not rows:
+                continue
+            ri = torch.tensor(rows)
+            out = torch.nn.functional.scaled_dot_product_attention(
+                qs[:, ri], kr, vr, attn_mask=torch.tensor(mask[rows]), scale=scale)
+            dot = torch.tensor(do[cq[s]:cq[s + 1]].transpose(1, 0, 2))[:, ri]
+            (out * dot).sum().backward()
+            ref_o = out.detach().numpy().transpose(1, 0, 2)
+            got_o = o[cq[s]:cq[s + 1]][rows]
+            np.testing.assert_allclose(got_o, ref_o, rtol=1e-10, atol=1e-12)
+            got_dq = dq[cq[s]:cq[s + 1]][rows]
+            ref_dq = qs.grad.numpy().transpose(1, 0, 2)[rows]
+            np.testing.assert_allclose(got_dq, ref_dq, rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dk[ck[s]:ck[s + 1]], ks.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dv[ck[s]:ck[s + 1]], vs.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+
+
+# --------------------------------------------------------------------------
+# backward ("attention-algorithm-error-and-complexity-tests", fourth paragraph)
+# --------------------------------------------------------------------------
+def pin_finite_differences(orc):
+    """Central differences of L = sum O * dO on a tiny smooth case (the mask
+    does not depend on the values, so no step crosses a discontinuity)."""
+    rng = np.random.default_rng(9)
+    lq, lk = (3, 4), (3, 5)
+    hq, hkv, d, scale = 2, 1, 3, 0.7
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    do = rng.standard_normal(q.shape)
+    kind = BOTTOM_RIGHT
+    dq, dk, dv, _, _ = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind)
+
+    def loss(qq, kk, vv):
+        o, _ = orc.fwd(qq, kk, vv, cu(lq), cu(lk), scale, kind)
+        return float((o * do).sum())
+
+    h = 1e-5
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xs = []
+            for sign in (1.0, -1.0):
+                xx = x.copy()
+                xx[idx] += sign * h
+                xs.append({"q": (xx, k, v), "k": (q, xx, v), "v": (q, k, xx)}[name])
+            fd[idx] = (loss(*xs[0]) - loss(*xs[1])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def pin_dv_column_sum(orc):
+    """Softmax rows sum to one, so sum_j dV_j of a KV head equals the sum of
+    dO over every non-empty row of its query heads."""
+    rng = np.random.default_rng(10)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind)
+        g = hq // hkv
+        nonempty = np.zeros((sum(lq), hq), bool)
+        for t, a, b in allowed_interval(kind, lq, lk):
+            nonempty[t, :] = b > a
+        for hk in range(hkv):
+            ref = np.zeros(d)
+            for h in range(hk * g, hk * g + g):
+                ref += do[nonempty[:, h], h].sum(axis=0)
+            np.testing.assert_allclose(dv[:, hk].sum(axis=0), ref, rtol=1e-10, atol=1e-10)
+
+
+def pin_dq_key_shift(orc):
+    """Each row of dS sums to zero (softmax Jacobian), so adding a common
+    vector to every key leaves dQ unchanged."""
+    rng = np.random.default_rng(11)
+    lq, lk, hq, hkv, d, kind = SHAPES[0]
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    do = rng.standard_normal(q.shape)
+    w = rng.standard_normal(d)
+    a = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind)
+    b = orc.bwd(q, k + w, v, do, cu(lq), cu(lk), 0.5, kind)
+    np.testing.assert_allclose(b[0], a[0], rtol=1e-8, atol=1e-10)
+
+
+def pin_scale_identity(orc):
+    """L depends on Q and K only through Q K^T, so d/da L(aQ) = d/da L(aK) at
+    a = 1: sum <dQ, Q> = sum <dK, K>."""
+    rng = np.random.default_rng(12)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        dq, dk, dv, _, _ = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.45, kind)
+        a, b = float((dq * q).sum()), float((dk * k).sum())
+        assert abs(a - b) <= 1e-10 * max(1.0, abs(a)), (a, b)
+
+
+def pin_empty_rows_backward(orc):
+    """All-masked rows (bottom-right, Nq > Nk) have zero dQ and add nothing
+    to dK/dV: zeroing their dO changes no gradient."""
+    rng = np.random.default_rng(13)
+    lq, lk = (6,), (2,)
+    q, k, v = rand_case(rng, lq, lk, 2, 1, 4)
+    do = rng.standard_normal(q.shape)
+    dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, BOTTOM_RIGHT)
+    empty = [i for i in range(6) if row_count(BOTTOM_RIGHT, i, 6, 2) == 0]
+    assert empty == [0, 1, 2, 3]
+    assert np.all(dq[empty] == 0.0) and np.all(o[empty] == 0.0)
+    assert np.all(lse[:, empty] == -math.inf)
+    do2 = do.copy()
+    do2[empty] = 0.0
+    _, dk2, dv2, _, _ = orc.bwd(q, k, v, do2, cu(lq), cu(lk), 0.5, BOTTOM_RIGHT)
+    assert np.array_equal(dk, dk2) and np.array_equal(dv, dv2)
+
+
+ALL_PINS = [
+    pin_token_meta, pin_mask_intervals, pin_golden_mask_counts,
+    pin_uniform_logits, pin_single_dominant_score, pin_masked_dominant_score,
+    pin_row_shift, pin_permutation_noncausal, pin_gqa_vs_repeat,
+    pin_packed_vs_separate, pin_torch_sdpa_fp64, pin_finite_differences,
+    pin_dv_column_sum, pin_dq_key_shift, pin_scale_identity,
+    pin_empty_rows_backward,
+]

@@ -1,0 +1,223 @@
+"""Python binding of the C ABI in ``include/attn.h`` (ctypes).
+
+Argument marshalling only: this module checks tensor shapes and dtypes,
+allocates outputs and workspace through PyTorch's caching allocator, and passes
+raw device pointers and the current CUDA stream to the library.  Every step of
+the attention itself runs in the library's CUDA kernels; there is no other
+implementation behind these functions, and they raise if the library is
+missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MASK_NONE = 0
+CAUSAL_TOP_LEFT = 1
+CAUSAL_BOTTOM_RIGHT = 2
+DTYPE_BF16 = 0
+DTYPE_FP32 = 1
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
+          4: "CUDA error", 5: "device wait timed out", 6: "cu_seqlens out of bounds"}
+
+_SYMBOLS = ["attn_fwd", "attn_bwd", "attn_fwd_workspace_size", "attn_bwd_workspace_size",
+            "attn_mask_probe", "attn_get_device_error", "attn_status_string",
+            "attn_last_plan", "attn_version"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: status {status} ({STATUS.get(status, '?')})")
+        self.status = status
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load the in-tree CUDA library (built by ``build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA attention library not built: {path} is missing "
+                           "(run exact_tiled_attention_online_gb300.build.build())")
+    L = ctypes.CDLL(path)
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.argtypes = [P, P, P, P, P, P, P, P] + [I] * 8 + [F, I, I, P, SZ, P]
+    L.attn_fwd.restype = I
+    L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, P, SZ, P]
+    L.attn_bwd.restype = I
+    L.attn_fwd_workspace_size.argtypes = [I] * 8
+    L.attn_fwd_workspace_size.restype = SZ
+    L.attn_bwd_workspace_size.argtypes = [I] * 9
+    L.attn_bwd_workspace_size.restype = SZ
+    L.attn_mask_probe.argtypes = [P, P] + [I] * 7 + [P, P]
+    L.attn_mask_probe.restype = I
+    L.attn_get_device_error.argtypes = [P]
+    L.attn_get_device_error.restype = I
+    L.attn_status_string.argtypes = [I]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_last_plan.argtypes = []
+    L.attn_last_plan.restype = ctypes.c_char_p
+    L.attn_version.argtypes = []
+    L.attn_version.restype = I
+    _lib = L
+    return L
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32 expected")
+
+
+def _check(t: torch.Tensor, name: str, dims: int):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code) -> int:
+    n = library().attn_fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code)
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError("attn_fwd_workspace_size", 1)
+    return n
+
+
+def bwd_workspace_size(batch, max_q, max_k, total_q, total_k, hq, hkv, d, dtype_code) -> int:
+    n = library().attn_bwd_workspace_size(batch, max_q, max_k, total_q, total_k, hq, hkv, d,
+                                          dtype_code)
+    if n == ctypes.c_size_t(-1).value:
+        raise AttnError("attn_bwd_workspace_size", 1)
+    return n
+
+
+def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+        mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
+        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+        workspace: Optional[torch.Tensor] = None, stream=None, want_lse: bool = True,
+        o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False):
+    """Attention forward on packed ragged tensors (layouts in include/attn.h).
+
+    Returns (o, lse), or (o, lse, o_f32) when ``want_o_f32`` is set or an
+    ``o_f32`` buffer is given.  lse is [n_heads_q, total_q] fp32 (None when
+    ``want_lse`` is False and no ``lse`` buffer is given); o_f32 is the fp32
+    output before rounding, which ``bwd`` uses for the D term.
+    """
+    _check(q, "q", 3), _check(k, "k", 3), _check(v, "v", 3)
+    _check(cu_seqlens_q, "cu_seqlens_q", 1), _check(cu_seqlens_k, "cu_seqlens_k", 1)
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share a dtype")
+    total_q, hq, d = q.shape
+    total_k, hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
+    ret_f32 = want_o_f32 or o_f32 is not None
+    if o_f32 is None and want_o_f32:
+        o_f32 = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    ws_bytes = fwd_workspace_size(batch, max_seqlen_q, max_seqlen_k, total_q, hq, hkv, d, dt)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = library().attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(o_f32), _ptr(cu_seqlens_q),
+        _ptr(cu_seqlens_k),
+        batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv, d, float(scale),
+        int(mask), dt, _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream))
+    if st != 0:
+        raise AttnError("attn_fwd", st)
+    return (out, lse, o_f32) if ret_f32 else (out, lse)
+
+
+def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+        max_seqlen_k: int, mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
+        dq=None, dk=None, dv=None, workspace=None, stream=None,
+        o_f32: Optional[torch.Tensor] = None):
+    """Attention backward; returns (dq, dk, dv) with dk/dv summed over each
+    KV head's group of query heads.  Pass the forward's ``o_f32`` when it was
+    kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n, 3)
+    _check(lse, "lse", 2)
+    dt = _dtype_code(q)
+    total_q, hq, d = q.shape
+    total_k, hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = bwd_workspace_size(batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv,
+                                  d, dt)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = library().attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_f32), _ptr(dout), _ptr(dq),
+        _ptr(dk), _ptr(dv),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, max_seqlen_q, max_seqlen_k, total_q,
+        total_k, hq, hkv, d, float(scale), int(mask), dt, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
+    if st != 0:
+        raise AttnError("attn_bwd", st)
+    return dq, dk, dv
+
+
+def mask_probe(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k,
+               mask, tile_rows=128, stream=None) -> torch.Tensor:
+    out = torch.empty((total_q, total_k), dtype=torch.uint8, device=cu_seqlens_q.device)
+    st = library().attn_mask_probe(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                   cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
+                                   total_q, total_k, int(mask), int(tile_rows), _ptr(out),
+                                   _stream(stream))
+    if st != 0:
+        raise AttnError("attn_mask_probe", st)
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    return library().attn_get_device_error(_stream(stream))
+
+
+def last_plan() -> str:
+    return library().attn_last_plan().decode()
+
+
+def status_string(code: int) -> str:
+    return library().attn_status_string(code).decode()

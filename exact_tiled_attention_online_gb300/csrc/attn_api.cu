@@ -1,0 +1,253 @@
+// attn_api.cu -- the C ABI declared in include/attn.h: argument validation,
+// plan selection, workspace carving and kernel launches.  Nothing here
+// allocates memory; every buffer is the caller's.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace attn {
+
+cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t st);
+cudaError_t launch_bwd_simt(const BwdParams &p, attn_dtype dtype, cudaStream_t st);
+cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st,
+                          char *desc, size_t desc_len);
+cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
+cudaError_t launch_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
+                              int max_k, int total_q, int total_k, int mask, int tile_rows,
+                              uint8_t *out, int *err, cudaStream_t st);
+
+// The per-device error flag.  Device code reaches it through a pointer kernel
+// argument; the host looks its address up once per device.
+__device__ int g_device_error;
+
+static int *device_error_ptr() {
+  static int *cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int *>(ptr);
+  }
+  return cache[dev];
+}
+
+static thread_local char t_plan[512] = "none";
+
+static void set_plan(const char *s) {
+  snprintf(t_plan, sizeof(t_plan), "%s", s);
+}
+
+// ---------------------------------------------------------------------------
+// Validation shared by every entry point.
+// ---------------------------------------------------------------------------
+static attn_status check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
+                               int hq, int hkv, int d, int mask, int dtype) {
+  if (batch < 0 || max_q < 0 || max_k < 0 || total_q < 0 || total_k < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (hq > 65535 || hkv > 65535 || batch > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (mask < ATTN_MASK_NONE || mask > ATTN_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (max_q > total_q || max_k > total_k) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char *attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head_dim, dtype or size";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait expired";
+    case ATTN_ERR_DEVICE_BOUNDS: return "cu_seqlens inconsistent with the sizes passed";
+  }
+  return "unknown status";
+}
+
+const char *attn_last_plan(void) { return t_plan; }
+
+size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int hq, int hkv,
+                               int d, attn_dtype dtype) {
+  if (check_sizes(batch, max_q, max_k, total_q, max_k, hq, hkv, d, ATTN_MASK_NONE, dtype) !=
+      ATTN_OK)
+    return (size_t)-1;
+  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, dtype, sm_count());
+  if (plan.kind != PLAN_TC_SPLIT) return 0;
+  return fwd_split_workspace(plan, total_q, hq, d);
+}
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                     float *o_f32, const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
+                     int total_q, int total_k, int hq, int hkv, int d, float scale,
+                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+  if (st != ATTN_OK) return st;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
+  if (total_q > 0 && (!q || !o)) return ATTN_ERR_INVALID_ARG;
+  if (total_k > 0 && (!k || !v)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.o_f32 = o_f32;
+  p.cu_q = cu_q; p.cu_k = cu_k;
+  p.batch = batch; p.max_q = max_q; p.max_k = max_k; p.total_q = total_q; p.total_k = total_k;
+  p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
+  p.mask = mask;
+  p.err = device_error_ptr();
+  if (!p.err) return ATTN_ERR_CUDA;
+  if (batch == 0 || total_q == 0 || max_q == 0) {
+    set_plan("empty");
+    return ATTN_OK;
+  }
+  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, dtype, sm_count());
+  if (plan.kind != PLAN_SIMT) {
+    // TMA needs 16-byte aligned tensors; with no keys at all every row is
+    // empty and the CUDA-core kernel writes the zeros and -inf directly.
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if (mis & 15) return ATTN_ERR_INVALID_ARG;
+    if (total_k == 0) plan.kind = PLAN_SIMT;
+    const long long gz = (long long)batch * plan.n_splits;
+    if (gz > 65535) return ATTN_ERR_UNSUPPORTED;
+  }
+  char desc[384];
+  cudaError_t ce;
+  if (plan.kind == PLAN_SIMT) {
+    ce = launch_fwd_simt(p, dtype, cs);
+    snprintf(desc, sizeof(desc), "fwd_simt_%s_d%d grid=(%d,%d,%d)",
+             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d, (max_q + 3) / 4, hq, batch);
+  } else {
+    if (plan.kind == PLAN_TC_SPLIT) {
+      size_t need = fwd_split_workspace(plan, total_q, hq, d);
+      if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+      if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_INVALID_ARG;
+      p.o_part = static_cast<float *>(workspace);
+      p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             align256((size_t)plan.n_splits * total_q * hq * d * 4));
+      p.n_splits = plan.n_splits;
+    }
+    ce = launch_fwd_tc(p, plan, cs, desc, sizeof(desc));
+    if (ce == cudaSuccess && plan.kind == PLAN_TC_SPLIT) ce = launch_combine(p, plan, cs);
+  }
+  set_plan(desc);
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_size(int batch, int max_q, int max_k, int total_q, int total_k,
+                               int hq, int hkv, int d, attn_dtype dtype) {
+  if (check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, ATTN_MASK_NONE, dtype) !=
+      ATTN_OK)
+    return (size_t)-1;
+  size_t acc = align256((size_t)total_q * hq * d * 4);
+  size_t rows = align256((size_t)hq * total_q * 4);
+  return acc + 2 * rows;
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const float *o_f32, const void *dout, void *dq, void *dk, void *dv,
+                     const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
+                     int total_q, int total_k, int hq, int hkv, int d, float scale,
+                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+  if (st != ATTN_OK) return st;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
+  if (total_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_INVALID_ARG;
+  if (total_k > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  size_t need = attn_bwd_workspace_size(batch, max_q, max_k, total_q, total_k, hq, hkv, d, dtype);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  BwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse; p.o_f32 = o_f32;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.cu_q = cu_q; p.cu_k = cu_k;
+  p.batch = batch; p.max_q = max_q; p.max_k = max_k; p.total_q = total_q; p.total_k = total_k;
+  p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
+  p.mask = mask;
+  p.err = device_error_ptr();
+  if (!p.err) return ATTN_ERR_CUDA;
+  char *ws = static_cast<char *>(workspace);
+  size_t acc = align256((size_t)total_q * hq * d * 4);
+  size_t rows = align256((size_t)hq * total_q * 4);
+  p.dq_acc = reinterpret_cast<float *>(ws);
+  p.delta = reinterpret_cast<float *>(ws + acc);
+  p.lse2 = reinterpret_cast<float *>(ws + acc + rows);
+  if (batch == 0) {
+    set_plan("empty");
+    return ATTN_OK;
+  }
+  // Keys of no sequence (none when cu_k[batch] == total_k) and rows beyond
+  // max_k are covered by the kernels; a zero fill first keeps dk/dv defined
+  // even when the device flags inconsistent cu_seqlens.
+  cudaError_t ce = cudaSuccess;
+  if (total_k > 0) {
+    size_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+    ce = cudaMemsetAsync(dk, 0, (size_t)total_k * hkv * d * es, cs);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(dv, 0, (size_t)total_k * hkv * d * es, cs);
+  }
+  if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);
+  char desc[256];
+  snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d",
+           dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d);
+  set_plan(desc);
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
+                            int max_k, int total_q, int total_k, attn_mask_kind mask,
+                            int tile_rows, uint8_t *out, void *stream) {
+  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, 1, 1, 64, mask,
+                               ATTN_DTYPE_BF16);
+  if (st != ATTN_OK) return st;
+  if (tile_rows != 16 && tile_rows != 32 && tile_rows != 64 && tile_rows != 128)
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)total_q * total_k >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
+  if ((long long)total_q * total_k > 0 && !out) return ATTN_ERR_INVALID_ARG;
+  int *err = device_error_ptr();
+  if (!err) return ATTN_ERR_CUDA;
+  if ((long long)total_q * total_k == 0) return ATTN_OK;
+  cudaError_t ce = launch_mask_probe(cu_q, cu_k, batch, max_q, max_k, total_q, total_k, mask,
+                                     tile_rows, out, err, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_get_device_error(void *stream) {
+  int *flag = device_error_ptr();
+  if (!flag) return ATTN_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return static_cast<attn_status>(v);
+}
+
+}  // extern "C"

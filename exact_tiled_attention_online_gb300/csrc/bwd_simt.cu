@@ -1,0 +1,179 @@
+// bwd_simt.cu -- CUDA-core backward (recompute form).
+//
+//   pre:  D_i = dO_i . O_i and lse in log2 units per (row, head);
+//   dq:   one warp per (query row, head) walks the row's allowed keys,
+//         recomputes P_ij = 2^(c s_ij - lse2_i), dS_ij = P_ij (dO_i.v_j - D_i)
+//         and sums dQ_i = scale sum_j dS_ij k_j;
+//   dkdv: one warp per (key, KV head) walks every query head of its group
+//         and every row allowed to see the key, summing
+//         dK_j = scale sum dS_ij q_i and dV_j = sum P_ij dO_i, so the GQA sum
+//         over shared heads happens in registers.
+// The same per-row key bound as the forward decides every pair
+// ("causal-mask-and-ragged-sequence-layouts", sixth paragraph: backward
+// recomputation rebuilds the same mask).  No atomics: each output row has one
+// owner warp, so the result is deterministic.
+#include "common.cuh"
+
+namespace attn {
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + warp;  // t * hq + h
+  if (row >= (long long)p.total_q * p.hq) return;
+  const int t = (int)(row / p.hq), h = (int)(row % p.hq);
+  const T *op = reinterpret_cast<const T *>(p.o) + (size_t)row * D + lane * E;
+  const T *dp = reinterpret_cast<const T *>(p.dout) + (size_t)row * D + lane * E;
+  float part = 0.f;
+  if (p.o_f32) {
+    const float *of = p.o_f32 + (size_t)row * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e++) part += of[e] * Elem<T>::to_f(dp[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; e++) part += Elem<T>::to_f(op[e]) * Elem<T>::to_f(dp[e]);
+  }
+  const float D_i = warp_sum(part);
+  if (lane == 0) {
+    const float l = p.lse[(size_t)h * p.total_q + t];
+    p.delta[(size_t)h * p.total_q + t] = D_i;
+    // An empty row (lse = -inf) gets +inf so that 2^(s - lse2) = 0.
+    p.lse2[(size_t)h * p.total_q + t] = l == -INFINITY ? INFINITY : l * kLog2e;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, h = blockIdx.y;
+  const int i = blockIdx.x * 4 + warp;
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (i >= g.nq) return;
+  const int hk = h / (p.hq / p.hkv);
+  const int t = g.q0 + i;
+  const size_t row = (size_t)t * p.hq + h;
+  const T *qp = reinterpret_cast<const T *>(p.q) + row * D + lane * E;
+  const T *dop = reinterpret_cast<const T *>(p.dout) + row * D + lane * E;
+  float qf[E], dof[E], dq[E];
+#pragma unroll
+  for (int e = 0; e < E; e++) {
+    qf[e] = Elem<T>::to_f(qp[e]) * p.scale_log2;
+    dof[e] = Elem<T>::to_f(dop[e]);
+    dq[e] = 0.f;
+  }
+  const float lse2 = p.lse2[(size_t)h * p.total_q + t];
+  const float D_i = p.delta[(size_t)h * p.total_q + t];
+  const int kend = key_end(g.mask, i, g.nq, g.nk);
+  const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
+  const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
+  const size_t stride = (size_t)p.hkv * D;
+  for (int j = 0; j < kend; j++) {
+    float kf[E], ps = 0.f, pd = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      kf[e] = Elem<T>::to_f(kb[j * stride + e]);
+      ps += qf[e] * kf[e];
+      pd += dof[e] * Elem<T>::to_f(vb[j * stride + e]);
+    }
+    const float sc = warp_sum(ps), dpij = warp_sum(pd);
+    const float pij = fast_exp2(sc - lse2);
+    const float ds = pij * (dpij - D_i);
+#pragma unroll
+    for (int e = 0; e < E; e++) dq[e] += ds * kf[e];
+  }
+  T *out = reinterpret_cast<T *>(p.dq) + row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e++) out[e] = Elem<T>::from_f(dq[e] * p.scale);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, hk = blockIdx.y;
+  const int j = blockIdx.x * 4 + warp;  // in-sequence key
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (j >= g.nk) return;
+  const int grp = p.hq / p.hkv;
+  const size_t krow = ((size_t)(g.k0 + j)) * p.hkv + hk;
+  const T *kp = reinterpret_cast<const T *>(p.k) + krow * D + lane * E;
+  const T *vp = reinterpret_cast<const T *>(p.v) + krow * D + lane * E;
+  float kf[E], vf[E], dk[E], dv[E];
+#pragma unroll
+  for (int e = 0; e < E; e++) {
+    kf[e] = Elem<T>::to_f(kp[e]) * p.scale_log2;
+    vf[e] = Elem<T>::to_f(vp[e]);
+    dk[e] = 0.f;
+    dv[e] = 0.f;
+  }
+  const int i_begin = row_begin(g.mask, j, g.nq, g.nk);
+  for (int h = hk * grp; h < hk * grp + grp; h++) {
+    for (int i = i_begin; i < g.nq; i++) {
+      const int t = g.q0 + i;
+      const size_t row = (size_t)t * p.hq + h;
+      const T *qp = reinterpret_cast<const T *>(p.q) + row * D + lane * E;
+      const T *dop = reinterpret_cast<const T *>(p.dout) + row * D + lane * E;
+      float qf[E], dof[E], ps = 0.f, pd = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; e++) {
+        qf[e] = Elem<T>::to_f(qp[e]);
+        dof[e] = Elem<T>::to_f(dop[e]);
+        ps += qf[e] * kf[e];
+        pd += dof[e] * vf[e];
+      }
+      const float sc = warp_sum(ps), dpij = warp_sum(pd);
+      const float lse2 = p.lse2[(size_t)h * p.total_q + t];
+      const float D_i = p.delta[(size_t)h * p.total_q + t];
+      const float pij = fast_exp2(sc - lse2);
+      const float ds = pij * (dpij - D_i);
+#pragma unroll
+      for (int e = 0; e < E; e++) {
+        dk[e] += ds * qf[e];
+        dv[e] += pij * dof[e];
+      }
+    }
+  }
+  T *dkp = reinterpret_cast<T *>(p.dk) + krow * D + lane * E;
+  T *dvp = reinterpret_cast<T *>(p.dv) + krow * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e++) {
+    dkp[e] = Elem<T>::from_f(dk[e] * p.scale);
+    dvp[e] = Elem<T>::from_f(dv[e]);
+  }
+}
+
+template <typename T, int D>
+static void launch_all(const BwdParams &p, cudaStream_t st) {
+  const long long rows = (long long)p.total_q * p.hq;
+  if (rows > 0) bwd_pre_kernel<T, D><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p);
+  if (p.max_q > 0)
+    bwd_dq_simt_kernel<T, D><<<dim3((p.max_q + 3) / 4, p.hq, p.batch), 128, 0, st>>>(p);
+  if (p.max_k > 0)
+    bwd_dkdv_simt_kernel<T, D><<<dim3((p.max_k + 3) / 4, p.hkv, p.batch), 128, 0, st>>>(p);
+}
+
+cudaError_t launch_bwd_simt(const BwdParams &p, attn_dtype dtype, cudaStream_t st) {
+  if (p.batch == 0) return cudaSuccess;
+  if (dtype == ATTN_DTYPE_FP32) {
+    if (p.d == 64) launch_all<float, 64>(p, st);
+    else launch_all<float, 128>(p, st);
+  } else {
+    if (p.d == 64) launch_all<__nv_bfloat16, 64>(p, st);
+    else launch_all<__nv_bfloat16, 128>(p, st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,174 @@
+// common.cuh -- device helpers shared by every attention kernel: sequence
+// lookup from cumulative lengths, the alignment rule as a per-row key bound,
+// the device error flag, bf16 conversions and bounded mbarrier waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// Sequence geometry ("causal-mask-and-ragged-sequence-layouts", first and
+// third paragraphs).  Every alignment rule allows, for query row i of a
+// sequence, a prefix of that sequence's keys: j < key_end(i).  Tiles take
+// in-sequence coordinates (row i, key j) before any comparison, so a packed
+// global offset never becomes a position.
+// ---------------------------------------------------------------------------
+struct SeqGeom {
+  int q0, nq;  // first packed query token, number of queries
+  int k0, nk;  // first packed key token, number of keys
+  int mask;    // attn_mask_kind
+  bool ok;     // cu_seqlens consistent with the sizes passed
+};
+
+__device__ __forceinline__ SeqGeom load_seq(const int32_t *__restrict__ cu_q,
+                                            const int32_t *__restrict__ cu_k,
+                                            int s, int total_q, int total_k,
+                                            int max_q, int max_k, int mask) {
+  SeqGeom g;
+  g.q0 = __ldg(cu_q + s);
+  int q1 = __ldg(cu_q + s + 1);
+  g.k0 = __ldg(cu_k + s);
+  int k1 = __ldg(cu_k + s + 1);
+  g.nq = q1 - g.q0;
+  g.nk = k1 - g.k0;
+  g.mask = mask;
+  g.ok = g.q0 >= 0 && g.k0 >= 0 && g.nq >= 0 && g.nk >= 0 && q1 <= total_q &&
+         k1 <= total_k && g.nq <= max_q && g.nk <= max_k;
+  if (!g.ok) {
+    g.nq = 0;
+    g.nk = 0;
+  }
+  return g;
+}
+
+// Shift of the causal diagonal: key j is allowed for row i iff j <= i + off.
+__host__ __device__ __forceinline__ int causal_offset(int mask, int nq, int nk) {
+  return mask == ATTN_CAUSAL_BOTTOM_RIGHT ? nk - nq : 0;
+}
+
+// Exclusive end of the allowed key prefix of in-sequence row i (0 = empty).
+__host__ __device__ __forceinline__ int key_end(int mask, int i, int nq, int nk) {
+  if (mask == ATTN_MASK_NONE) return nk;
+  int e = i + causal_offset(mask, nq, nk) + 1;
+  return e < 0 ? 0 : (e > nk ? nk : e);
+}
+
+// First in-sequence query row that is allowed to see key j (rows below it do
+// not); rows >= nq are out of range.
+__host__ __device__ __forceinline__ int row_begin(int mask, int j, int nq, int nk) {
+  if (mask == ATTN_MASK_NONE) return 0;
+  int b = j - causal_offset(mask, nq, nk);
+  return b < 0 ? 0 : b;
+}
+
+// ---------------------------------------------------------------------------
+// Tile planner.  A tile holds in-sequence query rows [i0, i0 + rows) (rows
+// past nq are out-of-range lanes) against key tiles of bn keys.  Because
+// key_end() is non-decreasing in i, the tile needs key tiles [0, n_end) with
+// n_end from its last in-range row, and key tiles below n_full lie entirely
+// inside the smallest row bound, so they need no per-element mask.
+// ---------------------------------------------------------------------------
+struct KvRange {
+  int n_end;   // key tiles [0, n_end) hold every allowed key of the tile
+  int n_full;  // key tiles [0, n_full) are allowed for every in-range row
+};
+
+__host__ __device__ __forceinline__ KvRange plan_kv_tiles(int mask, int nq, int nk, int i0,
+                                                           int rows, int bn) {
+  KvRange r{0, 0};
+  int i_last = (i0 + rows < nq ? i0 + rows : nq) - 1;
+  if (i_last < i0) return r;
+  int kend_max = key_end(mask, i_last, nq, nk);
+  int kend_min = key_end(mask, i0, nq, nk);
+  r.n_end = (kend_max + bn - 1) / bn;
+  r.n_full = kend_min / bn;
+  return r;
+}
+
+// Key tiles [*a, *b) of split `split` out of n_splits over [0, n_end).
+__host__ __device__ __forceinline__ void split_tiles(int n_end, int split, int n_splits, int *a,
+                                                     int *b) {
+  int per = (n_end + n_splits - 1) / n_splits;
+  int lo = split * per;
+  *a = lo < n_end ? lo : n_end;
+  *b = lo + per < n_end ? lo + per : n_end;
+}
+
+// Per-element predicate for tile lanes on a boundary tile: in-sequence row i,
+// key j.  Out-of-range rows and keys are never allowed.
+__host__ __device__ __forceinline__ bool lane_allowed(int mask, int i, int j, int nq, int nk) {
+  return i < nq && j < key_end(mask, i, nq, nk);
+}
+
+// ---------------------------------------------------------------------------
+// Device error flag: the first error code sticks until the host clears it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_error(int *flag, int code) {
+  if (flag) atomicCAS(flag, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Element access for the two supported element types.
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Kernel launch parameters common to the forward kernels.
+struct FwdParams {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  float *o_f32;  // optional fp32 copy of the output before rounding
+  const int32_t *cu_q, *cu_k;
+  int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
+  float scale, scale_log2;  // scale and scale * log2(e)
+  int mask;
+  int *err;
+  // split-KV partial outputs (NULL when the plan writes o/lse directly)
+  float *o_part, *lse_part;
+  int n_splits;
+};
+
+struct BwdParams {
+  const void *q, *k, *v, *o, *dout;
+  const float *lse;
+  const float *o_f32;  // optional fp32 output of the forward (NULL: use o)
+  void *dq, *dk, *dv;
+  const int32_t *cu_q, *cu_k;
+  int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
+  float scale, scale_log2;
+  int mask;
+  int *err;
+  float *dq_acc;   // [total_q, hq, d] fp32
+  float *delta;    // [hq, total_q]  D_i = dO_i . O_i
+  float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)
+};
+
+}  // namespace attn

@@ -1,0 +1,80 @@
+// fwd_simt.cu -- CUDA-core forward: one warp per (query row, head), the keys
+// of the row's allowed prefix streamed in order through the online-softmax
+// recurrence ("formal-correctness", "The FlashAttention Proof": running max,
+// rescale of denominator and accumulator when the max moves, final divide).
+//
+// This is the fp32 path (fp32 inputs have no tensor-core kind that keeps fp32
+// operands exact) and the small-problem path; each lane owns head_dim/32
+// consecutive features, so every key row is read with one coalesced access
+// and the score is a warp-wide reduction of lane-partial products.
+#include "common.cuh"
+
+namespace attn {
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
+  constexpr int E = D / 32;  // features per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.z, h = blockIdx.y;
+  const int i = blockIdx.x * 4 + warp;  // in-sequence query row
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (i >= g.nq) return;
+  const int hk = h / (p.hq / p.hkv);
+  const int t = g.q0 + i;
+  const T *qp = reinterpret_cast<const T *>(p.q) + ((size_t)t * p.hq + h) * D + lane * E;
+  float qf[E], acc[E];
+#pragma unroll
+  for (int e = 0; e < E; e++) {
+    qf[e] = Elem<T>::to_f(qp[e]) * p.scale_log2;
+    acc[e] = 0.f;
+  }
+  const int kend = key_end(g.mask, i, g.nq, g.nk);
+  float m = -INFINITY, l = 0.f;
+  const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
+  const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
+  const size_t stride = (size_t)p.hkv * D;
+  for (int j = 0; j < kend; j++) {
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * stride + e]);
+    const float sc = warp_sum(part);  // scaled logit in log2 units
+    const float m_new = fmaxf(m, sc);
+    const float alpha = fast_exp2(m - m_new);
+    const float pj = fast_exp2(sc - m_new);
+    l = l * alpha + pj;
+#pragma unroll
+    for (int e = 0; e < E; e++) acc[e] = acc[e] * alpha + pj * Elem<T>::to_f(vb[j * stride + e]);
+    m = m_new;
+  }
+  T *op = reinterpret_cast<T *>(p.o) + ((size_t)t * p.hq + h) * D + lane * E;
+  const float inv = kend > 0 ? 1.f / l : 0.f;
+#pragma unroll
+  for (int e = 0; e < E; e++) op[e] = Elem<T>::from_f(acc[e] * inv);
+  if (p.o_f32) {
+    float *of = p.o_f32 + ((size_t)t * p.hq + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e++) of[e] = acc[e] * inv;
+  }
+  if (p.lse && lane == 0)
+    p.lse[(size_t)h * p.total_q + t] = kend > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t st) {
+  dim3 grid((p.max_q + 3) / 4, p.hq, p.batch), block(128);
+  if (grid.x == 0 || p.batch == 0) return cudaSuccess;
+  if (dtype == ATTN_DTYPE_FP32) {
+    if (p.d == 64) fwd_simt_kernel<float, 64><<<grid, block, 0, st>>>(p);
+    else fwd_simt_kernel<float, 128><<<grid, block, 0, st>>>(p);
+  } else {
+    if (p.d == 64) fwd_simt_kernel<__nv_bfloat16, 64><<<grid, block, 0, st>>>(p);
+    else fwd_simt_kernel<__nv_bfloat16, 128><<<grid, block, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,198 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact tiled attention library.
+ *
+ * The library computes exact scaled-dot-product attention over packed ragged
+ * batches,
+ *
+ *     O = softmax(scale * Q K^T + mask) V,
+ *
+ * tile by tile with the online-softmax recurrence (running max, rescaled
+ * denominator and accumulator, final divide: "formal-correctness", section
+ * "The FlashAttention Proof"), saves the natural-log logsumexp of the scaled
+ * logits per query row, and provides the recompute-based backward (dQ, dK,
+ * dV; GQA gradients summed over each shared KV head:
+ * "attention-algorithm-error-and-complexity-tests", third and fourth
+ * paragraphs).
+ *
+ * Layout ("THD", row-major, contiguous, no padding between tokens):
+ *   q, o, dout, dq : [total_q, n_heads_q,  head_dim]
+ *   k, v, dk, dv   : [total_k, n_heads_kv, head_dim]
+ *   lse            : [n_heads_q, total_q] fp32
+ *   cu_seqlens_q/k : int32 [batch + 1], device memory, cu[0] = 0,
+ *                    non-decreasing, cu[batch] = total.  Sequence s owns
+ *                    tokens cu[s] .. cu[s+1]-1 and its positions restart at
+ *                    0 ("causal-mask-and-ragged-sequence-layouts", first
+ *                    paragraph).  A zero-length sequence and batch = 0 are
+ *                    legal and do nothing.
+ *
+ * Mask rules (same page, third and fourth paragraphs), for zero-based
+ * in-sequence query position i and key position j of one sequence with Nq
+ * queries and Nk keys:
+ *   ATTN_MASK_NONE           every key of the sequence;
+ *   ATTN_CAUSAL_TOP_LEFT     j <= i;
+ *   ATTN_CAUSAL_BOTTOM_RIGHT j <= i + Nk - Nq.
+ * Pairs from different sequences are never allowed; tile lanes past a
+ * sequence's end never enter the max, the denominator or a gradient sum
+ * (same page, second paragraph).  A row with no allowed key gets O = 0 and
+ * lse = -inf, and contributes nothing to the backward.
+ *
+ * GQA: n_heads_q must be a multiple of n_heads_kv; query head h reads KV head
+ * h / (n_heads_q / n_heads_kv) (contiguous grouping).
+ *
+ * Ownership: the caller owns and allocates every buffer (device memory);
+ * the library allocates nothing on any call path.  Every call is
+ * asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ * legacy default stream).  max_seqlen_* and total_* come from the host so no
+ * call synchronises.  Argument errors are returned before anything is
+ * launched.  Errors the device detects (cu_seqlens inconsistent with the
+ * sizes passed, a bounded wait that expired) are recorded in a per-device
+ * flag that attn_get_device_error() reads.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum, ... */
+  ATTN_ERR_UNSUPPORTED = 2,    /* head_dim, dtype or feature not built       */
+  ATTN_ERR_WORKSPACE = 3,      /* workspace missing or smaller than needed   */
+  ATTN_ERR_CUDA = 4,           /* a CUDA runtime call failed                 */
+  ATTN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait expired              */
+  ATTN_ERR_DEVICE_BOUNDS = 6   /* cu_seqlens disagree with the sizes passed  */
+} attn_status;
+
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_CAUSAL_TOP_LEFT = 1,
+  ATTN_CAUSAL_BOTTOM_RIGHT = 2
+} attn_mask_kind;
+
+typedef enum {
+  ATTN_DTYPE_BF16 = 0, /* bf16 inputs/outputs, fp32 accumulation */
+  ATTN_DTYPE_FP32 = 1  /* fp32 inputs/outputs, fp32 arithmetic   */
+} attn_dtype;
+
+/*
+ * Workspace bytes attn_fwd needs for these sizes on the current device (0 when
+ * the chosen plan needs none).  The split-KV decode plan keeps one partial
+ * output row (fp32) and one partial logsumexp per key split in it.  Returns
+ * (size_t)-1 for arguments attn_fwd would reject.
+ */
+size_t attn_fwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
+                               int total_q, int n_heads_q, int n_heads_kv,
+                               int head_dim, attn_dtype dtype);
+
+/*
+ * Forward ("formal-correctness", "The FlashAttention Proof": the online
+ * softmax recurrence; "causal-mask-and-ragged-sequence-layouts": mask rules).
+ *   q, k, v      inputs, layouts above, element type `dtype`.
+ *   o            output [total_q, n_heads_q, head_dim], type `dtype`.
+ *   lse          output [n_heads_q, total_q] fp32, natural log of the sum of
+ *                exp(scale * q.k) over the allowed keys; -inf for empty rows.
+ *                May be NULL when not wanted.
+ *   o_f32        optional output [total_q, n_heads_q, head_dim] fp32: the
+ *                normalised output before its rounding to `dtype`.  Pass it
+ *                on to attn_bwd, which then forms D_i = dO_i . O_i from it;
+ *                with a bf16 O alone, the rounding error of O enters every
+ *                gradient through D.  NULL skips it.
+ *   scale        finite softmax scale (usually 1/sqrt(head_dim)).
+ *   workspace    device scratch of at least attn_fwd_workspace_size() bytes,
+ *                256-byte aligned (may be NULL when that size is 0).
+ * head_dim must be 64 or 128.  bf16 q, k, v and o must be 16-byte aligned
+ * (tensor-memory-accelerator loads).  Returns ATTN_OK once the kernels are
+ * queued.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
+                     float *lse, float *o_f32, const int32_t *cu_seqlens_q,
+                     const int32_t *cu_seqlens_k, int batch, int max_seqlen_q,
+                     int max_seqlen_k, int total_q, int total_k, int n_heads_q,
+                     int n_heads_kv, int head_dim, float scale,
+                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * Workspace bytes attn_bwd needs: an fp32 dQ accumulator [total_q,
+ * n_heads_q, head_dim] and the per-row terms D_i = dO_i . O_i and the
+ * base-2 logsumexp [n_heads_q, total_q] fp32 each.  (size_t)-1 for bad
+ * arguments.
+ */
+size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
+                               int total_q, int total_k, int n_heads_q,
+                               int n_heads_kv, int head_dim, attn_dtype dtype);
+
+/*
+ * Backward at upstream gradient dout, recomputing the probabilities from q, k
+ * and the saved lse with the same mask rule as the forward
+ * ("causal-mask-and-ragged-sequence-layouts", sixth paragraph):
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - dO_i . O_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ * with dK and dV summed over the query heads that share each KV head
+ * ("attention-algorithm-error-and-complexity-tests", third paragraph).
+ *   o, lse   the forward's outputs for the same inputs.
+ *   o_f32    the forward's optional fp32 output, or NULL: D_i is then formed
+ *            from the rounded o.
+ *   dq       [total_q, n_heads_q, head_dim]; dk, dv [total_k, n_heads_kv,
+ *            head_dim]; type `dtype`.  Fully overwritten (rows no query
+ *            reaches get zeros).
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v,
+                     const void *o, const float *lse, const float *o_f32,
+                     const void *dout,
+                     void *dq, void *dk, void *dv,
+                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                     int batch, int max_seqlen_q, int max_seqlen_k,
+                     int total_q, int total_k, int n_heads_q, int n_heads_kv,
+                     int head_dim, float scale, attn_mask_kind mask,
+                     attn_dtype dtype, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * Mask probe (diagnostic): writes, for one query head, the packed allowed-pair
+ * matrix that the kernels' tile planner and mask predicate produce, as bytes
+ * out[total_q * total_k] (1 = allowed).  It runs the same device code the
+ * attention kernels use to bound and mask their tiles, so tests can compare
+ * it bit for bit with an independent definition.  tile_rows (16, 32, 64 or
+ * 128) is the number of query tokens per tile the planner assumes: 128 for
+ * one head per tile, 128 / group when the query heads of a KV head share a
+ * tile.  `out` is caller-owned device memory; total_q * total_k must be
+ * below 2^31.
+ */
+attn_status attn_mask_probe(const int32_t *cu_seqlens_q,
+                            const int32_t *cu_seqlens_k, int batch,
+                            int max_seqlen_q, int max_seqlen_k, int total_q,
+                            int total_k, attn_mask_kind mask, int tile_rows,
+                            uint8_t *out, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * flag.  Returns ATTN_OK, ATTN_ERR_DEVICE_BOUNDS, ATTN_ERR_DEVICE_TIMEOUT, or
+ * ATTN_ERR_CUDA when the synchronisation itself failed.
+ */
+attn_status attn_get_device_error(void *stream);
+
+/* Static description of a status code. */
+const char *attn_status_string(attn_status status);
+
+/*
+ * The kernel plan the calling thread's last attn_fwd / attn_bwd chose (kernel
+ * names, grid sizes, splits), so timings can be tied to the kernel that ran
+ * ("attention-algorithm-error-and-complexity-tests", sixth paragraph).
+ * Thread-local, valid until the thread's next call.
+ */
+const char *attn_last_plan(void);
+
+/* Library ABI version (major * 100 + minor). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,83 @@
+"""The C-ABI library on the host: it loads without a GPU, exports every
+symbol include/attn.h declares, and rejects bad arguments before launching
+anything."""
+import ctypes
+import re
+import os
+
+import pytest
+
+from exact_tiled_attention_online_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert "attn_fwd" in names and "attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/attn.h but not exported"
+
+
+def test_version_and_strings(lib):
+    assert lib.attn_version() >= 100
+    for code in range(7):
+        assert attn.status_string(code)
+
+
+def _fwd(lib, **over):
+    args = dict(q=1, k=1, v=1, o=1, lse=1, o_f32=None, cu_q=1, cu_k=1, batch=1, max_q=4, max_k=4,
+                total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, dtype=0,
+                ws=None, ws_bytes=0, stream=None)
+    args.update(over)
+    return lib.attn_fwd(*args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"hq": 3, "hkv": 2}, 1),            # Hq not a multiple of Hkv
+    ({"hkv": 0}, 1),
+    ({"d": 96}, 2),                      # head_dim not built
+    ({"batch": -1}, 1),
+    ({"total_q": -5}, 1),
+    ({"max_q": 8}, 1),                   # max_seqlen above total
+    ({"mask": 7}, 1),
+    ({"dtype": 9}, 1),
+    ({"scale": float("nan")}, 1),
+    ({"scale": float("inf")}, 1),
+    ({"q": None}, 1),
+    ({"cu_q": None}, 1),
+])
+def test_fwd_rejects_bad_arguments(lib, over, code):
+    assert _fwd(lib, **over) == code
+
+
+def test_workspace_size_rejects_bad_arguments(lib):
+    assert lib.attn_fwd_workspace_size(1, 4, 4, 4, 3, 2, 64, 0) == ctypes.c_size_t(-1).value
+    assert lib.attn_bwd_workspace_size(1, 4, 4, 4, 4, 2, 1, 80, 0) == ctypes.c_size_t(-1).value
+
+
+def test_bwd_workspace_covers_accumulator(lib):
+    n = lib.attn_bwd_workspace_size(2, 100, 100, 200, 200, 4, 2, 128, 0)
+    assert n >= 200 * 4 * 128 * 4 + 2 * 4 * 200 * 4
+
+
+def test_bwd_rejects_missing_workspace(lib):
+    st = lib.attn_bwd(1, 1, 1, 1, 1, None, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.1, 1, 0,
+                      None, 0, None)
+    assert st == 3
+
+
+def test_probe_rejects_bad_tile_rows(lib):
+    assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, 48, 1, None) == 1

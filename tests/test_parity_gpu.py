@@ -1,0 +1,136 @@
+"""CUDA path against the fp64 oracle, element by element, on seeded inputs.
+
+Small and mid-size problems are compared in full; the full-size workloads
+are compared on sampled rows that the oracle computes one by one, in the same
+launch configuration the benchmark times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_online_gb300 import attn, inputs
+from tests import compare
+from tests.gpu_cases import oracle_fwd, run_fwd, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
+
+
+def check_full(x, o, lse):
+    o_ref, lse_ref = oracle_fwd(x)
+    compare.check_close("o", o, o_ref)
+    compare.check_lse("lse", lse, lse_ref)
+    # empty rows: exact zeros and -inf
+    empty = np.isneginf(lse_ref)
+    if empty.any():
+        on = compare.to_np(o)
+        for h, t in np.argwhere(empty):
+            assert np.all(on[t, h] == 0.0)
+
+
+def check_rows(x, o, lse, rows):
+    o_ref, lse_ref = oracle_fwd(x, rows=rows)
+    on, ln = compare.to_np(o), compare.to_np(lse)
+    compare.check_close("o", on[rows[:, 0], rows[:, 1]], o_ref)
+    compare.check_lse("lse", ln[rows[:, 1], rows[:, 0]], lse_ref)
+
+
+def test_tiny_fp32():
+    x = inputs.make_inputs(inputs.WORKLOADS["tiny_fp32"])
+    o, lse, _ = run_fwd(x)
+    check_full(x, o, lse)
+    o_ref, _ = oracle_fwd(x)
+    # the fp32 path is far inside the bf16 contract
+    assert np.abs(compare.to_np(o) - o_ref).max() < 1e-4
+
+
+def test_varlen_causal_full():
+    x = inputs.make_inputs(inputs.WORKLOADS["varlen_causal"])
+    o, lse, _ = run_fwd(x)
+    check_full(x, o, lse)
+
+
+EDGE = [  # (name, lq, lk, hq, hkv, d, mask)
+    ("ragged_tile_edges_tl", (63, 64, 65, 127, 128, 129, 1), None, 4, 1, 128, TL),
+    ("ragged_tile_edges_br", (1, 5, 129), (300, 5, 128), 8, 2, 128, BR),
+    ("q_longer_br_empty_rows", (64, 100), (32, 7), 8, 8, 128, BR),
+    ("q_longer_tl", (200,), (70,), 4, 2, 64, TL),
+    ("noncausal_gqa8", (130, 3), (257, 9), 16, 2, 128, NONE),
+    ("zero_length_segments", (0, 40, 0, 17), (0, 40, 5, 17), 2, 1, 64, TL),
+    ("d64_gqa4", (256, 190), (256, 190), 8, 2, 64, TL),
+    ("single_token_each", (1, 1, 1), (1, 1, 1), 4, 4, 128, TL),
+    ("decode_like_q1", (1,) * 5, (1000, 129, 128, 1, 4097), 32, 8, 128, BR),
+    ("decode_like_q16", (16,) * 3, (2000, 16, 300), 32, 8, 128, BR),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[c[0] for c in EDGE])
+def test_edge_shapes(case):
+    name, lq, lk, hq, hkv, d, mask = case
+    w = inputs.custom(name, lq, lk if lk else lq, hq, hkv, d, "bf16", mask, seed=11,
+                      v_shift_per_seq=3.0)
+    x = inputs.make_inputs(w)
+    o, lse, _ = run_fwd(x)
+    check_full(x, o, lse)
+
+
+def test_decode_empty_rows_full():
+    x = inputs.make_inputs(inputs.WORKLOADS["decode_empty_rows"])
+    o, lse, _ = run_fwd(x)
+    check_full(x, o, lse)
+    ln = compare.to_np(lse)
+    # rows 0..31 of every sequence are empty under bottom-right alignment
+    for s in range(32):
+        assert np.all(np.isneginf(ln[:, s * 64:s * 64 + 32]))
+        assert np.all(np.isfinite(ln[:, s * 64 + 32:s * 64 + 64]))
+
+
+def test_count_probe():
+    """Q = 0 makes every allowed logit 0, so exp(lse) is the allowed-set size
+    of the row: the allowed sets are checked end to end."""
+    w = inputs.custom("count", (5, 130, 64), (300, 129, 64), 4, 2, 128, "bf16", BR, seed=3)
+    x = inputs.make_inputs(w)
+    x["q"] = torch.zeros_like(x["q"])
+    o, lse, _ = run_fwd(x)
+    ln = compare.to_np(lse)
+    cu = inputs.cu_seqlens(w.seqlens_q).numpy()
+    for s, (nq, nk) in enumerate(zip(w.seqlens_q, w.seqlens_k)):
+        for i in range(nq):
+            n = max(0, min(i + nk - nq + 1, nk))
+            got = ln[:, cu[s] + i]
+            if n == 0:
+                assert np.all(np.isneginf(got))
+            else:
+                assert np.all(np.abs(got - math.log(n)) <= 1e-4 * max(1.0, math.log(n)))
+
+
+@pytest.mark.parametrize("name", ["gqa_prefill", "decode_q1", "decode_q16"])
+def test_full_size_sampled(name):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w)
+    o, lse, _ = run_fwd(x)
+    rows = sample_rows(w, 48, seed=5)
+    check_rows(x, o, lse, rows)
+    assert np.all(np.isfinite(compare.to_np(o)))
+
+
+def test_forward_deterministic():
+    x = inputs.make_inputs(inputs.WORKLOADS["varlen_causal"])
+    o1, l1, dev = run_fwd(x)
+    for _ in range(3):
+        o2, l2, _ = run_fwd(x)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bad_cu_seqlens_sets_device_flag():
+    """cu_seqlens that run past total_q are caught on the device (no access
+    beyond the buffers) and reported through the error flag."""
+    w = inputs.custom("bad", (8, 8), (8, 8), 2, 1, 64, "bf16", TL)
+    x = inputs.make_inputs(w, device="cuda")
+    bad = torch.tensor([0, 8, 20], dtype=torch.int32, device="cuda")
+    attn.fwd(x["q"], x["k"], x["v"], bad, x["cu_seqlens_k"], 12, 8, TL)
+    assert attn.get_device_error() == 6
+    assert attn.get_device_error() == 0  # cleared by the read

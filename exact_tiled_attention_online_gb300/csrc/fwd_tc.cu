@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = g.q0 + i;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int n = n_begin + jj, sb = jj & 1;
@@ -267,19 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = mt > m_ref + kRescaleLog2 ? mt : m_ref;
       const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
       const float base = m_new == -INFINITY ? 0.f : m_new;
-#pragma unroll
-      for (int c = 0; c < kTileKeys; c++) sv[c] = fast_exp2(sv[c] - base);
-      // The denominator sums the bf16-rounded probabilities that the P V
-      // product uses, so O / l is an exact convex combination of V rows: a
-      // common offset in V cancels instead of carrying P's rounding error.
-      uint32_t pk[kTileKeys / 2];
       float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < kTileKeys; c++) {
+        sv[c] = fast_exp2(sv[c] - base);
+        rs += sv[c];
+      }
+      // Two denominators: l sums the fp32 probabilities and gives lse; lr
+      // sums the bf16-rounded probabilities that the P V product uses, so
+      // O / lr is an exact convex combination of V rows and a common offset
+      // in V cancels instead of carrying P's rounding error.
+      uint32_t pk[kTileKeys / 2];
+      float rr = 0.f;
 #pragma unroll
       for (int c = 0; c < kTileKeys / 2; c++) {
         pk[c] = pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
-        rs += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        rr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
       }
       l = l * alpha + rs;
+      lr = lr * alpha + rr;
       m_ref = m_new;
       if (jj > 0) {
         // P V of the previous tile must be done: it reads the P buffer and
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ------------------------------------------------------------ epilogue
     const bool have = __all_sync(0xffffffffu, ok) && n_tiles > 0;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
     const float lse2 = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
     if (a.n_splits > 1) {
       float *dst = p.o_part + (((size_t)split * p.total_q + t) * p.hq + h) * D;

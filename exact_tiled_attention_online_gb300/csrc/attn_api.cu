@@ -66,6 +66,15 @@ static int sm_count() {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Internal helpers for the other entry-point file of the library.
+int *internal_error_flag() { return device_error_ptr(); }
+attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
+                                 int hq, int hkv, int d, int mask, int dtype) {
+  return check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+}
+int internal_sm_count() { return sm_count(); }
+void internal_set_plan(const char *s) { set_plan(s); }
+
 }  // namespace attn
 
 using namespace attn;
@@ -83,6 +92,7 @@ const char *attn_status_string(attn_status s) {
     case ATTN_ERR_CUDA: return "CUDA runtime error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait expired";
     case ATTN_ERR_DEVICE_BOUNDS: return "cu_seqlens inconsistent with the sizes passed";
+    case ATTN_ERR_SCRATCH_LIMIT: return "problem needs more than the library's static scratch";
   }
   return "unknown status";
 }

@@ -65,7 +65,8 @@ typedef enum {
   ATTN_ERR_WORKSPACE = 3,      /* workspace missing or smaller than needed   */
   ATTN_ERR_CUDA = 4,           /* a CUDA runtime call failed                 */
   ATTN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait expired              */
-  ATTN_ERR_DEVICE_BOUNDS = 6   /* cu_seqlens disagree with the sizes passed  */
+  ATTN_ERR_DEVICE_BOUNDS = 6,  /* cu_seqlens disagree with the sizes passed  */
+  ATTN_ERR_SCRATCH_LIMIT = 7   /* needs more than the static scratch holds   */
 } attn_status;
 
 typedef enum {
@@ -176,6 +177,42 @@ attn_status attn_mask_probe(const int32_t *cu_seqlens_q,
  * ATTN_ERR_CUDA when the synchronisation itself failed.
  */
 attn_status attn_get_device_error(void *stream);
+
+/*
+ * Forward that allocates nothing, not even through the caller: for callers
+ * that cannot hand the library a workspace.  Typical ones are plug-ins and
+ * embedded runtimes whose host owns a fixed, pre-planned device memory pool
+ * and exposes no allocator to them, and latency-critical serving loops where
+ * a cudaMalloc (which can synchronise the device, or fail under memory
+ * pressure) is not allowed once the loop runs.  The pages have no
+ * counterpart: this is a packaging variant of attn_fwd, not a different
+ * computation.
+ *
+ * Same arguments, layouts and results as attn_fwd, minus the workspace.  The
+ * split-KV decode plan keeps its per-split partial outputs in one array of
+ * ATTN_STATIC_SCRATCH_BYTES (64 MiB) that the library holds in device memory
+ * of every GPU it is loaded on, until the process exits.  A problem whose
+ * split scratch would exceed that array is rejected with
+ * ATTN_ERR_SCRATCH_LIMIT before anything is launched; plans that need no
+ * scratch run exactly as in attn_fwd.
+ *
+ * The array's device address is looked up on the first call on each device
+ * (make that first call outside any stream capture).  All calls share the
+ * array: calls whose kernels overlap on the GPU (different streams, or
+ * different host threads, without ordering between them) race on it and
+ * must be serialised by the caller.  Every scratch entry a call reads is
+ * written earlier in the same call, so nothing needs clearing between calls.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES (64u << 20)
+attn_status attn_fwd_static_scratch(const void *q, const void *k, const void *v,
+                                    void *o, float *lse, float *o_f32,
+                                    const int32_t *cu_seqlens_q,
+                                    const int32_t *cu_seqlens_k, int batch,
+                                    int max_seqlen_q, int max_seqlen_k,
+                                    int total_q, int total_k, int n_heads_q,
+                                    int n_heads_kv, int head_dim, float scale,
+                                    attn_mask_kind mask, attn_dtype dtype,
+                                    void *stream);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status status);

@@ -12,6 +12,9 @@ namespace attn {
 
 cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t st);
 cudaError_t launch_bwd_simt(const BwdParams &p, attn_dtype dtype, cudaStream_t st);
+cudaError_t launch_bwd_pre(const BwdParams &p, attn_dtype dtype, cudaStream_t st);
+cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
 cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st,
                           char *desc, size_t desc_len);
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
@@ -66,6 +69,30 @@ static int sm_count() {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Backward workspace: D and lse2 [hq, total_q] fp32; for bf16 also fp16
+// copies of q, dout ([total_q, hq, d]) and k, v ([total_k, hkv, d]).
+struct BwdLayout {
+  size_t delta, lse2, q16, do16, k16, v16, total;
+};
+static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, int dtype) {
+  BwdLayout l{};
+  const size_t rows = align256((size_t)hq * total_q * 4);
+  l.delta = 0;
+  l.lse2 = rows;
+  size_t off = 2 * rows;
+  if (dtype == ATTN_DTYPE_BF16) {
+    const size_t qb = align256((size_t)total_q * hq * d * 2);
+    const size_t kb = align256((size_t)total_k * hkv * d * 2);
+    l.q16 = off;
+    l.do16 = off + qb;
+    l.k16 = off + 2 * qb;
+    l.v16 = off + 2 * qb + kb;
+    off += 2 * qb + 2 * kb;
+  }
+  l.total = off;
+  return l;
+}
+
 // Internal helpers for the other entry-point file of the library.
 int *internal_error_flag() { return device_error_ptr(); }
 attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
@@ -93,6 +120,7 @@ const char *attn_status_string(attn_status s) {
     case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait expired";
     case ATTN_ERR_DEVICE_BOUNDS: return "cu_seqlens inconsistent with the sizes passed";
     case ATTN_ERR_SCRATCH_LIMIT: return "problem needs more than the library's static scratch";
+    case ATTN_ERR_DEVICE_RANGE: return "a backward input lies outside the fp16 range";
   }
   return "unknown status";
 }
@@ -172,9 +200,7 @@ size_t attn_bwd_workspace_size(int batch, int max_q, int max_k, int total_q, int
   if (check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, ATTN_MASK_NONE, dtype) !=
       ATTN_OK)
     return (size_t)-1;
-  size_t acc = align256((size_t)total_q * hq * d * 4);
-  size_t rows = align256((size_t)hq * total_q * 4);
-  return acc + 2 * rows;
+  return bwd_layout(total_q, total_k, hq, hkv, d, dtype).total;
 }
 
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
@@ -203,11 +229,9 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   char *ws = static_cast<char *>(workspace);
-  size_t acc = align256((size_t)total_q * hq * d * 4);
-  size_t rows = align256((size_t)hq * total_q * 4);
-  p.dq_acc = reinterpret_cast<float *>(ws);
-  p.delta = reinterpret_cast<float *>(ws + acc);
-  p.lse2 = reinterpret_cast<float *>(ws + acc + rows);
+  const BwdLayout wl = bwd_layout(total_q, total_k, hq, hkv, d, dtype);
+  p.delta = reinterpret_cast<float *>(ws + wl.delta);
+  p.lse2 = reinterpret_cast<float *>(ws + wl.lse2);
   if (batch == 0) {
     set_plan("empty");
     return ATTN_OK;
@@ -221,10 +245,24 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
     ce = cudaMemsetAsync(dk, 0, (size_t)total_k * hkv * d * es, cs);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(dv, 0, (size_t)total_k * hkv * d * es, cs);
   }
-  if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);
   char desc[256];
-  snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d",
-           dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d);
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(dout);
+  const bool tc = dtype == ATTN_DTYPE_BF16 && kTensorCorePath && total_k > 0 && total_q > 0 &&
+                  (mis & 15) == 0;
+  if (tc) {
+    p.q16 = ws + wl.q16;
+    p.do16 = ws + wl.do16;
+    p.k16 = ws + wl.k16;
+    p.v16 = ws + wl.v16;
+    if (ce == cudaSuccess) ce = launch_bwd_pre(p, dtype, cs);
+    if (ce == cudaSuccess) ce = launch_kv_to_f16(p, cs);
+    if (ce == cudaSuccess) ce = launch_bwd_tc(p, cs, desc, sizeof(desc));
+  } else {
+    if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);
+    snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d",
+             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d);
+  }
   set_plan(desc);
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

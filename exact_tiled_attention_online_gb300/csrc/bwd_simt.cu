@@ -12,6 +12,8 @@
 // ("causal-mask-and-ragged-sequence-layouts", sixth paragraph: backward
 // recomputation rebuilds the same mask).  No atomics: each output row has one
 // owner warp, so the result is deterministic.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace attn {
@@ -35,6 +37,22 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
     for (int e = 0; e < E; e++) part += Elem<T>::to_f(op[e]) * Elem<T>::to_f(dp[e]);
   }
   const float D_i = warp_sum(part);
+  if (p.q16) {
+    // fp16 copies for the tensor-core backward; bf16 -> fp16 is exact inside
+    // the fp16 normal range, larger magnitudes are reported.
+    const T *qp = reinterpret_cast<const T *>(p.q) + (size_t)row * D + lane * E;
+    __half *q16 = reinterpret_cast<__half *>(p.q16) + (size_t)row * D + lane * E;
+    __half *d16 = reinterpret_cast<__half *>(p.do16) + (size_t)row * D + lane * E;
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < E; e++) {
+      const float a = Elem<T>::to_f(qp[e]), c = Elem<T>::to_f(dp[e]);
+      bad |= fabsf(a) > 65504.f || fabsf(c) > 65504.f;
+      q16[e] = __float2half_rn(a);
+      d16[e] = __float2half_rn(c);
+    }
+    if (bad) raise_error(p.err, ATTN_ERR_DEVICE_RANGE);
+  }
   if (lane == 0) {
     const float l = p.lse[(size_t)h * p.total_q + t];
     p.delta[(size_t)h * p.total_q + t] = D_i;
@@ -162,6 +180,57 @@ static void launch_all(const BwdParams &p, cudaStream_t st) {
     bwd_dq_simt_kernel<T, D><<<dim3((p.max_q + 3) / 4, p.hq, p.batch), 128, 0, st>>>(p);
   if (p.max_k > 0)
     bwd_dkdv_simt_kernel<T, D><<<dim3((p.max_k + 3) / 4, p.hkv, p.batch), 128, 0, st>>>(p);
+}
+
+// K and V -> fp16 copies for the tensor-core backward, 8 elements a thread.
+__global__ void __launch_bounds__(256) kv_to_f16_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                        const __nv_bfloat16 *__restrict__ v,
+                                                        __half *__restrict__ k16,
+                                                        __half *__restrict__ v16, size_t n8,
+                                                        int *err) {
+  bool bad = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= n8;
+    const size_t j = is_v ? i - n8 : i;
+    const uint4 in = reinterpret_cast<const uint4 *>(is_v ? v : k)[j];
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&in);
+    uint4 out;
+    __half *y = reinterpret_cast<__half *>(&out);
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const float f = __bfloat162float(x[e]);
+      bad |= fabsf(f) > 65504.f;
+      y[e] = __float2half_rn(f);
+    }
+    reinterpret_cast<uint4 *>(is_v ? v16 : k16)[j] = out;
+  }
+  if (bad) raise_error(err, ATTN_ERR_DEVICE_RANGE);
+}
+
+cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st) {
+  const size_t n8 = (size_t)p.total_k * p.hkv * p.d / 8;
+  if (n8 == 0) return cudaSuccess;
+  size_t blocks = (2 * n8 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  kv_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16 *>(p.k), reinterpret_cast<const __nv_bfloat16 *>(p.v),
+      reinterpret_cast<__half *>(p.k16), reinterpret_cast<__half *>(p.v16), n8, p.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const BwdParams &p, attn_dtype dtype, cudaStream_t st) {
+  const long long rows = (long long)p.total_q * p.hq;
+  if (rows == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((rows + 3) / 4);
+  if (dtype == ATTN_DTYPE_FP32) {
+    if (p.d == 64) bwd_pre_kernel<float, 64><<<blocks, 128, 0, st>>>(p);
+    else bwd_pre_kernel<float, 128><<<blocks, 128, 0, st>>>(p);
+  } else {
+    if (p.d == 64) bwd_pre_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, st>>>(p);
+    else bwd_pre_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, st>>>(p);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_simt(const BwdParams &p, attn_dtype dtype, cudaStream_t st) {

@@ -1,0 +1,671 @@
+// bwd_tc.cu -- tensor-core backward for bf16 inputs (recompute form), two kernels
+// that share nothing but their inputs, so no atomics and a deterministic
+// result:
+//
+//   dkdv: one CTA per (sequence, KV head, 128-key tile).  It walks every
+//         query head of the KV head's group and every 64-row query tile that
+//         can see its keys, and per tile computes on tcgen05
+//           S^T = K Q^T, dP^T = V dO^T        (M = 128 keys, N = 64 rows),
+//         turns them into P^T = 2^(c S^T - lse2) and dS^T = P^T (dP^T - D)
+//         in registers (thread = key), and accumulates
+//           dV += P^T dO, dK += dS^T Q        (M = 128 keys, N = d)
+//         in TMEM, so the GQA sum over shared heads never leaves the SM
+//         ("attention-algorithm-error-and-complexity-tests", third paragraph).
+//   dq:   one CTA per (sequence, query head, 128-row query tile).  It walks
+//         the row tile's key tiles and computes S = Q K^T, dP = dO V^T,
+//         dS = P (dP - D) (thread = row) and dQ += dS K in TMEM.
+//
+// The products run in fp16 on fp16 copies of q, k, v and dout (exact for bf16
+// values inside the fp16 range), so the P and dS operands keep 11 significant
+// bits: with bf16 P, dV of a key that thousands of rows attend misses the
+// 1e-2 contract.  Accumulation is fp32 in TMEM.
+//
+// Both rebuild the forward's mask with the same planner and lane predicate
+// ("causal-mask-and-ragged-sequence-layouts", sixth paragraph); masked and
+// out-of-range lanes get P = dS = 0.  D and lse2 (lse in log2 units, +inf for
+// empty rows) come from the preprocess kernel.  Waits are bounded like the
+// forward's.
+#include <stdio.h>
+
+#include "common.cuh"
+#include "plan.h"
+#include "sm100.cuh"
+#include "tma_map.h"
+
+namespace attn {
+using namespace sm100;
+
+namespace {
+
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 math
+constexpr uint32_t kTmemCols = 512;
+constexpr int kChunk128 = 128 * 128;  // [128 rows x 64 bf16] swizzled chunk
+constexpr int kChunk64 = 64 * 128;    // [64 rows x 64 bf16] swizzled chunk
+
+struct BwdTcArgs {
+  BwdParams p;
+  int group;
+  int n_key_tiles;  // dkdv grid x
+  int n_row_tiles;  // dq grid x
+};
+
+struct Sync {
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_bar(Sync *sy, uint64_t *bar, uint32_t parity, int *err) {
+  if (*reinterpret_cast<volatile int *>(&sy->abort)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *reinterpret_cast<volatile int *>(&sy->abort) = 1;
+  raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void math_group_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// ===========================================================================
+// dK, dV
+// ===========================================================================
+constexpr int kRowsA = 64;   // query rows per step
+constexpr int kKeysA = 128;  // keys per CTA
+
+template <int D>
+struct LayoutA {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kKV = kChunks * kChunk128;  // K or V tile
+  static constexpr int kQT = kChunks * kChunk64;   // Q or dO tile (64 rows)
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kKV;
+  static constexpr int kQ = kV + kKV;         // [2] stages
+  static constexpr int kDO = kQ + 2 * kQT;    // [2]
+  static constexpr int kPT = kDO + 2 * kQT;   // [2] x [128 keys x 64 rows] bf16
+  static constexpr int kDST = kPT + 2 * kChunk128;
+  static constexpr int kRow = kDST + 2 * kChunk128;  // [2] x {lse2[64], D[64]}
+  static constexpr int kBar = kRow + 2 * 2 * kRowsA * 4;
+  static constexpr int kUsed = kBar + 512;
+  static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
+};
+
+struct BarsA {
+  uint64_t kv_full, q_full[2], do_full[2], q_empty[2], do_empty[2], s_full[2], dp_full[2],
+      ps_full[2], mm_done[2];
+  uint32_t tmem_base;
+  Sync sync;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const BwdTcArgs a) {
+  using L = LayoutA<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  BarsA *b = reinterpret_cast<BarsA *>(smem + L::kBar);
+  const BwdParams &p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int n = blockIdx.x;  // key tile (early keys are seen by the most rows)
+  const int hk = blockIdx.y;
+  const int seq = blockIdx.z;
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int j0 = n * kKeysA;
+  if (j0 >= g.nk) return;
+  // 64-row query tiles with at least one row that sees a key of this tile
+  const int m_begin = row_begin(g.mask, j0, g.nq, g.nk) / kRowsA;
+  const int m_end = (g.nq + kRowsA - 1) / kRowsA;
+  const int n_m = m_end > m_begin ? m_end - m_begin : 0;
+  const int n_it = n_m * a.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&b->kv_full, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->q_full[s], 1);
+      mbar_init(&b->do_full[s], 1);
+      mbar_init(&b->q_empty[s], 1);
+      mbar_init(&b->do_empty[s], 1);
+      mbar_init(&b->s_full[s], 1);
+      mbar_init(&b->dp_full[s], 1);
+      mbar_init(&b->ps_full[s], 128);
+      mbar_init(&b->mm_done[s], 1);
+    }
+    b->sync.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&b->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  // TMEM columns: S^T[2] at 0 / 64, dP^T[2] at 128 / 192, dV at 256, dK at 256 + D.
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+  const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+  const uint32_t sPT = smem_u32(smem + L::kPT), sDST = smem_u32(smem + L::kDST);
+  float *sRow = reinterpret_cast<float *>(smem + L::kRow);
+
+  auto it_head = [&](int it) { return hk * a.group + it / n_m; };
+  auto it_row0 = [&](int it) { return (m_begin + it % n_m) * kRowsA; };
+
+  if (warp == 0) {
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&b->kv_full, 2 * L::kKV);
+      for (int c = 0; c < L::kChunks; c++) {
+        tma_load_3d(smem + L::kK + c * kChunk128, &tm_k, &b->kv_full, c * 64, hk, g.k0 + j0);
+        tma_load_3d(smem + L::kV + c * kChunk128, &tm_v, &b->kv_full, c * 64, hk, g.k0 + j0);
+      }
+      for (int it = 0; it < n_it; it++) {
+        const int st = it & 1, u = it >> 1;
+        const int h = it_head(it), tok = g.q0 + it_row0(it);
+        if (it >= 2 && !wait_bar(&b->sync, &b->q_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->q_full[st], L::kQT);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kQ + st * L::kQT + c * kChunk64, &tm_q, &b->q_full[st], c * 64, h,
+                      tok);
+        if (it >= 2 && !wait_bar(&b->sync, &b->do_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->do_full[st], L::kQT);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kDO + st * L::kQT + c * kChunk64, &tm_do, &b->do_full[st], c * 64,
+                      h, tok);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_it > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32(128, kRowsA, 0, 0);
+      constexpr uint32_t idesc_g = idesc_f16_f32(128, D, 0, 1);
+      // S^T (or dP^T) = A_tile [128 keys x d] * B_tile [64 rows x d]^T
+      auto issue_st = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+          const uint64_t ad = smem_desc_sw128(a_base + (kk >> 2) * kChunk128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_base + (kk >> 2) * kChunk64 + (kk & 3) * 32, 16, 1024);
+          mma_bf16_ss(tmem + col, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      // acc [128 keys x d] += A [128 keys x 64 rows] * B [64 rows x d]
+      auto issue_grad = [&](uint32_t a_base, uint32_t b_base, uint32_t col, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kRowsA / 16; kk++) {
+          const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, kChunk64, 1024);
+          mma_bf16_ss(tmem + col, ad, bd, idesc_g, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
+                wait_bar(&b->sync, &b->q_full[0], 0, p.err);
+      if (ok) {
+        tc_fence_after();
+        issue_st(sK, sQ, kColS);
+        mma_commit(&b->s_full[0]);
+        ok = wait_bar(&b->sync, &b->do_full[0], 0, p.err);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_st(sV, sDO, kColDP);
+        mma_commit(&b->dp_full[0]);
+      }
+      for (int it = 0; ok && it < n_it; it++) {
+        const int st = it & 1;
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) & 1, u1 = (it + 1) >> 1;
+          if (!wait_bar(&b->sync, &b->q_full[s1], u1 & 1, p.err)) break;
+          tc_fence_after();
+          issue_st(sK, sQ + s1 * L::kQT, kColS + s1 * kRowsA);
+          mma_commit(&b->s_full[s1]);
+          if (!wait_bar(&b->sync, &b->do_full[s1], u1 & 1, p.err)) break;
+          tc_fence_after();
+          issue_st(sV, sDO + s1 * L::kQT, kColDP + s1 * kRowsA);
+          mma_commit(&b->dp_full[s1]);
+        }
+        if (!wait_bar(&b->sync, &b->ps_full[st], (it >> 1) & 1, p.err)) break;
+        tc_fence_after();
+        issue_grad(sPT + st * kChunk128, sDO + st * L::kQT, kColDV, it > 0);
+        issue_grad(sDST + st * kChunk128, sQ + st * L::kQT, kColDK, it > 0);
+        mma_commit(&b->mm_done[st]);
+        mma_commit(&b->q_empty[st]);
+        mma_commit(&b->do_empty[st]);
+      }
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key lane
+    const int tid = threadIdx.x - 64;
+    const int j = j0 + r;          // in-sequence key
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; it++) {
+      const int st = it & 1;
+      const int h = it_head(it), i0 = it_row0(it);
+      {  // lse2 and D of the 64 rows into shared memory
+        const int c = tid & (kRowsA - 1);
+        const int i = i0 + c;
+        float val;
+        if (tid < kRowsA)
+          val = i < g.nq ? p.lse2[(size_t)h * p.total_q + g.q0 + i] : INFINITY;
+        else
+          val = i < g.nq ? p.delta[(size_t)h * p.total_q + g.q0 + i] : 0.f;
+        sRow[st * 2 * kRowsA + tid] = val;
+      }
+      math_group_sync();  // every math thread reaches it once per step, even after an abort
+      const float *lse2 = sRow + st * 2 * kRowsA;
+      const float *dl = lse2 + kRowsA;
+      if (ok)
+        ok = wait_bar(&b->sync, &b->s_full[st], (it >> 1) & 1, p.err) &&
+             wait_bar(&b->sync, &b->dp_full[st], (it >> 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) continue;
+      tc_fence_after();
+      const bool full = i0 + kRowsA <= g.nq && key_end(g.mask, i0, g.nq, g.nk) >= j0 + kKeysA;
+      uint32_t pp[kRowsA / 2], dd[kRowsA / 2];
+#pragma unroll
+      for (int cc = 0; cc < kRowsA / 32; cc++) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(t_lane + kColS + st * kRowsA + cc * 32, sv);
+        tmem_ld32(t_lane + kColDP + st * kRowsA + cc * 32, dv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int c0 = cc * 32 + e;
+          float pr[2], ds[2];
+#pragma unroll
+          for (int q = 0; q < 2; q++) {
+            const int c = c0 + q;
+            float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2[c]);
+            if (!full && !lane_allowed(g.mask, i0 + c, j, g.nq, g.nk)) pv = 0.f;
+            pr[q] = pv;
+            ds[q] = pv * (__uint_as_float(dv[e + q]) - dl[c]);
+          }
+          pp[c0 / 2] = pack_f16x2(pr[0], pr[1]);
+          dd[c0 / 2] = pack_f16x2(ds[0], ds[1]);
+        }
+      }
+      if (it >= 2) ok = wait_bar(&b->sync, &b->mm_done[st], ((it >> 1) - 1) & 1, p.err);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) continue;
+      // [128 keys x 64 rows] K-major, 128-byte swizzle: key r's 128 bytes
+#pragma unroll
+      for (int v = 0; v < kRowsA / 8; v++) {
+        const uint32_t off = r * 128 + (((v & 7) ^ (r & 7)) << 4);
+        st_shared_v4(sPT + st * kChunk128 + off, pp[4 * v], pp[4 * v + 1], pp[4 * v + 2],
+                     pp[4 * v + 3]);
+        st_shared_v4(sDST + st * kChunk128 + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2],
+                     dd[4 * v + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&b->ps_full[st]);
+    }
+    if (ok && n_it > 0) {
+      const int last = n_it - 1;
+      if (wait_bar(&b->sync, &b->mm_done[last & 1], (last >> 1) & 1, p.err))
+        tc_fence_after();
+      else
+        ok = false;
+    }
+    const bool have = __all_sync(0xffffffffu, ok) && n_it > 0;
+    const size_t krow = ((size_t)(g.k0 + (j < g.nk ? j : 0)) * p.hkv + hk) * D;
+    __nv_bfloat16 *dkp = reinterpret_cast<__nv_bfloat16 *>(p.dk) + krow;
+    __nv_bfloat16 *dvp = reinterpret_cast<__nv_bfloat16 *>(p.dv) + krow;
+#pragma unroll
+    for (int c = 0; c < D / 32; c++) {
+      uint32_t kv32[32], vv32[32];
+      if (have) {  // warp-uniform: every lane of the warp loads
+        tmem_ld32(t_lane + kColDK + c * 32, kv32);
+        tmem_ld32(t_lane + kColDV + c * 32, vv32);
+        tmem_wait_ld();
+      }
+      if (j < g.nk) {  // keys past the sequence end own no storage
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 wk, wv;
+          wk.x = have ? pack_bf16x2(__uint_as_float(kv32[e]) * p.scale, __uint_as_float(kv32[e + 1]) * p.scale) : 0u;
+          wk.y = have ? pack_bf16x2(__uint_as_float(kv32[e + 2]) * p.scale, __uint_as_float(kv32[e + 3]) * p.scale) : 0u;
+          wk.z = have ? pack_bf16x2(__uint_as_float(kv32[e + 4]) * p.scale, __uint_as_float(kv32[e + 5]) * p.scale) : 0u;
+          wk.w = have ? pack_bf16x2(__uint_as_float(kv32[e + 6]) * p.scale, __uint_as_float(kv32[e + 7]) * p.scale) : 0u;
+          wv.x = have ? pack_bf16x2(__uint_as_float(vv32[e]), __uint_as_float(vv32[e + 1])) : 0u;
+          wv.y = have ? pack_bf16x2(__uint_as_float(vv32[e + 2]), __uint_as_float(vv32[e + 3])) : 0u;
+          wv.z = have ? pack_bf16x2(__uint_as_float(vv32[e + 4]), __uint_as_float(vv32[e + 5])) : 0u;
+          wv.w = have ? pack_bf16x2(__uint_as_float(vv32[e + 6]), __uint_as_float(vv32[e + 7])) : 0u;
+          *reinterpret_cast<uint4 *>(dkp + c * 32 + e) = wk;
+          *reinterpret_cast<uint4 *>(dvp + c * 32 + e) = wv;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// dQ
+// ===========================================================================
+template <int D>
+struct LayoutB {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kChunks * kChunk128;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTile;
+  static constexpr int kK = kDO + kTile;   // [2]
+  static constexpr int kV = kK + 2 * kTile;  // [2]
+  static constexpr int kDS = kV + 2 * kTile;  // [128 rows x 128 keys] bf16
+  static constexpr int kBar = kDS + 2 * kChunk128;
+  static constexpr int kUsed = kBar + 256;
+  static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
+};
+
+struct BarsB {
+  uint64_t qdo_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], dp_full, ds_full,
+      dq_done;
+  uint32_t tmem_base;
+  Sync sync;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const BwdTcArgs a) {
+  using L = LayoutB<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  BarsB *b = reinterpret_cast<BarsB *>(smem + L::kBar);
+  const BwdParams &p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int m_tile = a.n_row_tiles - 1 - (int)blockIdx.x;
+  const int h = blockIdx.y;
+  const int seq = blockIdx.z;
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int i0 = m_tile * kTileRows;
+  if (i0 >= g.nq) return;
+  const KvRange kr = plan_kv_tiles(g.mask, g.nq, g.nk, i0, kTileRows, kTileKeys);
+  const int n_tiles = kr.n_end;
+  const int hk = h / a.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&b->qdo_full, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->k_full[s], 1);
+      mbar_init(&b->v_full[s], 1);
+      mbar_init(&b->k_empty[s], 1);
+      mbar_init(&b->v_empty[s], 1);
+      mbar_init(&b->s_full[s], 1);
+    }
+    mbar_init(&b->dp_full, 1);
+    mbar_init(&b->ds_full, 128);
+    mbar_init(&b->dq_done, 1);
+    b->sync.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&b->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  // TMEM columns: S[2] at 0 / 128, dP at 256, dQ at 384.
+  constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
+
+  const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+  const uint32_t sDS = smem_u32(smem + L::kDS);
+
+  if (warp == 0) {
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&b->qdo_full, 2 * L::kTile);
+      for (int c = 0; c < L::kChunks; c++) {
+        tma_load_3d(smem + L::kQ + c * kChunk128, &tm_q, &b->qdo_full, c * 64, h, g.q0 + i0);
+        tma_load_3d(smem + L::kDO + c * kChunk128, &tm_do, &b->qdo_full, c * 64, h, g.q0 + i0);
+      }
+      for (int jj = 0; jj < n_tiles; jj++) {
+        const int st = jj & 1, u = jj >> 1;
+        const int key_row = g.k0 + jj * kTileKeys;
+        if (jj >= 2 && !wait_bar(&b->sync, &b->k_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kK + st * L::kTile + c * kChunk128, &tm_k, &b->k_full[st], c * 64,
+                      hk, key_row);
+        if (jj >= 2 && !wait_bar(&b->sync, &b->v_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kV + st * L::kTile + c * kChunk128, &tm_v, &b->v_full[st], c * 64,
+                      hk, key_row);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32(128, kTileKeys, 0, 0);
+      constexpr uint32_t idesc_q = idesc_f16_f32(128, D, 0, 1);
+      auto issue_s = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+          const uint32_t off = (kk >> 2) * kChunk128 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + col, smem_desc_sw128(a_base + off, 16, 1024),
+                      smem_desc_sw128(b_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dq = [&](int st, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTileKeys / 16; kk++) {
+          const uint64_t ad = smem_desc_sw128(sDS + (kk >> 2) * kChunk128 + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sK + st * L::kTile + kk * 16 * 128, kChunk128, 1024);
+          mma_bf16_ss(tmem + kColDQ, ad, bd, idesc_q, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bar(&b->sync, &b->qdo_full, 0, p.err) &&
+                wait_bar(&b->sync, &b->k_full[0], 0, p.err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(sQ, sK, kColS);
+        mma_commit(&b->s_full[0]);
+        ok = wait_bar(&b->sync, &b->v_full[0], 0, p.err);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_s(sDO, sV, kColDP);
+        mma_commit(&b->dp_full);
+        mma_commit(&b->v_empty[0]);
+      }
+      for (int jj = 0; ok && jj < n_tiles; jj++) {
+        const int st = jj & 1;
+        const int s1 = (jj + 1) & 1, u1 = (jj + 1) >> 1;
+        if (jj + 1 < n_tiles) {
+          if (!wait_bar(&b->sync, &b->k_full[s1], u1 & 1, p.err)) break;
+          tc_fence_after();
+          issue_s(sQ, sK + s1 * L::kTile, kColS + s1 * kTileKeys);
+          mma_commit(&b->s_full[s1]);
+        }
+        if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
+        tc_fence_after();
+        issue_dq(st, jj > 0);
+        mma_commit(&b->dq_done);
+        mma_commit(&b->k_empty[st]);
+        if (jj + 1 < n_tiles) {
+          if (!wait_bar(&b->sync, &b->v_full[s1], u1 & 1, p.err)) break;
+          tc_fence_after();
+          issue_s(sDO, sV + s1 * L::kTile, kColDP);
+          mma_commit(&b->dp_full);
+          mma_commit(&b->v_empty[s1]);
+        }
+      }
+    }
+  } else {
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int i = i0 + r;
+    const bool row_in = i < g.nq;
+    const int t = g.q0 + i;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float c2 = p.scale_log2;
+    const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
+    const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
+    bool ok = true;
+    for (int jj = 0; jj < n_tiles; jj++) {
+      const int st = jj & 1;
+      ok = wait_bar(&b->sync, &b->s_full[st], (jj >> 1) & 1, p.err) &&
+           wait_bar(&b->sync, &b->dp_full, jj & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool boundary = jj >= kr.n_full;
+      const int jb = jj * kTileKeys;
+      uint32_t dd[kTileKeys / 2];
+#pragma unroll
+      for (int cc = 0; cc < kTileKeys / 32; cc++) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
+        tmem_ld32(t_lane + kColDP + cc * 32, dv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds[2];
+#pragma unroll
+          for (int q = 0; q < 2; q++) {
+            const int c = cc * 32 + e + q;
+            float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2);
+            if (boundary && !lane_allowed(g.mask, i, jb + c, g.nq, g.nk)) pv = 0.f;
+            ds[q] = pv * (__uint_as_float(dv[e + q]) - D_i);
+          }
+          dd[(cc * 32 + e) / 2] = pack_f16x2(ds[0], ds[1]);
+        }
+      }
+      if (jj > 0) ok = wait_bar(&b->sync, &b->dq_done, (jj - 1) & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int v = 0; v < kTileKeys / 8; v++) {
+        const uint32_t addr = sDS + (v >> 3) * kChunk128 + r * 128 + (((v & 7) ^ (r & 7)) << 4);
+        st_shared_v4(addr, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&b->ds_full);
+    }
+    if (ok && n_tiles > 0) {
+      if (wait_bar(&b->sync, &b->dq_done, (n_tiles - 1) & 1, p.err))
+        tc_fence_after();
+      else
+        ok = false;
+    }
+    const bool have = __all_sync(0xffffffffu, ok) && n_tiles > 0;
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)t * p.hq + h) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; c++) {
+      uint32_t q32[32];
+      if (have) {
+        tmem_ld32(t_lane + kColDQ + c * 32, q32);
+        tmem_wait_ld();
+      }
+      if (row_in) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = have ? pack_bf16x2(__uint_as_float(q32[e]) * p.scale, __uint_as_float(q32[e + 1]) * p.scale) : 0u;
+          w.y = have ? pack_bf16x2(__uint_as_float(q32[e + 2]) * p.scale, __uint_as_float(q32[e + 3]) * p.scale) : 0u;
+          w.z = have ? pack_bf16x2(__uint_as_float(q32[e + 4]) * p.scale, __uint_as_float(q32[e + 5]) * p.scale) : 0u;
+          w.w = have ? pack_bf16x2(__uint_as_float(q32[e + 6]) * p.scale, __uint_as_float(q32[e + 7]) * p.scale) : 0u;
+          *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes, bool *configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
+  const BwdParams &p = a.p;
+  // Every tensor-core product of the backward runs on the fp16 copies.
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap q64, do64, q128, do128, mk, mv;
+  if (!make_map(&q64, p.q16, D, p.hq, p.total_q, 1, kRowsA, f16) ||
+      !make_map(&do64, p.do16, D, p.hq, p.total_q, 1, kRowsA, f16) ||
+      !make_map(&q128, p.q16, D, p.hq, p.total_q, 1, kTileRows, f16) ||
+      !make_map(&do128, p.do16, D, p.hq, p.total_q, 1, kTileRows, f16) ||
+      !make_map(&mk, p.k16, D, p.hkv, p.total_k, 1, kTileKeys, f16) ||
+      !make_map(&mv, p.v16, D, p.hkv, p.total_k, 1, kTileKeys, f16))
+    return cudaErrorInvalidValue;
+  static bool conf_a[64] = {false}, conf_b[64] = {false};
+  cudaError_t e = set_smem(bwd_dkdv_tc_kernel<D>, LayoutA<D>::kAlloc, conf_a);
+  if (e != cudaSuccess) return e;
+  e = set_smem(bwd_dq_tc_kernel<D>, LayoutB<D>::kAlloc, conf_b);
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_tc_kernel<D><<<dim3(a.n_key_tiles, p.hkv, p.batch), kThreads, LayoutA<D>::kAlloc, st>>>(
+      q64, do64, mk, mv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_tc_kernel<D><<<dim3(a.n_row_tiles, p.hq, p.batch), kThreads, LayoutB<D>::kAlloc, st>>>(
+      q128, do128, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// The tensor-core backward after the preprocess kernel (D and lse2 ready).
+cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_t desc_len) {
+  BwdTcArgs a;
+  a.p = p;
+  a.group = p.hq / p.hkv;
+  a.n_key_tiles = (p.max_k + kKeysA - 1) / kKeysA;
+  a.n_row_tiles = (p.max_q + kTileRows - 1) / kTileRows;
+  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d grid_dkdv=(%d,%d,%d) grid_dq=(%d,%d,%d)",
+           p.d, p.d, a.n_key_tiles, p.hkv, p.batch, a.n_row_tiles, p.hq, p.batch);
+  if (a.n_key_tiles == 0 || a.n_row_tiles == 0) return cudaSuccess;
+  if (p.d == 64) return launch_d<64>(a, st);
+  return launch_d<128>(a, st);
+}
+
+}  // namespace attn

@@ -166,9 +166,10 @@ struct BwdParams {
   float scale, scale_log2;
   int mask;
   int *err;
-  float *dq_acc;   // [total_q, hq, d] fp32
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i
   float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)
+  // fp16 copies of the inputs for the tensor-core backward (NULL otherwise)
+  void *q16, *do16, *k16, *v16;
 };
 
 }  // namespace attn

@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "plan.h"
 #include "sm100.cuh"
+#include "tma_map.h"
 
 namespace attn {
 using namespace sm100;
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int n = n_begin + jj, sb = jj & 1;
-      if (!wait_or_abort(b, &b->s_full[sb], (jj >> 1) & 1, p.err)) {
+      ok = wait_or_abort(b, &b->s_full[sb], (jj >> 1) & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {  // leave together: tcgen05.ld is warp-wide
         ok = false;
         break;
       }
@@ -290,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (jj > 0) {
         // P V of the previous tile must be done: it reads the P buffer and
         // writes O, both of which are about to change.
-        if (!wait_or_abort(b, &b->o_done, (jj - 1) & 1, p.err)) {
+        ok = wait_or_abort(b, &b->o_done, (jj - 1) & 1, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
@@ -394,34 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// A [T, H, D] bf16 tensor seen as 3-D (d, head, token), loaded in boxes of
-// 64 features x box_h heads x box_t tokens with the 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int box_h, int box_t) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_h, (cuuint32_t)box_t};
-  cuuint32_t es[3] = {1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 template <int D>

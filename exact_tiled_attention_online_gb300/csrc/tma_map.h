@@ -1,0 +1,44 @@
+// tma_map.h -- host-side construction of the TMA tensor maps the kernels use.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// The driver's tensor-map encoder, looked up once through the runtime so the
+// library does not link libcuda directly.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// A [T, H, D] 16-bit (bf16 or fp16) tensor seen as 3-D (d, head, token), loaded in boxes of
+// 64 features x box_h heads x box_t tokens with the 128-byte swizzle (one
+// 128-byte row per (token, head), the K-major layout tcgen05 descriptors
+// expect).
+inline bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int box_h,
+                     int box_t,
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  auto enc = tensor_map_encoder();
+  if (!enc || T <= 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_h, (cuuint32_t)box_t};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, dt, 3, const_cast<void *>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace attn

@@ -66,7 +66,8 @@ typedef enum {
   ATTN_ERR_CUDA = 4,           /* a CUDA runtime call failed                 */
   ATTN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait expired              */
   ATTN_ERR_DEVICE_BOUNDS = 6,  /* cu_seqlens disagree with the sizes passed  */
-  ATTN_ERR_SCRATCH_LIMIT = 7   /* needs more than the static scratch holds   */
+  ATTN_ERR_SCRATCH_LIMIT = 7,  /* needs more than the static scratch holds   */
+  ATTN_ERR_DEVICE_RANGE = 8    /* a bf16 backward input is outside fp16 range */
 } attn_status;
 
 typedef enum {
@@ -119,10 +120,12 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
                      size_t workspace_bytes, void *stream);
 
 /*
- * Workspace bytes attn_bwd needs: an fp32 dQ accumulator [total_q,
- * n_heads_q, head_dim] and the per-row terms D_i = dO_i . O_i and the
- * base-2 logsumexp [n_heads_q, total_q] fp32 each.  (size_t)-1 for bad
- * arguments.
+ * Workspace bytes attn_bwd needs: the per-row terms D_i = dO_i . O_i and the
+ * base-2 logsumexp ([n_heads_q, total_q] fp32 each) and, for bf16, fp16
+ * copies of q, dout, k and v: the tensor-core backward multiplies in fp16 so
+ * that the probabilities P and the score gradients dS it feeds to the tensor
+ * cores keep 11 significant bits (bf16 keeps 8, which is not enough for a
+ * key seen by thousands of rows).  (size_t)-1 for bad arguments.
  */
 size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
                                int total_q, int total_k, int n_heads_q,
@@ -142,6 +145,8 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
  *   dq       [total_q, n_heads_q, head_dim]; dk, dv [total_k, n_heads_kv,
  *            head_dim]; type `dtype`.  Fully overwritten (rows no query
  *            reaches get zeros).
+ * For bf16, q, k, v and dout must lie inside the fp16 range (|x| < 65504);
+ * a larger value sets ATTN_ERR_DEVICE_RANGE on the device flag.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v,
                      const void *o, const float *lse, const float *o_f32,

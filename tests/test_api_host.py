@@ -33,7 +33,7 @@ def test_header_symbols_exported(lib):
 
 def test_version_and_strings(lib):
     assert lib.attn_version() >= 100
-    for code in range(7):
+    for code in range(9):
         assert attn.status_string(code)
 
 
@@ -68,9 +68,12 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.attn_bwd_workspace_size(1, 4, 4, 4, 4, 2, 1, 80, 0) == ctypes.c_size_t(-1).value
 
 
-def test_bwd_workspace_covers_accumulator(lib):
+def test_bwd_workspace_covers_rows_and_fp16_copies(lib):
     n = lib.attn_bwd_workspace_size(2, 100, 100, 200, 200, 4, 2, 128, 0)
-    assert n >= 200 * 4 * 128 * 4 + 2 * 4 * 200 * 4
+    rows = 2 * 4 * 200 * 4                         # D and lse2
+    copies = 2 * 200 * 4 * 128 * 2 + 2 * 200 * 2 * 128 * 2   # q, dout, k, v in fp16
+    assert n >= rows + copies
+    assert lib.attn_bwd_workspace_size(2, 100, 100, 200, 200, 4, 2, 128, 1) >= rows
 
 
 def test_bwd_rejects_missing_workspace(lib):

@@ -108,12 +108,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BwdParams &p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int n = blockIdx.x;  // key tile (early keys are seen by the most rows)
-  const int hk = blockIdx.y;
-  const int seq = blockIdx.z;
+  // One-dimensional grid, key-tile index slowest: early keys (seen by the
+  // most causal rows) of every (KV head, sequence) are scheduled first.
+  const int per_rank = p.hkv * p.batch;
+  const int n = (int)blockIdx.x / per_rank;
+  const int hk = (int)blockIdx.x % p.hkv;
+  const int seq = ((int)blockIdx.x % per_rank) / p.hkv;
   const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
   if (!g.ok) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+    if (threadIdx.x == 0 && n == 0 && hk == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -245,23 +248,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;  // key lane
     const int tid = threadIdx.x - 64;
     const int j = j0 + r;          // in-sequence key
+    const int rb = key_row_begin(g.mask, j, g.nq, g.nk);  // rows [rb, nq) see key j
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     bool ok = true;
+    // lse2 (threads 0..63) or D (64..127) of one row of a step's query tile;
+    // the next step's value is fetched while the current step computes.
+    auto row_value = [&](int it) {
+      const int c = tid & (kRowsA - 1);
+      const int i = it_row0(it) + c;
+      const size_t at = (size_t)it_head(it) * p.total_q + g.q0 + i;
+      if (tid < kRowsA) return i < g.nq ? p.lse2[at] : INFINITY;
+      return i < g.nq ? p.delta[at] : 0.f;
+    };
+    float next_val = n_it > 0 ? row_value(0) : 0.f;
     for (int it = 0; it < n_it; it++) {
       const int st = it & 1;
-      const int h = it_head(it), i0 = it_row0(it);
-      {  // lse2 and D of the 64 rows into shared memory
-        const int c = tid & (kRowsA - 1);
-        const int i = i0 + c;
-        float val;
-        if (tid < kRowsA)
-          val = i < g.nq ? p.lse2[(size_t)h * p.total_q + g.q0 + i] : INFINITY;
-        else
-          val = i < g.nq ? p.delta[(size_t)h * p.total_q + g.q0 + i] : 0.f;
-        sRow[st * 2 * kRowsA + tid] = val;
-      }
+      const int i0 = it_row0(it);
+      sRow[st * 2 * kRowsA + tid] = next_val;
       math_group_sync();  // every math thread reaches it once per step, even after an abort
+      if (it + 1 < n_it) next_val = row_value(it + 1);
       const float *lse2 = sRow + st * 2 * kRowsA;
       const float *dl = lse2 + kRowsA;
       if (ok)
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) continue;
       tc_fence_after();
-      const bool full = i0 + kRowsA <= g.nq && key_end(g.mask, i0, g.nq, g.nk) >= j0 + kKeysA;
+      const int c_lo = rb - i0, c_hi = g.nq - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
       uint32_t pp[kRowsA / 2], dd[kRowsA / 2];
 #pragma unroll
       for (int cc = 0; cc < kRowsA / 32; cc++) {
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 2; q++) {
             const int c = c0 + q;
             float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2[c]);
-            if (!full && !lane_allowed(g.mask, i0 + c, j, g.nq, g.nk)) pv = 0.f;
+            if (c < c_lo || c >= c_hi) pv = 0.f;
             pr[q] = pv;
             ds[q] = pv * (__uint_as_float(dv[e + q]) - dl[c]);
           }
@@ -393,12 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BwdParams &p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int m_tile = a.n_row_tiles - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y;
-  const int seq = blockIdx.z;
+  // One-dimensional grid, row-tile rank slowest: the last row tiles (most
+  // causal keys) of every (head, sequence) first.
+  const int per_rank = p.hq * p.batch;
+  const int rank = (int)blockIdx.x / per_rank;
+  const int h = (int)blockIdx.x % p.hq;
+  const int seq = ((int)blockIdx.x % per_rank) / p.hq;
+  const int m_tile = a.n_row_tiles - 1 - rank;
   const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
   if (!g.ok) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+    if (threadIdx.x == 0 && rank == 0 && h == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -527,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = g.q0 + i;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
+    const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
     const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
     const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
     bool ok = true;
@@ -541,10 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool boundary = jj >= kr.n_full;
       const int jb = jj * kTileKeys;
-      uint32_t dd[kTileKeys / 2];
+      // dQ of the previous tile was issued before this tile's dP, so it is
+      // complete by now; the dS buffer is free to overwrite chunk by chunk.
+      if (jj > 0) ok = wait_bar(&b->sync, &b->dq_done, (jj - 1) & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
 #pragma unroll
       for (int cc = 0; cc < kTileKeys / 32; cc++) {
-        uint32_t sv[32], dv[32];
+        uint32_t sv[32], dv[32], dd[16];
         tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
         tmem_ld32(t_lane + kColDP + cc * 32, dv);
         tmem_wait_ld();
@@ -555,21 +572,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 2; q++) {
             const int c = cc * 32 + e + q;
             float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2);
-            if (boundary && !lane_allowed(g.mask, i, jb + c, g.nq, g.nk)) pv = 0.f;
+            if (boundary && jb + c >= row_limit) pv = 0.f;
             ds[q] = pv * (__uint_as_float(dv[e + q]) - D_i);
           }
-          dd[(cc * 32 + e) / 2] = pack_f16x2(ds[0], ds[1]);
+          dd[e / 2] = pack_f16x2(ds[0], ds[1]);
         }
-      }
-      if (jj > 0) ok = wait_bar(&b->sync, &b->dq_done, (jj - 1) & 1, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
 #pragma unroll
-      for (int v = 0; v < kTileKeys / 8; v++) {
-        const uint32_t addr = sDS + (v >> 3) * kChunk128 + r * 128 + (((v & 7) ^ (r & 7)) << 4);
-        st_shared_v4(addr, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2], dd[4 * v + 3]);
+        for (int w = 0; w < 4; w++) {
+          const int v = cc * 4 + w;  // 16-byte vector: keys 8v .. 8v+7
+          const uint32_t addr = sDS + (v >> 3) * kChunk128 + r * 128 + (((v & 7) ^ (r & 7)) << 4);
+          st_shared_v4(addr, dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -643,12 +656,13 @@ cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = set_smem(bwd_dq_tc_kernel<D>, LayoutB<D>::kAlloc, conf_b);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_tc_kernel<D><<<dim3(a.n_key_tiles, p.hkv, p.batch), kThreads, LayoutA<D>::kAlloc, st>>>(
-      q64, do64, mk, mv, a);
+  const long long ga = (long long)a.n_key_tiles * p.hkv * p.batch;
+  const long long gb = (long long)a.n_row_tiles * p.hq * p.batch;
+  if (ga >= (1LL << 31) || gb >= (1LL << 31)) return cudaErrorInvalidValue;
+  bwd_dkdv_tc_kernel<D><<<(unsigned)ga, kThreads, LayoutA<D>::kAlloc, st>>>(q64, do64, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<D><<<dim3(a.n_row_tiles, p.hq, p.batch), kThreads, LayoutB<D>::kAlloc, st>>>(
-      q128, do128, mk, mv, a);
+  bwd_dq_tc_kernel<D><<<(unsigned)gb, kThreads, LayoutB<D>::kAlloc, st>>>(q128, do128, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -661,8 +675,9 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_
   a.group = p.hq / p.hkv;
   a.n_key_tiles = (p.max_k + kKeysA - 1) / kKeysA;
   a.n_row_tiles = (p.max_q + kTileRows - 1) / kTileRows;
-  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d grid_dkdv=(%d,%d,%d) grid_dq=(%d,%d,%d)",
-           p.d, p.d, a.n_key_tiles, p.hkv, p.batch, a.n_row_tiles, p.hq, p.batch);
+  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d ctas_dkdv=%lld ctas_dq=%lld",
+           p.d, p.d, (long long)a.n_key_tiles * p.hkv * p.batch,
+           (long long)a.n_row_tiles * p.hq * p.batch);
   if (a.n_key_tiles == 0 || a.n_row_tiles == 0) return cudaSuccess;
   if (p.d == 64) return launch_d<64>(a, st);
   return launch_d<128>(a, st);

@@ -102,10 +102,23 @@ __host__ __device__ __forceinline__ void split_tiles(int n_end, int split, int n
   *b = lo + per < n_end ? lo + per : n_end;
 }
 
-// Per-element predicate for tile lanes on a boundary tile: in-sequence row i,
-// key j.  Out-of-range rows and keys are never allowed.
+// Per-lane predicate on a boundary tile, hoisted per row: lane (row i, key j)
+// is allowed iff j < row_key_limit(i).  Out-of-range rows get 0, so none of
+// their lanes are allowed; keys past the sequence end are never allowed
+// because key_end() <= nk.
+__host__ __device__ __forceinline__ int row_key_limit(int mask, int i, int nq, int nk) {
+  return i < nq ? key_end(mask, i, nq, nk) : 0;
+}
+
 __host__ __device__ __forceinline__ bool lane_allowed(int mask, int i, int j, int nq, int nk) {
-  return i < nq && j < key_end(mask, i, nq, nk);
+  return j < row_key_limit(mask, i, nq, nk);
+}
+
+// The same predicate hoisted per key (the backward's transposed tiles): lane
+// (row i, key j) is allowed iff key_row_begin(j) <= i < nq.  For j >= nk no
+// row is allowed.
+__host__ __device__ __forceinline__ int key_row_begin(int mask, int j, int nq, int nk) {
+  return j < nk ? row_begin(mask, j, nq, nk) : nq;
 }
 
 // ---------------------------------------------------------------------------

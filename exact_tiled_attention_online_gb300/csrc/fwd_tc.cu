@@ -108,13 +108,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const FwdParams &p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int m_tile = a.n_m_tiles - 1 - (int)blockIdx.x;  // longest causal rows first
-  const int head_idx = blockIdx.y;
-  const int split = (int)blockIdx.z % a.n_splits;
-  const int seq = (int)blockIdx.z / a.n_splits;
+  // One-dimensional grid, the query-tile rank slowest: every (head, split,
+  // sequence) gets its last query tile (the longest causal rows) before any
+  // gets a shorter one, so the block scheduler hands out the heaviest tiles
+  // first.
+  const int n_heads = a.pack ? p.hkv : p.hq;
+  const int per_rank = n_heads * p.batch * a.n_splits;
+  const int rank = (int)blockIdx.x / per_rank;
+  const int rem = (int)blockIdx.x % per_rank;
+  const int head_idx = rem % n_heads;
+  const int split = (rem / n_heads) % a.n_splits;
+  const int seq = rem / (n_heads * a.n_splits);
+  const int m_tile = a.n_m_tiles - 1 - rank;
   const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
   if (!g.ok) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && split == 0)
+    if (threadIdx.x == 0 && rank == 0 && head_idx == 0 && split == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -236,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     row_map(a, head_idx, i0, r, &i, &h);
     const bool row_in = i < g.nq;
     const int t = g.q0 + i;
+    const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
@@ -248,43 +257,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float sv[kTileKeys];
+      uint32_t raw[kTileKeys];
 #pragma unroll
       for (int c = 0; c < kTileKeys / 32; c++) {
         uint32_t u32[32];
         tmem_ld32(t_lane + sb * kTileKeys + c * 32, u32);
 #pragma unroll
-        for (int e = 0; e < 32; e++) sv[c * 32 + e] = __uint_as_float(u32[e]) * c2;
+        for (int e = 0; e < 32; e++) raw[c * 32 + e] = u32[e];
       }
       tmem_wait_ld();
-      if (n >= kr.n_full) {  // boundary tile: per-lane mask
-        const int j0 = n * kTileKeys;
+      if (n >= kr.n_full) {  // boundary tile: keys at or past this row's limit
+        const int limit = row_limit - n * kTileKeys;
 #pragma unroll
         for (int c = 0; c < kTileKeys; c++)
-          if (!lane_allowed(g.mask, i, j0 + c, g.nq, g.nk)) sv[c] = -INFINITY;
+          if (c >= limit) raw[c] = 0xff800000u;  // -inf
       }
-      float mt = sv[0];
+      float mt;
+      if (c2 > 0.f) {  // the max of the raw scores scales to the max of the logits
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 1; c < kTileKeys; c++) mt = fmaxf(mt, sv[c]);
+        for (int c = 0; c < kTileKeys; c++) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(raw[c]));
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
+      } else {  // scale <= 0: scale first, keep masked lanes at -inf
+        mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTileKeys; c++) {
+          const float x = __uint_as_float(raw[c]);
+          const float y = x == -INFINITY ? -INFINITY : x * c2;
+          raw[c] = __float_as_uint(y);
+          mt = fmaxf(mt, y);
+        }
+      }
+      const float cm = c2 > 0.f ? c2 : 1.f;  // multiplier still to apply to raw
       const float m_new = mt > m_ref + kRescaleLog2 ? mt : m_ref;
       const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
       const float base = m_new == -INFINITY ? 0.f : m_new;
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kTileKeys; c++) {
-        sv[c] = fast_exp2(sv[c] - base);
-        rs += sv[c];
-      }
-      // Two denominators: l sums the fp32 probabilities and gives lse; lr
-      // sums the bf16-rounded probabilities that the P V product uses, so
-      // O / lr is an exact convex combination of V rows and a common offset
-      // in V cancels instead of carrying P's rounding error.
+      // P = 2^(raw * c - base) two lanes per instruction; two denominators:
+      // l sums the fp32 probabilities and gives lse; lr sums the bf16-rounded
+      // probabilities that the P V product uses, so O / lr is an exact convex
+      // combination of V rows and a common offset in V cancels instead of
+      // carrying P's rounding error.
+      const uint64_t cx2 = f2(cm, cm), nb2 = f2(-base, -base);
+      uint64_t s2[4] = {0, 0, 0, 0}, r2[4] = {0, 0, 0, 0};
       uint32_t pk[kTileKeys / 2];
-      float rr = 0.f;
 #pragma unroll
       for (int c = 0; c < kTileKeys / 2; c++) {
-        pk[c] = pack_bf16x2(sv[2 * c], sv[2 * c + 1]);
-        rr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        const uint64_t x = ffma2(f2(__uint_as_float(raw[2 * c]), __uint_as_float(raw[2 * c + 1])),
+                                 cx2, nb2);
+        float x0, x1;
+        f2_split(x, x0, x1);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        s2[c & 3] = fadd2(s2[c & 3], f2(p0, p1));
+        pk[c] = pack_bf16x2(p0, p1);
+        r2[c & 3] = fadd2(r2[c & 3], f2(__uint_as_float(pk[c] << 16),
+                                        __uint_as_float(pk[c] & 0xffff0000u)));
+      }
+      float rs, rr;
+      {
+        float a0, a1, b0, b1;
+        f2_split(fadd2(fadd2(s2[0], s2[1]), fadd2(s2[2], s2[3])), a0, a1);
+        f2_split(fadd2(fadd2(r2[0], r2[1]), fadd2(r2[2], r2[3])), b0, b1);
+        rs = a0 + a1;
+        rr = b0 + b1;
       }
       l = l * alpha + rs;
       lr = lr * alpha + rr;
@@ -432,10 +466,12 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
       !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys) ||
       !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys))
     return cudaErrorInvalidValue;
-  const long long gz = (long long)p.batch * plan.n_splits;
-  dim3 grid(plan.n_m_tiles, plan.pack ? p.hkv : p.hq, (unsigned)gz);
-  snprintf(desc, desc_len, "fwd_tc_d%d%s grid=(%u,%u,%u) tile_tokens=%d splits=%d%s", p.d,
-           plan.pack ? "_packgqa" : "", grid.x, grid.y, grid.z, plan.tile_tokens, plan.n_splits,
+  const long long ctas = (long long)plan.n_m_tiles * (plan.pack ? p.hkv : p.hq) * p.batch *
+                         plan.n_splits;
+  if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)ctas);
+  snprintf(desc, desc_len, "fwd_tc_d%d%s ctas=%lld tile_tokens=%d splits=%d%s", p.d,
+           plan.pack ? "_packgqa" : "", ctas, plan.tile_tokens, plan.n_splits,
            plan.n_splits > 1 ? " +combine" : "");
   if (p.d == 64) return launch_d<64>(a, mq, mk, mv, grid, st);
   return launch_d<128>(a, mq, mk, mv, grid, st);

@@ -18,6 +18,7 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_
 cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st,
                           char *desc, size_t desc_len);
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
+cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
 cudaError_t launch_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
                               int max_k, int total_q, int total_k, int mask, int tile_rows,
                               uint8_t *out, int *err, cudaStream_t st);
@@ -188,8 +189,15 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                                              align256((size_t)plan.n_splits * total_q * hq * d * 4));
       p.n_splits = plan.n_splits;
     }
-    ce = launch_fwd_tc(p, plan, cs, desc, sizeof(desc));
+    if (plan.kind == PLAN_TC && !plan.pack)
+      ce = launch_fwd_tc2(p, cs, desc, sizeof(desc));  // prefill: two query tiles per CTA
+    else
+      ce = launch_fwd_tc(p, plan, cs, desc, sizeof(desc));
     if (ce == cudaSuccess && plan.kind == PLAN_TC_SPLIT) ce = launch_combine(p, plan, cs);
+  }
+  if (ce != cudaSuccess) {  // keep the runtime's reason with the plan
+    const size_t n = strlen(desc);
+    snprintf(desc + n, sizeof(desc) - n, " [launch failed: %s]", cudaGetErrorString(ce));
   }
   set_plan(desc);
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -258,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c = tid & (kRowsA - 1);
       const int i = it_row0(it) + c;
       const size_t at = (size_t)it_head(it) * p.total_q + g.q0 + i;
-      if (tid < kRowsA) return i < g.nq ? p.lse2[at] : INFINITY;
-      return i < g.nq ? p.delta[at] : 0.f;
+      // stored negated: the math below adds them
+      if (tid < kRowsA) return i < g.nq ? -p.lse2[at] : -INFINITY;
+      return i < g.nq ? -p.delta[at] : 0.f;
     };
     float next_val = n_it > 0 ? row_value(0) : 0.f;
     for (int it = 0; it < n_it; it++) {
@@ -268,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sRow[st * 2 * kRowsA + tid] = next_val;
       math_group_sync();  // every math thread reaches it once per step, even after an abort
       if (it + 1 < n_it) next_val = row_value(it + 1);
-      const float *lse2 = sRow + st * 2 * kRowsA;
-      const float *dl = lse2 + kRowsA;
+      const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
+      const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
       if (ok)
         ok = wait_bar(&b->sync, &b->s_full[st], (it >> 1) & 1, p.err) &&
              wait_bar(&b->sync, &b->dp_full[st], (it >> 1) & 1, p.err);
@@ -277,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) continue;
       tc_fence_after();
       const int c_lo = rb - i0, c_hi = g.nq - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
+      const bool full = c_lo <= 0 && c_hi >= kRowsA;
+      const uint64_t c2x2 = f2(c2, c2);
       uint32_t pp[kRowsA / 2], dd[kRowsA / 2];
 #pragma unroll
       for (int cc = 0; cc < kRowsA / 32; cc++) {
@@ -287,17 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int c0 = cc * 32 + e;
-          float pr[2], ds[2];
-#pragma unroll
-          for (int q = 0; q < 2; q++) {
-            const int c = c0 + q;
-            float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2[c]);
-            if (c < c_lo || c >= c_hi) pv = 0.f;
-            pr[q] = pv;
-            ds[q] = pv * (__uint_as_float(dv[e + q]) - dl[c]);
+          // two lanes per instruction: x = c S - lse2, P = 2^x, dS = P (dP - D)
+          const float2 nl = *reinterpret_cast<const float2 *>(nlse2 + c0);
+          const float2 ndd = *reinterpret_cast<const float2 *>(nd + c0);
+          float x0, x1;
+          f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, f2(nl.x, nl.y)),
+                   x0, x1);
+          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (!full) {
+            if (c0 < c_lo || c0 >= c_hi) p0 = 0.f;
+            if (c0 + 1 < c_lo || c0 + 1 >= c_hi) p1 = 0.f;
           }
-          pp[c0 / 2] = pack_f16x2(pr[0], pr[1]);
-          dd[c0 / 2] = pack_f16x2(ds[0], ds[1]);
+          const uint64_t pv = f2(p0, p1);
+          float d0, d1;
+          f2_split(fmul2(pv, fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                   f2(ndd.x, ndd.y))),
+                   d0, d1);
+          pp[c0 / 2] = pack_f16x2(p0, p1);
+          dd[c0 / 2] = pack_f16x2(d0, d1);
         }
       }
       if (it >= 2) ok = wait_bar(&b->sync, &b->mm_done[st], ((it >> 1) - 1) & 1, p.err);
@@ -540,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
     const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
     const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
+    const uint64_t c2x2 = f2(c2, c2), nl2 = f2(-lse2, -lse2), nd2 = f2(-D_i, -D_i);
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int st = jj & 1;
@@ -567,15 +578,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float ds[2];
-#pragma unroll
-          for (int q = 0; q < 2; q++) {
-            const int c = cc * 32 + e + q;
-            float pv = fast_exp2(__uint_as_float(sv[e + q]) * c2 - lse2);
-            if (boundary && jb + c >= row_limit) pv = 0.f;
-            ds[q] = pv * (__uint_as_float(dv[e + q]) - D_i);
+          const int c = cc * 32 + e;
+          float x0, x1;
+          f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, nl2), x0, x1);
+          float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (boundary) {
+            if (jb + c >= row_limit) p0 = 0.f;
+            if (jb + c + 1 >= row_limit) p1 = 0.f;
           }
-          dd[e / 2] = pack_f16x2(ds[0], ds[1]);
+          float d0, d1;
+          f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)),
+                   d0, d1);
+          dd[e / 2] = pack_f16x2(d0, d1);
         }
 #pragma unroll
         for (int w = 0; w < 4; w++) {

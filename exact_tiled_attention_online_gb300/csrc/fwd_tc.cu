@@ -96,7 +96,9 @@ __device__ __forceinline__ void row_map(const TcArgs &a, int head_idx, int i0, i
   }
 }
 
-template <int D>
+// kPosScale: scale > 0, so the max of the raw scores gives the max of the
+// logits (the common case); otherwise the scores are scaled before the max.
+template <int D, bool kPosScale>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c >= limit) raw[c] = 0xff800000u;  // -inf
       }
       float mt;
-      if (c2 > 0.f) {  // the max of the raw scores scales to the max of the logits
+      if constexpr (kPosScale) {  // the max of the raw scores scales to the max of the logits
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kTileKeys; c++) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(raw[c]));
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt = fmaxf(mt, y);
         }
       }
-      const float cm = c2 > 0.f ? c2 : 1.f;  // multiplier still to apply to raw
+      const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw
       const float m_new = mt > m_ref + kRescaleLog2 ? mt : m_ref;
       const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
       const float base = m_new == -INFINITY ? 0.f : m_new;
@@ -433,19 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kPos>
 cudaError_t launch_d(const TcArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
                      const CUtensorMap &mv, dim3 grid, cudaStream_t st) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, kPos>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc_kernel<D, kPos><<<grid, kThreads, Layout<D>::kAlloc, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -473,8 +476,11 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
   snprintf(desc, desc_len, "fwd_tc_d%d%s ctas=%lld tile_tokens=%d splits=%d%s", p.d,
            plan.pack ? "_packgqa" : "", ctas, plan.tile_tokens, plan.n_splits,
            plan.n_splits > 1 ? " +combine" : "");
-  if (p.d == 64) return launch_d<64>(a, mq, mk, mv, grid, st);
-  return launch_d<128>(a, mq, mk, mv, grid, st);
+  const bool pos = p.scale_log2 > 0.f;
+  if (p.d == 64) return pos ? launch_d<64, true>(a, mq, mk, mv, grid, st)
+                            : launch_d<64, false>(a, mq, mk, mv, grid, st);
+  return pos ? launch_d<128, true>(a, mq, mk, mv, grid, st)
+             : launch_d<128, false>(a, mq, mk, mv, grid, st);
 }
 
 }  // namespace attn

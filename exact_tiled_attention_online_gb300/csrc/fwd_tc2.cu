@@ -1,0 +1,431 @@
+// fwd_tc2.cu -- tensor-core prefill forward with two query tiles per CTA.
+//
+// Same arithmetic as fwd_tc.cu (the online-softmax recurrence of the
+// "formal-correctness" page, "The FlashAttention Proof"; masks from the tile
+// planner of common.cuh), scheduled so the tensor core never waits on one
+// softmax: a CTA owns 256 query rows of one head as two 128-row tiles A and B
+// that share every K/V tile, and the MMA thread interleaves their products
+//
+//   QK_A(n), QK_B(n), PV_A(n), QK_A(n+1), PV_B(n), QK_B(n+1), PV_A(n+1), ...
+//
+// so that while one softmax warpgroup turns its S into P, the tensor core is
+// busy with the other tile.  Warps: 0 TMA producer, 1 TMEM allocation and MMA
+// issue, 2..5 softmax of tile A, 6..9 softmax of tile B (thread = row = TMEM
+// lane).  TMEM: S_A, S_B, O_A, O_B; each tile's bf16 P overwrites the first
+// half of its S and feeds P V from tensor memory, so P never passes through
+// shared memory.  Shared memory: Q_A, Q_B and a 2-stage K/V ring.
+//
+// The softmax reads S from TMEM twice (once for the row max, once for the
+// exponentials) 32 columns at a time, so a thread holds at most 32 scores and
+// the 64 packed probabilities.
+#include <stdio.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "plan.h"
+#include "sm100.cuh"
+#include "tma_map.h"
+
+namespace attn {
+using namespace sm100;
+
+namespace {
+
+constexpr int kThreads2 = 320;
+constexpr float kRescale2 = 8.0f;
+constexpr uint32_t kCols2 = 512;
+
+template <int D>
+struct Layout2 {
+  static constexpr int kChunk = 128 * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kChunks * kChunk;
+  static constexpr int kQA = 0;
+  static constexpr int kK = 2 * kTile;      // [2] stages
+  static constexpr int kV = kK + 2 * kTile;  // [2] stages
+  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kUsed = kBar + 256;
+  static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
+};
+
+struct Tc2Args {
+  FwdParams p;
+  int group;
+  int n_pairs;  // 256-row query tiles per (sequence, head)
+};
+
+struct Bars2 {
+  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];  // [tile A, tile B]
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, int *err) {
+  if (*reinterpret_cast<volatile int *>(&b->abort)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *reinterpret_cast<volatile int *>(&b->abort) = 1;
+  raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
+  return false;
+}
+
+template <int D, bool kPosScale>
+__global__ void __launch_bounds__(kThreads2, 1)
+    fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
+  using L = Layout2<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
+  Bars2 *b = reinterpret_cast<Bars2 *>(smem + L::kBar);
+  const FwdParams &p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // One-dimensional grid, the 256-row tile rank slowest (longest causal rows
+  // of every (head, sequence) first).
+  const int per_rank = p.hq * p.batch;
+  const int rank = (int)blockIdx.x / per_rank;
+  const int h = (int)blockIdx.x % p.hq;
+  const int seq = ((int)blockIdx.x % per_rank) / p.hq;
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  if (!g.ok) {
+    if (threadIdx.x == 0 && rank == 0 && h == 0) raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int i0 = (a.n_pairs - 1 - rank) * 2 * kTileRows;  // first row of tile A
+  if (i0 >= g.nq) return;
+  const KvRange kra = plan_kv_tiles(g.mask, g.nq, g.nk, i0, kTileRows, kTileKeys);
+  const KvRange krb = plan_kv_tiles(g.mask, g.nq, g.nk, i0 + kTileRows, kTileRows, kTileKeys);
+  const int na = kra.n_end, nb = krb.n_end;  // tile X is active on key tiles [0, n_X)
+  const int N = na > nb ? na : nb;
+  const int hk = h / a.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&b->q_full, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->k_full[s], 1);
+      mbar_init(&b->v_full[s], 1);
+      mbar_init(&b->k_empty[s], 1);
+      mbar_init(&b->v_empty[s], 1);
+      mbar_init(&b->s_full[s], 1);
+      mbar_init(&b->p_full[s], 128);
+      mbar_init(&b->pv_done[s], 1);
+    }
+    b->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&b->tmem_base, kCols2);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b->tmem_base;
+  // TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + D.
+  const uint32_t sQ = smem_u32(smem + L::kQA);
+  const uint32_t sK = smem_u32(smem + L::kK);
+  const uint32_t sV = smem_u32(smem + L::kV);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && N > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
+      for (int t2 = 0; t2 < 2; t2++)
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full, c * 64, h,
+                      g.q0 + i0 + t2 * kTileRows);
+      for (int n = 0; n < N; n++) {
+        const int st = n & 1, u = n >> 1;
+        const int key_row = g.k0 + n * kTileKeys;
+        if (n >= 2 && !wait2(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
+                      hk, key_row);
+        if (n >= 2 && !wait2(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+        for (int c = 0; c < L::kChunks; c++)
+          tma_load_3d(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st], c * 64,
+                      hk, key_row);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0 && N > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+      auto issue_qk = [&](int x, int st) {  // S_x = Q_x K^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk++) {
+          const uint32_t off = (kk >> 2) * L::kChunk + (kk & 3) * 32;
+          mma_bf16_ss(tmem + (uint32_t)(x * kTileKeys),
+                      smem_desc_sw128(sQ + x * L::kTile + off, 16, 1024),
+                      smem_desc_sw128(sK + st * L::kTile + off, 16, 1024), idesc_qk,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
+#pragma unroll
+        for (int kk = 0; kk < kTileKeys / 16; kk++)
+          mma_bf16_ts(tmem + 256u + (uint32_t)(x * D), tmem + (uint32_t)(x * kTileKeys + kk * 8),
+                      smem_desc_sw128(sV + st * L::kTile + kk * 16 * 128, L::kChunk, 1024),
+                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
+      if (ok) {
+        tc_fence_after();
+        if (na > 0) {
+          issue_qk(0, 0);
+          mma_commit(&b->s_full[0]);
+        }
+        if (nb > 0) {
+          issue_qk(1, 0);
+          mma_commit(&b->s_full[1]);
+        }
+        mma_commit(&b->k_empty[0]);
+      }
+      for (int n = 0; ok && n < N; n++) {
+        const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
+        bool v_ready = false, k1_ready = false;
+        if (n < na) {
+          if (!(ok = wait2(b, &b->p_full[0], n & 1, p.err))) break;
+          if (!(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
+          v_ready = true;
+          tc_fence_after();
+          issue_pv(0, st, n > 0);
+          mma_commit(&b->pv_done[0]);
+        }
+        if (n1 < na) {
+          if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
+          k1_ready = true;
+          tc_fence_after();
+          issue_qk(0, st1);
+          mma_commit(&b->s_full[0]);
+        }
+        if (n < nb) {
+          if (!(ok = wait2(b, &b->p_full[1], n & 1, p.err))) break;
+          if (!v_ready && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
+          tc_fence_after();
+          issue_pv(1, st, n > 0);
+          mma_commit(&b->pv_done[1]);
+        }
+        mma_commit(&b->v_empty[st]);
+        if (n1 < nb) {
+          if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
+          tc_fence_after();
+          issue_qk(1, st1);
+          mma_commit(&b->s_full[1]);
+        }
+        if (n1 < N) mma_commit(&b->k_empty[st1]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = warp >= 6 ? 1 : 0;  // tile A (0) or B (1)
+    const int wq = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;
+    const int i = i0 + x * kTileRows + r;
+    const bool row_in = i < g.nq;
+    const int t = g.q0 + i;
+    const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
+    const int n_mine = x ? nb : na;
+    const int n_full = x ? krb.n_full : kra.n_full;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_col = t_lane + (uint32_t)(x * kTileKeys);
+    const uint32_t o_col = t_lane + 256u + (uint32_t)(x * D);
+    const float c2 = p.scale_log2;
+    const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
+    float m_ref = -INFINITY, l = 0.f, lr = 0.f;
+    bool ok = true;
+    // Scores of `nc` consecutive 32-column chunks starting at chunk c0, loaded
+    // with one TMEM wait: raw (kPosScale) or scaled, masked to -inf.
+    auto load_chunks = [&](auto nc_tag, int c0, int limit, bool boundary, uint32_t *v) {
+      constexpr int nc = decltype(nc_tag)::value;
+#pragma unroll
+      for (int c = 0; c < nc; c++)
+        tmem_ld32(s_col + (c0 + c) * 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_wait_ld();
+      if (boundary) {
+#pragma unroll
+        for (int e = 0; e < 32 * nc; e++)
+          if (c0 * 32 + e >= limit) v[e] = 0xff800000u;
+      }
+      if constexpr (!kPosScale) {
+#pragma unroll
+        for (int e = 0; e < 32 * nc; e++) {
+          const float y = __uint_as_float(v[e]);
+          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : y * c2);
+        }
+      }
+    };
+    for (int n = 0; n < n_mine; n++) {
+      ok = wait2(b, &b->s_full[x], n & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool boundary = n >= n_full;
+      const int limit = row_limit - n * kTileKeys;
+      // pass 1: row max, 64 scores per TMEM wait
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < kTileKeys / 64; c++) {
+        uint32_t v[64];
+        load_chunks(std::integral_constant<int, 2>{}, 2 * c, limit, boundary, v);
+#pragma unroll
+        for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v[e]));
+      }
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if (kPosScale) mt *= c2;
+      const float m_new = mt > m_ref + kRescale2 ? mt : m_ref;
+      const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
+      const float base = m_new == -INFINITY ? 0.f : m_new;
+      // pass 2: P = 2^(raw * c - base), two lanes per instruction; l sums fp32
+      // P (for lse), lr the bf16-rounded P that P V uses (so O / lr is an
+      // exact convex combination of V rows).
+      const uint64_t cx2 = f2(cm, cm), nb2 = f2(-base, -base);
+      uint64_t s2[2] = {0, 0}, r2[2] = {0, 0};
+      // Each half of 64 scores becomes 32 packed bf16 pairs, written over
+      // S columns [32 c, 32 c + 32): those scores were read in half 0.
+#pragma unroll
+      for (int c = 0; c < kTileKeys / 64; c++) {
+        uint32_t v[64], pk[32];
+        load_chunks(std::integral_constant<int, 2>{}, 2 * c, limit, boundary, v);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float x0, x1;
+          f2_split(ffma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), cx2, nb2), x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          const int k = e / 2;
+          s2[k & 1] = fadd2(s2[k & 1], f2(p0, p1));
+          pk[k] = pack_bf16x2(p0, p1);
+          r2[k & 1] = fadd2(r2[k & 1], f2(__uint_as_float(pk[k] << 16),
+                                          __uint_as_float(pk[k] & 0xffff0000u)));
+        }
+        tmem_st32(s_col + c * 32, pk);
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_split(fadd2(s2[0], s2[1]), a0, a1);
+        f2_split(fadd2(r2[0], r2[1]), b0, b1);
+        l = l * alpha + (a0 + a1);
+        lr = lr * alpha + (b0 + b1);
+      }
+      m_ref = m_new;
+      // S_x(n) landed after every earlier product of this thread, so the
+      // previous P V into O_x is complete: O_x may be rescaled now.
+      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; c++) {
+          uint32_t o32[32];
+          tmem_ld32(o_col + c * 32, o32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e++) o32[e] = __float_as_uint(__uint_as_float(o32[e]) * alpha);
+          tmem_st32(o_col + c * 32, o32);
+        }
+      }
+      tmem_wait_st();  // P (first 64 columns of S_x) and any rescaled O are in place
+      tc_fence_before();
+      mbar_arrive(&b->p_full[x]);
+    }
+    if (ok && n_mine > 0) {
+      ok = wait2(b, &b->pv_done[x], (n_mine - 1) & 1, p.err);
+      if (ok) tc_fence_after();
+    }
+    // ------------------------------------------------------------ epilogue
+    const bool have = __all_sync(0xffffffffu, ok) && n_mine > 0;
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
+    const float lse2 = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t * p.hq + h) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; c++) {
+      uint32_t o32[32];
+      if (have) {
+        tmem_ld32(o_col + c * 32, o32);
+        tmem_wait_ld();
+      }
+      if (row_in) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = have ? pack_bf16x2(__uint_as_float(o32[e]) * inv, __uint_as_float(o32[e + 1]) * inv) : 0u;
+          w.y = have ? pack_bf16x2(__uint_as_float(o32[e + 2]) * inv, __uint_as_float(o32[e + 3]) * inv) : 0u;
+          w.z = have ? pack_bf16x2(__uint_as_float(o32[e + 4]) * inv, __uint_as_float(o32[e + 5]) * inv) : 0u;
+          w.w = have ? pack_bf16x2(__uint_as_float(o32[e + 6]) * inv, __uint_as_float(o32[e + 7]) * inv) : 0u;
+          *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+        }
+        if (p.o_f32) {
+          float *df = p.o_f32 + ((size_t)t * p.hq + h) * D + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 f;
+            f.x = have ? __uint_as_float(o32[e]) * inv : 0.f;
+            f.y = have ? __uint_as_float(o32[e + 1]) * inv : 0.f;
+            f.z = have ? __uint_as_float(o32[e + 2]) * inv : 0.f;
+            f.w = have ? __uint_as_float(o32[e + 3]) * inv : 0.f;
+            *reinterpret_cast<float4 *>(df + e) = f;
+          }
+        }
+      }
+    }
+    if (row_in && p.lse) p.lse[(size_t)h * p.total_q + t] = have ? lse2 * kLn2 : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols2);
+  }
+}
+
+template <int D, bool kPos>
+cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                    const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Layout2<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  fwd_tc2_kernel<D, kPos><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Prefill plan (one head per tile, no key splits) with two query tiles per CTA.
+cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len) {
+  Tc2Args a;
+  a.p = p;
+  a.group = p.hq / p.hkv;
+  a.n_pairs = (p.max_q + 2 * kTileRows - 1) / (2 * kTileRows);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, 1, kTileRows) ||
+      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys) ||
+      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys))
+    return cudaErrorInvalidValue;
+  const long long ctas = (long long)a.n_pairs * p.hq * p.batch;
+  if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
+  snprintf(desc, desc_len, "fwd_tc2_d%d ctas=%lld rows_per_cta=256", p.d, ctas);
+  if (ctas == 0) return cudaSuccess;
+  const bool pos = p.scale_log2 > 0.f;
+  if (p.d == 64)
+    return pos ? launch2<64, true>(a, mq, mk, mv, (unsigned)ctas, st)
+               : launch2<64, false>(a, mq, mk, mv, (unsigned)ctas, st);
+  return pos ? launch2<128, true>(a, mq, mk, mv, (unsigned)ctas, st)
+             : launch2<128, false>(a, mq, mk, mv, (unsigned)ctas, st);
+}
+
+}  // namespace attn

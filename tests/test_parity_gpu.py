@@ -134,3 +134,18 @@ def test_bad_cu_seqlens_sets_device_flag():
     attn.fwd(x["q"], x["k"], x["v"], bad, x["cu_seqlens_k"], 12, 8, TL)
     assert attn.get_device_error() == 6
     assert attn.get_device_error() == 0  # cleared by the read
+
+
+@pytest.mark.parametrize("scale", [-0.07, 0.0])
+def test_non_positive_scale(scale):
+    """scale <= 0 takes the path that scales scores before the row max."""
+    w = inputs.custom("negscale", (130, 7), (200, 7), 4, 2, 128, "bf16", BR, seed=5)
+    x = inputs.make_inputs(w)
+    d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
+    o, lse = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
+                      w.max_k, w.mask, scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"],
+                                scale, w.mask)
+    compare.check_close("o", o, o_ref)
+    compare.check_lse("lse", lse, lse_ref)

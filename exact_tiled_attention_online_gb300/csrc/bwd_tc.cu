@@ -80,9 +80,7 @@ struct LayoutA {
   static constexpr int kV = kK + kKV;
   static constexpr int kQ = kV + kKV;         // [2] stages
   static constexpr int kDO = kQ + 2 * kQT;    // [2]
-  static constexpr int kPT = kDO + 2 * kQT;   // [2] x [128 keys x 64 rows] bf16
-  static constexpr int kDST = kPT + 2 * kChunk128;
-  static constexpr int kRow = kDST + 2 * kChunk128;  // [2] x {lse2[64], D[64]}
+  static constexpr int kRow = kDO + 2 * kQT;  // [2] x {-lse2[64], -D[64]}
   static constexpr int kBar = kRow + 2 * 2 * kRowsA * 4;
   static constexpr int kUsed = kBar + 512;
   static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
@@ -156,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
   const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
-  const uint32_t sPT = smem_u32(smem + L::kPT), sDST = smem_u32(smem + L::kDST);
   float *sRow = reinterpret_cast<float *>(smem + L::kRow);
 
   auto it_head = [&](int it) { return hk * a.group + it / n_m; };
@@ -199,13 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + col, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      // acc [128 keys x d] += A [128 keys x 64 rows] * B [64 rows x d]
-      auto issue_grad = [&](uint32_t a_base, uint32_t b_base, uint32_t col, bool acc) {
+      // acc [128 keys x d] += A [128 keys x 64 rows] * B [64 rows x d], A in
+      // tensor memory (two fp16 rows per 32-bit column)
+      auto issue_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t col, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kRowsA / 16; kk++) {
-          const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, kChunk64, 1024);
-          mma_bf16_ss(tmem + col, ad, bd, idesc_g, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + col, tmem + a_col + kk * 8, bd, idesc_g, (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
@@ -236,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!wait_bar(&b->sync, &b->ps_full[st], (it >> 1) & 1, p.err)) break;
         tc_fence_after();
-        issue_grad(sPT + st * kChunk128, sDO + st * L::kQT, kColDV, it > 0);
-        issue_grad(sDST + st * kChunk128, sQ + st * L::kQT, kColDK, it > 0);
+        issue_grad(kColS + st * kRowsA, sDO + st * L::kQT, kColDV, it > 0);
+        issue_grad(kColDP + st * kRowsA, sQ + st * L::kQT, kColDK, it > 0);
         mma_commit(&b->mm_done[st]);
         mma_commit(&b->q_empty[st]);
         mma_commit(&b->do_empty[st]);
@@ -310,19 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           dd[c0 / 2] = pack_f16x2(d0, d1);
         }
       }
-      if (it >= 2) ok = wait_bar(&b->sync, &b->mm_done[st], ((it >> 1) - 1) & 1, p.err);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) continue;
-      // [128 keys x 64 rows] K-major, 128-byte swizzle: key r's 128 bytes
-#pragma unroll
-      for (int v = 0; v < kRowsA / 8; v++) {
-        const uint32_t off = r * 128 + (((v & 7) ^ (r & 7)) << 4);
-        st_shared_v4(sPT + st * kChunk128 + off, pp[4 * v], pp[4 * v + 1], pp[4 * v + 2],
-                     pp[4 * v + 3]);
-        st_shared_v4(sDST + st * kChunk128 + off, dd[4 * v], dd[4 * v + 1], dd[4 * v + 2],
-                     dd[4 * v + 3]);
-      }
-      fence_proxy_async_smem();
+      // P^T over the first 32 columns of S^T, dS^T over those of dP^T (all
+      // scores of this step are read): the A operands of the two gradient
+      // products, straight from tensor memory.
+      tmem_st32(t_lane + kColS + st * kRowsA, pp);
+      tmem_st32(t_lane + kColDP + st * kRowsA, dd);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ps_full[st]);
     }
@@ -383,8 +373,7 @@ struct LayoutB {
   static constexpr int kDO = kQ + kTile;
   static constexpr int kK = kDO + kTile;   // [2]
   static constexpr int kV = kK + 2 * kTile;  // [2]
-  static constexpr int kDS = kV + 2 * kTile;  // [128 rows x 128 keys] bf16
-  static constexpr int kBar = kDS + 2 * kChunk128;
+  static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kUsed = kBar + 256;
   static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
 };
@@ -456,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
   const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-  const uint32_t sDS = smem_u32(smem + L::kDS);
 
   if (warp == 0) {
     if (lane == 0 && n_tiles > 0) {
@@ -494,12 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       smem_desc_sw128(b_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_dq = [&](int st, bool acc) {
+      auto issue_dq = [&](int st, bool acc) {  // dQ += dS K, dS in tensor memory
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; kk++) {
-          const uint64_t ad = smem_desc_sw128(sDS + (kk >> 2) * kChunk128 + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(sK + st * L::kTile + kk * 16 * 128, kChunk128, 1024);
-          mma_bf16_ss(tmem + kColDQ, ad, bd, idesc_q, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColDQ, tmem + kColS + st * kTileKeys + kk * 8, bd, idesc_q,
+                      (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = wait_bar(&b->sync, &b->qdo_full, 0, p.err) &&
@@ -563,16 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool boundary = jj >= kr.n_full;
       const int jb = jj * kTileKeys;
-      // dQ of the previous tile was issued before this tile's dP, so it is
-      // complete by now; the dS buffer is free to overwrite chunk by chunk.
-      if (jj > 0) ok = wait_bar(&b->sync, &b->dq_done, (jj - 1) & 1, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      // dS (fp16 pairs) goes over the first 64 columns of this tile's S, 32
+      // columns at a time, each after the scores under it have been read.
+      uint32_t dd[32];
 #pragma unroll
       for (int cc = 0; cc < kTileKeys / 32; cc++) {
-        uint32_t sv[32], dv[32], dd[16];
+        uint32_t sv[32], dv[32];
         tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
         tmem_ld32(t_lane + kColDP + cc * 32, dv);
         tmem_wait_ld();
@@ -589,16 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float d0, d1;
           f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)),
                    d0, d1);
-          dd[e / 2] = pack_f16x2(d0, d1);
+          dd[(cc & 1) * 16 + e / 2] = pack_f16x2(d0, d1);
         }
-#pragma unroll
-        for (int w = 0; w < 4; w++) {
-          const int v = cc * 4 + w;  // 16-byte vector: keys 8v .. 8v+7
-          const uint32_t addr = sDS + (v >> 3) * kChunk128 + r * 128 + (((v & 7) ^ (r & 7)) << 4);
-          st_shared_v4(addr, dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
-        }
+        if (cc & 1) tmem_st32(t_lane + kColS + st * kTileKeys + (cc >> 1) * 32, dd);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ds_full);
     }

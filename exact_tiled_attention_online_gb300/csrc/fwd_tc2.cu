@@ -159,22 +159,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (lane == 0 && N > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
+      // Descriptors are built once; a byte offset below 256 KB adds to the
+      // start-address field (16-byte units) without carrying out of it.
+      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(sV, L::kChunk, 1024);
       auto issue_qk = [&](int x, int st) {  // S_x = Q_x K^T
+        const uint64_t dq = dQ0 + (uint64_t)((x * L::kTile) >> 4);
+        const uint64_t dk = dK0 + (uint64_t)((st * L::kTile) >> 4);
+        const uint32_t d_tmem = tmem + (uint32_t)(x * kTileKeys);
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
-          const uint32_t off = (kk >> 2) * L::kChunk + (kk & 3) * 32;
-          mma_bf16_ss(tmem + (uint32_t)(x * kTileKeys),
-                      smem_desc_sw128(sQ + x * L::kTile + off, 16, 1024),
-                      smem_desc_sw128(sK + st * L::kTile + off, 16, 1024), idesc_qk,
-                      kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((((kk >> 2) * L::kChunk) + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
+        const uint64_t dv = dV0 + (uint64_t)((st * L::kTile) >> 4);
+        const uint32_t d_tmem = tmem + 256u + (uint32_t)(x * D);
+        const uint32_t a_tmem = tmem + (uint32_t)(x * kTileKeys);
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; kk++)
-          mma_bf16_ts(tmem + 256u + (uint32_t)(x * D), tmem + (uint32_t)(x * kTileKeys + kk * 8),
-                      smem_desc_sw128(sV + st * L::kTile + kk * 16 * 128, L::kChunk, 1024),
-                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
+                      (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
       if (ok) {

@@ -11,7 +11,7 @@
 // so that while one softmax warpgroup turns its S into P, the tensor core is
 // busy with the other tile.  Warps: 0 TMA producer, 1 TMEM allocation and MMA
 // issue, 2..5 softmax of tile A, 6..9 softmax of tile B (thread = row = TMEM
-// lane).  TMEM: S_A, S_B, O_A, O_B; each tile's bf16 P overwrites the first
+// lane).  TMEM: S_A, S_B, O_A, O_B; each tile's bf16 P overwrites the second
 // half of its S and feeds P V from tensor memory, so P never passes through
 // shared memory.  Shared memory: Q_A, Q_B and a 2-stage K/V ring.
 //
@@ -70,7 +70,12 @@ __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, 
   return false;
 }
 
-template <int D, bool kPosScale>
+// kPosScale: scale > 0 (the row max of the raw scores gives the max of the
+// logits).  kRoundedSum: also sum the bf16-rounded probabilities so the fp32
+// output is an exact convex combination of V rows (wanted when the caller
+// keeps that output for the backward); without it O is normalised by the
+// fp32 sum.
+template <int D, bool kPosScale, bool kRoundedSum>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
         const uint64_t dv = dV0 + (uint64_t)((st * L::kTile) >> 4);
         const uint32_t d_tmem = tmem + 256u + (uint32_t)(x * D);
-        const uint32_t a_tmem = tmem + (uint32_t)(x * kTileKeys);
+        const uint32_t a_tmem = tmem + (uint32_t)(x * kTileKeys + 64);  // P: S columns [64, 128)
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; kk++)
           mma_bf16_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
@@ -279,15 +284,19 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_after();
       const bool boundary = n >= n_full;
       const int limit = row_limit - n * kTileKeys;
-      // pass 1: row max, 64 scores per TMEM wait
+      // pass 1: row max, 64 scores per TMEM wait; the second half stays in
+      // registers for pass 2
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      uint32_t v1[64];
+      {
+        uint32_t v0[64];
+        load_chunks(std::integral_constant<int, 2>{}, 0, limit, boundary, v0);
 #pragma unroll
-      for (int c = 0; c < kTileKeys / 64; c++) {
-        uint32_t v[64];
-        load_chunks(std::integral_constant<int, 2>{}, 2 * c, limit, boundary, v);
-#pragma unroll
-        for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v[e]));
+        for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v0[e]));
       }
+      load_chunks(std::integral_constant<int, 2>{}, 2, limit, boundary, v1);
+#pragma unroll
+      for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v1[e]));
       float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       if (kPosScale) mt *= c2;
       const float m_new = mt > m_ref + kRescale2 ? mt : m_ref;
@@ -298,12 +307,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // exact convex combination of V rows).
       const uint64_t cx2 = f2(cm, cm), nb2 = f2(-base, -base);
       uint64_t s2[2] = {0, 0}, r2[2] = {0, 0};
-      // Each half of 64 scores becomes 32 packed bf16 pairs, written over
-      // S columns [32 c, 32 c + 32): those scores were read in half 0.
-#pragma unroll
-      for (int c = 0; c < kTileKeys / 64; c++) {
-        uint32_t v[64], pk[32];
-        load_chunks(std::integral_constant<int, 2>{}, 2 * c, limit, boundary, v);
+      // Each half of 64 scores becomes 32 packed bf16 pairs; P goes over S
+      // columns [64, 128), whose scores pass 1 left in registers: half 1
+      // first, then half 0 reloaded from columns [0, 64), which P never
+      // touches.
+      auto exp_half = [&](const uint32_t (&v)[64], uint32_t (&pk)[32]) {
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           float x0, x1;
@@ -312,17 +320,28 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const int k = e / 2;
           s2[k & 1] = fadd2(s2[k & 1], f2(p0, p1));
           pk[k] = pack_bf16x2(p0, p1);
-          r2[k & 1] = fadd2(r2[k & 1], f2(__uint_as_float(pk[k] << 16),
-                                          __uint_as_float(pk[k] & 0xffff0000u)));
+          if constexpr (kRoundedSum)
+            r2[k & 1] = fadd2(r2[k & 1], f2(__uint_as_float(pk[k] << 16),
+                                            __uint_as_float(pk[k] & 0xffff0000u)));
         }
-        tmem_st32(s_col + c * 32, pk);
+      };
+      {
+        uint32_t pk[32];
+        exp_half(v1, pk);
+        tmem_st32(s_col + 96, pk);
+      }
+      {
+        uint32_t v0[64], pk[32];
+        load_chunks(std::integral_constant<int, 2>{}, 0, limit, boundary, v0);
+        exp_half(v0, pk);
+        tmem_st32(s_col + 64, pk);
       }
       {
         float a0, a1, b0, b1;
         f2_split(fadd2(s2[0], s2[1]), a0, a1);
         f2_split(fadd2(r2[0], r2[1]), b0, b1);
         l = l * alpha + (a0 + a1);
-        lr = lr * alpha + (b0 + b1);
+        lr = kRoundedSum ? lr * alpha + (b0 + b1) : l;
       }
       m_ref = m_new;
       // S_x(n) landed after every earlier product of this thread, so the
@@ -338,7 +357,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           tmem_st32(o_col + c * 32, o32);
         }
       }
-      tmem_wait_st();  // P (first 64 columns of S_x) and any rescaled O are in place
+      tmem_wait_st();  // P (S columns [64, 128)) and any rescaled O are in place
       tc_fence_before();
       mbar_arrive(&b->p_full[x]);
     }
@@ -393,21 +412,31 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-template <int D, bool kPos>
+template <int D, bool kPos, bool kRs>
 cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                     const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout2<D>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc2_kernel<D, kPos><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc2_kernel<D, kPos, kRs><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                      const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
+  const bool pos = a.p.scale_log2 > 0.f, rs = a.p.o_f32 != nullptr;
+  if (pos) return rs ? launch2<D, true, true>(a, mq, mk, mv, ctas, st)
+                     : launch2<D, true, false>(a, mq, mk, mv, ctas, st);
+  return rs ? launch2<D, false, true>(a, mq, mk, mv, ctas, st)
+            : launch2<D, false, false>(a, mq, mk, mv, ctas, st);
 }
 
 }  // namespace
@@ -427,12 +456,8 @@ cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size
   if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
   snprintf(desc, desc_len, "fwd_tc2_d%d ctas=%lld rows_per_cta=256", p.d, ctas);
   if (ctas == 0) return cudaSuccess;
-  const bool pos = p.scale_log2 > 0.f;
-  if (p.d == 64)
-    return pos ? launch2<64, true>(a, mq, mk, mv, (unsigned)ctas, st)
-               : launch2<64, false>(a, mq, mk, mv, (unsigned)ctas, st);
-  return pos ? launch2<128, true>(a, mq, mk, mv, (unsigned)ctas, st)
-             : launch2<128, false>(a, mq, mk, mv, (unsigned)ctas, st);
+  if (p.d == 64) return launch2_d<64>(a, mq, mk, mv, (unsigned)ctas, st);
+  return launch2_d<128>(a, mq, mk, mv, (unsigned)ctas, st);
 }
 
 }  // namespace attn

@@ -26,6 +26,7 @@ ranks and ``value`` sums the ranks' work.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -171,11 +172,15 @@ class ClockSampler:
 class Runner:
     """Inputs, outputs and workspaces of one workload, allocated once."""
 
-    def __init__(self, name, device, gen_device):
+    def __init__(self, name, device, gen_device, batch_div=1):
         from exact_tiled_attention_online_gb300 import attn
         self.attn = attn
         self.name = name
         self.w = inputs.WORKLOADS[name]
+        if batch_div > 1:  # a smaller case of the same kernels, for profiler captures
+            w = self.w
+            b = max(1, w.batch // batch_div)
+            self.w = dataclasses.replace(w, seqlens_q=w.seqlens_q[:b], seqlens_k=w.seqlens_k[:b])
         x = inputs.make_inputs(self.w, device=device, gen_device=gen_device)
         self.x = x
         w = self.w
@@ -246,7 +251,7 @@ def time_gpu(args, rank, world, device):
     runners = {}
     for n in names:
         big = n.startswith("decode") or n == "train_fwd_bwd"
-        runners[n] = Runner(n, device, device if big else "cpu")
+        runners[n] = Runner(n, device, device if big else "cpu", args.batch_div)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
@@ -394,6 +399,9 @@ def main():
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch-div", type=int, default=1,
+                    help="divide every workload's batch (smaller cases for profiler captures; "
+                         "not a benchmark setting)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -37,7 +37,9 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 math
+// warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 math: two warps per TMEM lane
+// quarter, each taking half of a row's columns
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunk128 = 128 * 128;  // [128 rows x 64 bf16] swizzled chunk
 constexpr int kChunk64 = 64 * 128;    // [64 rows x 64 bf16] swizzled chunk
@@ -62,7 +64,7 @@ __device__ __forceinline__ bool wait_bar(Sync *sy, uint64_t *bar, uint32_t parit
 }
 
 __device__ __forceinline__ void math_group_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
 // ===========================================================================
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b->do_empty[s], 1);
       mbar_init(&b->s_full[s], 1);
       mbar_init(&b->dp_full[s], 1);
-      mbar_init(&b->ps_full[s], 128);
+      mbar_init(&b->ps_full[s], 256);
       mbar_init(&b->mm_done[s], 1);
     }
     b->sync.abort = 0;
@@ -187,35 +189,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_it > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32(128, kRowsA, 0, 0);
       constexpr uint32_t idesc_g = idesc_f16_f32(128, D, 0, 1);
+      // Descriptors built once; byte offsets below 256 KB add to the
+      // start-address field (16-byte units).
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dQk = smem_desc_sw128(sQ, 16, 1024), dDOk = smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dQm = smem_desc_sw128(sQ, kChunk64, 1024);
+      const uint64_t dDOm = smem_desc_sw128(sDO, kChunk64, 1024);
       // S^T (or dP^T) = A_tile [128 keys x d] * B_tile [64 rows x d]^T
-      auto issue_st = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+      auto issue_st = [&](uint64_t da, uint64_t db, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
-          const uint64_t ad = smem_desc_sw128(a_base + (kk >> 2) * kChunk128 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(b_base + (kk >> 2) * kChunk64 + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + col, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t oa = (uint64_t)((((kk >> 2) * kChunk128) + (kk & 3) * 32) >> 4);
+          const uint64_t ob = (uint64_t)((((kk >> 2) * kChunk64) + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + col, da + oa, db + ob, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       // acc [128 keys x d] += A [128 keys x 64 rows] * B [64 rows x d], A in
-      // tensor memory (two fp16 rows per 32-bit column)
-      auto issue_grad = [&](uint32_t a_col, uint32_t b_base, uint32_t col, bool acc) {
+      // tensor memory: rows [32 h, 32 h + 32) as 16 packed columns at 32 h
+      auto issue_grad = [&](uint32_t a_col, uint64_t db, uint32_t col, bool acc) {
 #pragma unroll
-        for (int kk = 0; kk < kRowsA / 16; kk++) {
-          const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, kChunk64, 1024);
-          mma_bf16_ts(tmem + col, tmem + a_col + kk * 8, bd, idesc_g, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kRowsA / 16; kk++)
+          mma_bf16_ts(tmem + col, tmem + a_col + 32 * (kk >> 1) + 8 * (kk & 1),
+                      db + (uint64_t)((kk * 16 * 128) >> 4), idesc_g, (acc || kk > 0) ? 1u : 0u);
       };
+      auto qoff = [&](int s1) { return (uint64_t)((s1 * L::kQT) >> 4); };
       bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
                 wait_bar(&b->sync, &b->q_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
-        issue_st(sK, sQ, kColS);
+        issue_st(dK0, dQk, kColS);
         mma_commit(&b->s_full[0]);
         ok = wait_bar(&b->sync, &b->do_full[0], 0, p.err);
       }
       if (ok) {
         tc_fence_after();
-        issue_st(sV, sDO, kColDP);
+        issue_st(dV0, dDOk, kColDP);
         mma_commit(&b->dp_full[0]);
       }
       for (int it = 0; ok && it < n_it; it++) {
@@ -224,17 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s1 = (it + 1) & 1, u1 = (it + 1) >> 1;
           if (!wait_bar(&b->sync, &b->q_full[s1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_st(sK, sQ + s1 * L::kQT, kColS + s1 * kRowsA);
+          issue_st(dK0, dQk + qoff(s1), kColS + s1 * kRowsA);
           mma_commit(&b->s_full[s1]);
           if (!wait_bar(&b->sync, &b->do_full[s1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_st(sV, sDO + s1 * L::kQT, kColDP + s1 * kRowsA);
+          issue_st(dV0, dDOk + qoff(s1), kColDP + s1 * kRowsA);
           mma_commit(&b->dp_full[s1]);
         }
         if (!wait_bar(&b->sync, &b->ps_full[st], (it >> 1) & 1, p.err)) break;
         tc_fence_after();
-        issue_grad(kColS + st * kRowsA, sDO + st * L::kQT, kColDV, it > 0);
-        issue_grad(kColDP + st * kRowsA, sQ + st * L::kQT, kColDK, it > 0);
+        issue_grad(kColS + st * kRowsA, dDOm + qoff(st), kColDV, it > 0);
+        issue_grad(kColDP + st * kRowsA, dQm + qoff(st), kColDK, it > 0);
         mma_commit(&b->mm_done[st]);
         mma_commit(&b->q_empty[st]);
         mma_commit(&b->do_empty[st]);
@@ -242,8 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // key lane
-    const int tid = threadIdx.x - 64;
+    const int half = (warp - 2) >> 2;  // query rows [32 half, 32 half + 32) of each step
+    const int r = wq * 32 + lane;      // key lane
+    const int tid = threadIdx.x - 64;  // 0 .. 255; threads below 128 fetch row terms
     const int j = j0 + r;          // in-sequence key
     const int rb = key_row_begin(g.mask, j, g.nq, g.nk);  // rows [rb, nq) see key j
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
@@ -259,13 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < kRowsA) return i < g.nq ? -p.lse2[at] : -INFINITY;
       return i < g.nq ? -p.delta[at] : 0.f;
     };
-    float next_val = n_it > 0 ? row_value(0) : 0.f;
+    const bool fetcher = tid < 2 * kRowsA;
+    float next_val = (n_it > 0 && fetcher) ? row_value(0) : 0.f;
     for (int it = 0; it < n_it; it++) {
       const int st = it & 1;
       const int i0 = it_row0(it);
-      sRow[st * 2 * kRowsA + tid] = next_val;
+      if (fetcher) sRow[st * 2 * kRowsA + tid] = next_val;
       math_group_sync();  // every math thread reaches it once per step, even after an abort
-      if (it + 1 < n_it) next_val = row_value(it + 1);
+      if (fetcher && it + 1 < n_it) next_val = row_value(it + 1);
       const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
       const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
       if (ok)
@@ -277,9 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c_lo = rb - i0, c_hi = g.nq - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
       const bool full = c_lo <= 0 && c_hi >= kRowsA;
       const uint64_t c2x2 = f2(c2, c2);
-      uint32_t pp[kRowsA / 2], dd[kRowsA / 2];
-#pragma unroll
-      for (int cc = 0; cc < kRowsA / 32; cc++) {
+      uint32_t pp[16], dd[16];
+      {
+        const int cc = half;  // this warp's 32 rows of the step
         uint32_t sv[32], dv[32];
         tmem_ld32(t_lane + kColS + st * kRowsA + cc * 32, sv);
         tmem_ld32(t_lane + kColDP + st * kRowsA + cc * 32, dv);
@@ -303,15 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_split(fmul2(pv, fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
                                    f2(ndd.x, ndd.y))),
                    d0, d1);
-          pp[c0 / 2] = pack_f16x2(p0, p1);
-          dd[c0 / 2] = pack_f16x2(d0, d1);
+          pp[e / 2] = pack_f16x2(p0, p1);
+          dd[e / 2] = pack_f16x2(d0, d1);
         }
       }
-      // P^T over the first 32 columns of S^T, dS^T over those of dP^T (all
-      // scores of this step are read): the A operands of the two gradient
-      // products, straight from tensor memory.
-      tmem_st32(t_lane + kColS + st * kRowsA, pp);
-      tmem_st32(t_lane + kColDP + st * kRowsA, dd);
+      // P^T over the first 16 of the 32 S^T columns this warp just read, dS^T
+      // likewise over dP^T: the A operands of the two gradient products,
+      // straight from tensor memory.
+      tmem_st16(t_lane + kColS + st * kRowsA + half * 32, pp);
+      tmem_st16(t_lane + kColDP + st * kRowsA + half * 32, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ps_full[st]);
@@ -324,15 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
     }
     const bool have = __all_sync(0xffffffffu, ok) && n_it > 0;
-    const size_t krow = ((size_t)(g.k0 + (j < g.nk ? j : 0)) * p.hkv + hk) * D;
+    // this warp writes output columns [half D / 2, half D / 2 + D / 2)
+    const size_t krow = ((size_t)(g.k0 + (j < g.nk ? j : 0)) * p.hkv + hk) * D + half * (D / 2);
     __nv_bfloat16 *dkp = reinterpret_cast<__nv_bfloat16 *>(p.dk) + krow;
     __nv_bfloat16 *dvp = reinterpret_cast<__nv_bfloat16 *>(p.dv) + krow;
 #pragma unroll
-    for (int c = 0; c < D / 32; c++) {
+    for (int c = 0; c < D / 64; c++) {
       uint32_t kv32[32], vv32[32];
       if (have) {  // warp-uniform: every lane of the warp loads
-        tmem_ld32(t_lane + kColDK + c * 32, kv32);
-        tmem_ld32(t_lane + kColDV + c * 32, vv32);
+        tmem_ld32(t_lane + kColDK + half * (D / 2) + c * 32, kv32);
+        tmem_ld32(t_lane + kColDV + half * (D / 2) + c * 32, vv32);
         tmem_wait_ld();
       }
       if (j < g.nk) {  // keys past the sequence end own no storage
@@ -427,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b->s_full[s], 1);
     }
     mbar_init(&b->dp_full, 1);
-    mbar_init(&b->ds_full, 128);
+    mbar_init(&b->ds_full, 256);
     mbar_init(&b->dq_done, 1);
     b->sync.abort = 0;
     fence_mbar_init();
@@ -474,33 +485,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32(128, kTileKeys, 0, 0);
       constexpr uint32_t idesc_q = idesc_f16_f32(128, D, 0, 1);
-      auto issue_s = [&](uint32_t a_base, uint32_t b_base, uint32_t col) {
+      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dKm = smem_desc_sw128(sK, kChunk128, 1024);
+      auto toff = [&](int s1) { return (uint64_t)((s1 * L::kTile) >> 4); };
+      auto issue_s = [&](uint64_t da, uint64_t db, uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
-          const uint32_t off = (kk >> 2) * kChunk128 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + col, smem_desc_sw128(a_base + off, 16, 1024),
-                      smem_desc_sw128(b_base + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((((kk >> 2) * kChunk128) + (kk & 3) * 32) >> 4);
+          mma_bf16_ss(tmem + col, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_dq = [&](int st, bool acc) {  // dQ += dS K, dS in tensor memory
+      // dQ += dS K, dS in tensor memory: keys [64 h, 64 h + 64) as 32 packed
+      // columns at 64 h of this tile's S buffer
+      auto issue_dq = [&](int st, bool acc) {
 #pragma unroll
-        for (int kk = 0; kk < kTileKeys / 16; kk++) {
-          const uint64_t bd = smem_desc_sw128(sK + st * L::kTile + kk * 16 * 128, kChunk128, 1024);
-          mma_bf16_ts(tmem + kColDQ, tmem + kColS + st * kTileKeys + kk * 8, bd, idesc_q,
+        for (int kk = 0; kk < kTileKeys / 16; kk++)
+          mma_bf16_ts(tmem + kColDQ, tmem + kColS + st * kTileKeys + 64 * (kk >> 2) + 8 * (kk & 3),
+                      dKm + toff(st) + (uint64_t)((kk * 16 * 128) >> 4), idesc_q,
                       (acc || kk > 0) ? 1u : 0u);
-        }
       };
       bool ok = wait_bar(&b->sync, &b->qdo_full, 0, p.err) &&
                 wait_bar(&b->sync, &b->k_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
-        issue_s(sQ, sK, kColS);
+        issue_s(dQ0, dK0, kColS);
         mma_commit(&b->s_full[0]);
         ok = wait_bar(&b->sync, &b->v_full[0], 0, p.err);
       }
       if (ok) {
         tc_fence_after();
-        issue_s(sDO, sV, kColDP);
+        issue_s(dDO0, dV0, kColDP);
         mma_commit(&b->dp_full);
         mma_commit(&b->v_empty[0]);
       }
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj + 1 < n_tiles) {
           if (!wait_bar(&b->sync, &b->k_full[s1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_s(sQ, sK + s1 * L::kTile, kColS + s1 * kTileKeys);
+          issue_s(dQ0, dK0 + toff(s1), kColS + s1 * kTileKeys);
           mma_commit(&b->s_full[s1]);
         }
         if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj + 1 < n_tiles) {
           if (!wait_bar(&b->sync, &b->v_full[s1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_s(sDO, sV + s1 * L::kTile, kColDP);
+          issue_s(dDO0, dV0 + toff(s1), kColDP);
           mma_commit(&b->dp_full);
           mma_commit(&b->v_empty[s1]);
         }
@@ -529,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int wq = warp & 3;
+    const int half = (warp - 2) >> 2;  // keys [64 half, 64 half + 64) of each tile
     const int r = wq * 32 + lane;
     const int i = i0 + r;
     const bool row_in = i < g.nq;
@@ -551,11 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool boundary = jj >= kr.n_full;
       const int jb = jj * kTileKeys;
-      // dS (fp16 pairs) goes over the first 64 columns of this tile's S, 32
-      // columns at a time, each after the scores under it have been read.
+      // dS (fp16 pairs) of this warp's 64 keys goes over the first 32 of the
+      // S columns it read.
       uint32_t dd[32];
 #pragma unroll
-      for (int cc = 0; cc < kTileKeys / 32; cc++) {
+      for (int cc = 2 * half; cc < 2 * half + 2; cc++) {
         uint32_t sv[32], dv[32];
         tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
         tmem_ld32(t_lane + kColDP + cc * 32, dv);
@@ -575,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    d0, d1);
           dd[(cc & 1) * 16 + e / 2] = pack_f16x2(d0, d1);
         }
-        if (cc & 1) tmem_st32(t_lane + kColS + st * kTileKeys + (cc >> 1) * 32, dd);
       }
+      tmem_st32(t_lane + kColS + st * kTileKeys + half * 64, dd);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ds_full);
@@ -588,12 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
     }
     const bool have = __all_sync(0xffffffffu, ok) && n_tiles > 0;
-    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)t * p.hq + h) * D;
+    // this warp writes dQ columns [half D / 2, half D / 2 + D / 2)
+    __nv_bfloat16 *dst =
+        reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)t * p.hq + h) * D + half * (D / 2);
 #pragma unroll
-    for (int c = 0; c < D / 32; c++) {
+    for (int c = 0; c < D / 64; c++) {
       uint32_t q32[32];
       if (have) {
-        tmem_ld32(t_lane + kColDQ + c * 32, q32);
+        tmem_ld32(t_lane + kColDQ + half * (D / 2) + c * 32, q32);
         tmem_wait_ld();
       }
       if (row_in) {

@@ -388,6 +388,58 @@ def cpu_baseline(workload: str, budget_s: float = 12.0):
             "sample": f"{n} random (token, head) rows of {workload}, forward, fp64"}
 
 
+def run_sweep(args):
+    """Prefill forward over a range of sequence lengths with batch, heads,
+    head width, dtype and mask family fixed ("attention-algorithm-error-and-
+    complexity-tests", fifth paragraph): one JSON line per length with the
+    parameters beside the time, then the fitted exponent of time against N
+    (dense causal attention keeps quadratic pair work, so about 2 once the
+    GPU is full)."""
+    from exact_tiled_attention_online_gb300 import attn
+    attn.library()
+    device = torch.device("cuda", 0)
+    lengths = [int(x) for x in args.sweep.split(",")]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    points = []
+    for n in lengths:
+        w = inputs.custom(f"sweep_{n}", (n,) * args.sweep_batch, (n,) * args.sweep_batch, 32, 8,
+                          128, "bf16", inputs.MASK_TOP_LEFT, seed=2000 + n)
+        x = inputs.make_inputs(w, device=device, gen_device=device)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty((w.hq, w.total_q), dtype=torch.float32, device=device)
+
+        def run():
+            attn.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q,
+                     w.max_k, w.mask, w.scale, out=o, lse=lse)
+        for _ in range(args.warmup):
+            run()
+        ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        med = statistics.median(ms)
+        fl = fwd_flops(w)
+        points.append((n, med))
+        print(json.dumps({"sweep": "prefill_fwd", "seq_len": n, "batch": w.batch, "heads_q": w.hq,
+                          "heads_kv": w.hkv, "head_dim": w.d, "dtype": "bf16",
+                          "mask": "causal_top_left", "allowed_pairs": allowed_pairs(w),
+                          "ms_median": med, "tflops": fl / (med * 1e-3) / 1e12,
+                          "plan": attn.last_plan()}))
+    if len(points) >= 2:
+        lx = np.log([p[0] for p in points])
+        ly = np.log([p[1] for p in points])
+        slope = float(np.polyfit(lx[-3:], ly[-3:], 1)[0]) if len(points) >= 3 else \
+            float((ly[-1] - ly[0]) / (lx[-1] - lx[0]))
+        print(json.dumps({"sweep": "prefill_fwd", "fit": "time ~ N^a over the three longest",
+                          "a": slope, "batch": args.sweep_batch, "heads_q": 32, "heads_kv": 8,
+                          "head_dim": 128}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,9 +454,16 @@ def main():
     ap.add_argument("--batch-div", type=int, default=1,
                     help="divide every workload's batch (smaller cases for profiler captures; "
                          "not a benchmark setting)")
+    ap.add_argument("--sweep", default="",
+                    help="comma-separated sequence lengths: prefill-forward length sweep "
+                         "(one JSON line per length) instead of the benchmark")
+    ap.add_argument("--sweep-batch", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.sweep:
+        run_sweep(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -56,7 +56,11 @@ inline TcPlan choose_fwd_plan(int batch, int max_q, int max_k, int total_q, int 
   p.n_m_tiles = (max_q + p.tile_tokens - 1) / p.tile_tokens;
   const long long ctas = (long long)batch * (p.pack ? hkv : hq) * p.n_m_tiles;
   const int kv_tiles = (max_k + kTileKeys - 1) / kTileKeys;
-  if (sms > 0 && ctas < 4LL * sms && kv_tiles >= 8) {
+  // Split the keys across CTAs for decode (packed heads), or when even the
+  // prefill kernel's 256-row CTAs would leave most SMs idle.
+  const long long prefill_ctas = (long long)batch * hq * ((max_q + 2 * kTileRows - 1) / (2 * kTileRows));
+  const bool starved = p.pack ? ctas < 4LL * sms : 4 * prefill_ctas < sms;
+  if (sms > 0 && starved && kv_tiles >= 8) {
     long long want = (8LL * sms + ctas - 1) / ctas;
     long long cap = kv_tiles / 4;  // at least four key tiles per split
     int n = (int)(want < cap ? want : cap);

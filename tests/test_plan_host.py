@@ -1,0 +1,67 @@
+"""The host-side plan choice (plan.h), compiled with the host compiler and run
+on the CPU: decode shapes pack the query heads of a KV head into one tile and
+split the keys; prefill shapes use one head per tile and split only when the
+grid would leave most SMs idle."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SRC = r'''
+#include <stdio.h>
+#include "exact_tiled_attention_online_gb300/csrc/plan.h"
+using namespace attn;
+int main() {
+  int b, mq, mk, hq, hkv, sms;
+  while (scanf("%d %d %d %d %d %d", &b, &mq, &mk, &hq, &hkv, &sms) == 6) {
+    TcPlan p = choose_fwd_plan(b, mq, mk, b * mq, hq, hkv, 128, ATTN_DTYPE_BF16, sms);
+    printf("%d %d %d %d\n", p.kind, p.pack, p.tile_tokens, p.n_splits);
+  }
+}
+'''
+
+
+@pytest.fixture(scope="module")
+def plan_bin(tmp_path_factory):
+    if not shutil.which("g++"):
+        pytest.skip("no host C++ compiler")
+    d = tmp_path_factory.mktemp("plan")
+    src, exe = d / "plan.cpp", d / "plan"
+    src.write_text(SRC)
+    subprocess.run(["g++", "-std=c++17", "-DATTN_TC_FWD=1", f"-I{ROOT}", "-o", str(exe), str(src)],
+                   check=True)
+    return str(exe)
+
+
+def plan(exe, *shape):
+    out = subprocess.run([exe], input=" ".join(map(str, shape)), capture_output=True, text=True,
+                         check=True).stdout.split()
+    return tuple(int(x) for x in out)
+
+
+def test_decode_packs_and_splits(plan_bin):
+    kind, pack, tokens, splits = plan(plan_bin, 32, 1, 32768, 32, 8, 152)
+    assert (kind, pack, tokens) == (2, 1, 32) and splits >= 2
+    kind, pack, tokens, splits = plan(plan_bin, 32, 16, 32768, 32, 8, 152)
+    assert (kind, pack, tokens) == (2, 1, 32) and splits >= 2
+
+
+def test_prefill_one_head_per_tile_no_split(plan_bin):
+    for shape in ((4, 4096, 4096, 32, 8), (1, 1024, 1024, 32, 8), (2, 8192, 8192, 16, 4)):
+        assert plan(plan_bin, *shape, 152) == (1, 0, 128, 1), shape
+
+
+def test_long_single_query_mha_splits(plan_bin):
+    kind, pack, tokens, splits = plan(plan_bin, 1, 1, 100000, 32, 32, 152)
+    assert kind == 2 and pack == 0 and splits > 1
+
+
+def test_fp32_takes_cuda_cores(plan_bin, tmp_path):
+    src = SRC.replace("ATTN_DTYPE_BF16", "ATTN_DTYPE_FP32")
+    (tmp_path / "p.cpp").write_text(src)
+    subprocess.run(["g++", "-std=c++17", "-DATTN_TC_FWD=1", f"-I{ROOT}", "-o",
+                    str(tmp_path / "p"), str(tmp_path / "p.cpp")], check=True)
+    assert plan(str(tmp_path / "p"), 4, 4096, 4096, 32, 8, 152)[0] == 0

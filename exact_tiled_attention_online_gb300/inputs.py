@@ -44,6 +44,7 @@ class Workload:
     seed: int
     backward: bool = False
     v_shift_per_seq: float = 0.0
+    window: int = 0  # > 0: bounded causal window of that many keys per row
 
     @property
     def batch(self) -> int:
@@ -141,8 +142,9 @@ def make_inputs(w: Workload, device: str = "cpu", gen_device: str = "cpu",
 
 def custom(name: str, seqlens_q, seqlens_k, hq: int, hkv: int, d: int,
            dtype: str = "bf16", mask: int = MASK_TOP_LEFT, seed: int = 7,
-           backward: bool = False, v_shift_per_seq: float = 0.0) -> Workload:
+           backward: bool = False, v_shift_per_seq: float = 0.0,
+           window: int = 0) -> Workload:
     """A Workload for tests (small ragged shapes, edge cases)."""
     return Workload(name, tuple(int(x) for x in seqlens_q),
                     tuple(int(x) for x in seqlens_k), hq, hkv, d, dtype, mask,
-                    seed, backward, v_shift_per_seq)
+                    seed, backward, v_shift_per_seq, int(window))

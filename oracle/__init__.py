@@ -12,7 +12,10 @@ follows:
 
 * allowed pairs: per-token sequence id and in-sequence position, top-left
   ``j <= i`` or bottom-right ``j <= i + Nk - Nq`` ("causal-mask-and-ragged-
-  sequence-layouts", first and third paragraphs);
+  sequence-layouts", first and third paragraphs), optionally bounded to the
+  last ``window`` keys up to that causal bound (``window > 0``; the bounded
+  window of "attention-algorithm-error-and-complexity-tests", fifth
+  paragraph);
 * forward: two-pass stable softmax over the allowed set, empty rows give
   O = 0 and lse = -inf (same page, fourth paragraph; "formal-correctness",
   "The FlashAttention Proof", online recurrence equals recomputed softmax);
@@ -99,10 +102,11 @@ class Oracle:
         L.oracle_token_meta.argtypes = [_I32, ctypes.c_int, ctypes.c_int, _I32, _I32]
         L.oracle_token_meta.restype = ctypes.c_int
         L.oracle_mask.argtypes = [_I32, _I32, ctypes.c_int, ctypes.c_int,
-                                  ctypes.c_int, ctypes.c_int, _U8]
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _U8]
         L.oracle_mask.restype = ctypes.c_int
         common = [_F64, _F64, _F64]
-        sizes = [_I32, _I32] + [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int]
+        sizes = ([_I32, _I32] + [ctypes.c_int] * 6
+                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int])
         L.oracle_fwd.argtypes = common + sizes + [_I64, ctypes.c_int64, _F64, _F64]
         L.oracle_fwd.restype = ctypes.c_int
         L.oracle_bwd.argtypes = common + [_F64] + sizes + [_F64] * 5
@@ -125,18 +129,21 @@ class Oracle:
             raise ValueError("invalid cu_seqlens")
         return sid[:total], pos[:total]
 
-    def mask(self, cu_q, cu_k, total_q: int, total_k: int, mask_kind: int):
+    def mask(self, cu_q, cu_k, total_q: int, total_k: int, mask_kind: int,
+             window: int = 0):
         """The materialised packed mask, uint8 [total_q, total_k]."""
         cq, ck = _i32(cu_q), _i32(cu_k)
         m = np.zeros((total_q, total_k), np.uint8)
         rc = self.lib.oracle_mask(_ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1,
-                                  total_q, total_k, mask_kind, _ptr(m, _U8))
+                                  total_q, total_k, mask_kind, int(window),
+                                  _ptr(m, _U8))
         if rc != 0:
             raise ValueError("invalid mask arguments")
         return m[:total_q, :total_k]
 
     # -- forward ------------------------------------------------------------
-    def fwd(self, q, k, v, cu_q, cu_k, scale: float, mask_kind: int, rows=None):
+    def fwd(self, q, k, v, cu_q, cu_k, scale: float, mask_kind: int, rows=None,
+            window: int = 0):
         """Forward.  q [Tq, Hq, d], k/v [Tk, Hkv, d].
 
         rows None -> (o [Tq, Hq, d], lse [Hq, Tq]); rows = int array [n, 2] of
@@ -159,7 +166,8 @@ class Oracle:
         rc = self.lib.oracle_fwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1,
                                  tq, tk, hq, hkv, d, float(scale), mask_kind,
-                                 rp, n, _ptr(o, _F64), _ptr(lse, _F64))
+                                 int(window), rp, n, _ptr(o, _F64),
+                                 _ptr(lse, _F64))
         if rc != 0:
             raise ValueError("invalid oracle_fwd arguments")
         if rows is not None:
@@ -167,7 +175,8 @@ class Oracle:
         return o, lse
 
     # -- backward -----------------------------------------------------------
-    def bwd(self, q, k, v, dout, cu_q, cu_k, scale: float, mask_kind: int):
+    def bwd(self, q, k, v, dout, cu_q, cu_k, scale: float, mask_kind: int,
+            window: int = 0):
         """Full backward -> (dq, dk, dv, o, lse), fp64."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
         cq, ck = _i32(cu_q), _i32(cu_k)
@@ -181,14 +190,15 @@ class Oracle:
         rc = self.lib.oracle_bwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(dout, _F64), _ptr(cq, _I32), _ptr(ck, _I32),
                                  len(cq) - 1, tq, tk, hq, hkv, d, float(scale),
-                                 mask_kind, _ptr(dq, _F64), _ptr(dk, _F64),
+                                 mask_kind, int(window), _ptr(dq, _F64),
+                                 _ptr(dk, _F64),
                                  _ptr(dv, _F64), _ptr(o, _F64), _ptr(lse, _F64))
         if rc != 0:
             raise ValueError("invalid oracle_bwd arguments")
         return dq, dk, dv, o, lse
 
     def bwd_sampled(self, q, k, v, dout, cu_q, cu_k, scale: float,
-                    mask_kind: int, q_rows, k_rows):
+                    mask_kind: int, q_rows, k_rows, window: int = 0):
         """dQ at sampled (token, head) rows and dK, dV at sampled
         (key token, kv head) rows -> (dq [nq, d], dk [nk, d], dv [nk, d])."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -203,7 +213,8 @@ class Oracle:
         rc = self.lib.oracle_bwd_sampled(
             _ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64), _ptr(dout, _F64),
             _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1, tq, tk, hq, hkv, d,
-            float(scale), mask_kind, _ptr(qr, _I64), len(qr), _ptr(dq, _F64),
+            float(scale), mask_kind, int(window), _ptr(qr, _I64), len(qr),
+            _ptr(dq, _F64),
             _ptr(kr, _I64), len(kr), _ptr(dk, _F64), _ptr(dv, _F64))
         if rc != 0:
             raise ValueError("invalid oracle_bwd_sampled arguments")

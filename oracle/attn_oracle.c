@@ -29,6 +29,10 @@
  *   - mask_kind 0: no causal rule; 1: top-left, key position <= query
  *     position; 2: bottom-right, key position <= query position + Nk - Nq
  *     ("causal-mask-and-ragged-sequence-layouts", third paragraph).
+ *   - window > 0 (causal kinds only) keeps, of the keys the causal rule
+ *     allows, those at most window - 1 positions before the causal bound: a
+ *     bounded window ("attention-algorithm-error-and-complexity-tests",
+ *     fifth paragraph).
  *   - Pairs in different sequences are never allowed.
  *   - A row whose allowed set is empty has O = 0 exactly and lse = -inf
  *     (same page, fourth paragraph).
@@ -59,6 +63,7 @@ typedef struct {
   int batch, total_q, total_k, hq, hkv, d;
   double scale;
   int mask_kind;
+  int window; /* > 0: at most `window` keys per row, the latest allowed ones */
   int32_t *seq_q, *pos_q, *seq_k, *pos_k; /* per-token metadata */
 } problem_t;
 
@@ -89,16 +94,23 @@ static int pair_allowed(const problem_t *p, int tq, int tk) {
   int i = p->pos_q[tq], j = p->pos_k[tk];
   int nq = p->cu_q[s + 1] - p->cu_q[s];
   int nk = p->cu_k[s + 1] - p->cu_k[s];
+  int bound; /* the causal rule allows j <= bound */
   switch (p->mask_kind) {
     case ORACLE_MASK_NONE:
       return 1;
     case ORACLE_MASK_TOP_LEFT:
-      return j <= i;
+      bound = i;
+      break;
     case ORACLE_MASK_BOTTOM_RIGHT:
-      return j <= i + nk - nq;
+      bound = i + nk - nq;
+      break;
     default:
       return 0;
   }
+  if (j > bound) return 0;
+  /* bounded window: only the `window` positions up to the causal bound */
+  if (p->window > 0 && bound - j >= p->window) return 0;
+  return 1;
 }
 
 static double dot(const double *a, const double *b, int d) {
@@ -156,9 +168,11 @@ static void forward_row(const problem_t *p, int t, int h, unsigned char *mrow,
 static int setup(problem_t *p, const double *q, const double *k,
                  const double *v, const int32_t *cu_q, const int32_t *cu_k,
                  int batch, int total_q, int total_k, int hq, int hkv, int d,
-                 double scale, int mask_kind) {
+                 double scale, int mask_kind, int window) {
+  p->seq_q = p->pos_q = p->seq_k = p->pos_k = NULL;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0) return -1;
   if (mask_kind < 0 || mask_kind > 2) return -1;
+  if (window > 0 && mask_kind == ORACLE_MASK_NONE) return -1;
   p->q = q;
   p->k = k;
   p->v = v;
@@ -172,6 +186,7 @@ static int setup(problem_t *p, const double *q, const double *k,
   p->d = d;
   p->scale = scale;
   p->mask_kind = mask_kind;
+  p->window = window;
   p->seq_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->pos_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->seq_k = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_k + 1));
@@ -192,10 +207,11 @@ static void teardown(problem_t *p) {
 /* The packed boolean mask M[tq][tk] (total_q x total_k bytes) for a query head
  * (the rule does not depend on the head). */
 int oracle_mask(const int32_t *cu_q, const int32_t *cu_k, int batch,
-                int total_q, int total_k, int mask_kind, unsigned char *m) {
+                int total_q, int total_k, int mask_kind, int window,
+                unsigned char *m) {
   problem_t p;
   int rc = setup(&p, NULL, NULL, NULL, cu_q, cu_k, batch, total_q, total_k, 1,
-                 1, 1, 1.0, mask_kind);
+                 1, 1, 1.0, mask_kind, window);
   if (rc == 0)
     for (int t = 0; t < total_q; t++)
       for (int u = 0; u < total_k; u++)
@@ -210,11 +226,11 @@ int oracle_mask(const int32_t *cu_q, const int32_t *cu_k, int batch,
 int oracle_fwd(const double *q, const double *k, const double *v,
                const int32_t *cu_q, const int32_t *cu_k, int batch,
                int total_q, int total_k, int hq, int hkv, int d, double scale,
-               int mask_kind, const int64_t *rows, int64_t nrows, double *o,
-               double *lse) {
+               int mask_kind, int window, const int64_t *rows, int64_t nrows,
+               double *o, double *lse) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind);
+                 scale, mask_kind, window);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -285,14 +301,14 @@ static void backward_row(const problem_t *p, const double *dout, int t, int h,
 int oracle_bwd(const double *q, const double *k, const double *v,
                const double *dout, const int32_t *cu_q, const int32_t *cu_k,
                int batch, int total_q, int total_k, int hq, int hkv, int d,
-               double scale, int mask_kind, double *dq, double *dk, double *dv,
-               double *o, double *lse) {
+               double scale, int mask_kind, int window, double *dq, double *dk,
+               double *dv, double *o, double *lse) {
   int rc = oracle_fwd(q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                      scale, mask_kind, NULL, 0, o, lse);
+                      scale, mask_kind, window, NULL, 0, o, lse);
   if (rc != 0) return rc;
   problem_t p;
   rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-             scale, mask_kind);
+             scale, mask_kind, window);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -343,12 +359,13 @@ int oracle_bwd_sampled(const double *q, const double *k, const double *v,
                        const double *dout, const int32_t *cu_q,
                        const int32_t *cu_k, int batch, int total_q,
                        int total_k, int hq, int hkv, int d, double scale,
-                       int mask_kind, const int64_t *q_rows, int64_t nq_rows,
+                       int mask_kind, int window, const int64_t *q_rows,
+                       int64_t nq_rows,
                        double *dq_out, const int64_t *k_rows, int64_t nk_rows,
                        double *dk_out, double *dv_out) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind);
+                 scale, mask_kind, window);
   if (rc != 0) {
     teardown(&p);
     return rc;

@@ -30,24 +30,34 @@ def cu(lengths):
     return np.array(out, np.int32)
 
 
-def row_count(kind, i, nq, nk):
-    """Closed-form number of allowed keys of zero-based query row i."""
+def row_range(kind, i, nq, nk, window=0):
+    """Closed-form [a, b) of allowed key positions of zero-based query row i:
+    the causal bound is i (top-left) or i + nk - nq (bottom-right), and a
+    window W > 0 keeps only the W positions ending at that bound."""
     if kind == NONE:
-        return nk
-    if kind == TOP_LEFT:
-        return min(i + 1, nk)
-    return max(0, min(i + nk - nq + 1, nk))
+        return 0, nk
+    bound = i if kind == TOP_LEFT else i + nk - nq
+    b = min(max(bound + 1, 0), nk)
+    a = 0 if window <= 0 else min(max(bound + 1 - window, 0), nk)
+    return a, b
 
 
-def allowed_interval(kind, lq, lk):
+def row_count(kind, i, nq, nk, window=0):
+    """Closed-form number of allowed keys of zero-based query row i."""
+    a, b = row_range(kind, i, nq, nk, window)
+    return b - a
+
+
+def allowed_interval(kind, lq, lk, window=0):
     """[(token, key_start, key_end)] for every packed query token: under every
-    rule the allowed keys of a row are a prefix of its own sequence."""
+    rule the allowed keys of a row are one interval of its own sequence (a
+    prefix without a window)."""
     out = []
     cq, ck = cu(lq), cu(lk)
     for s, (nq, nk) in enumerate(zip(lq, lk)):
         for i in range(nq):
-            c = row_count(kind, i, nq, nk)
-            out.append((cq[s] + i, ck[s], ck[s] + c))
+            a, b = row_range(kind, i, nq, nk, window)
+            out.append((cq[s] + i, ck[s] + a, ck[s] + b))
     return out
 
 
@@ -67,6 +77,8 @@ SHAPES = [  # (lq, lk, hq, hkv, d, kind)
     ((2, 5), (9, 3), 4, 1, 3, BOTTOM_RIGHT),
 ]
 
+WINDOWS = (1, 2, 3, 7)  # bounded windows, all shorter than some sequence
+
 
 # --------------------------------------------------------------------------
 # mask
@@ -82,11 +94,71 @@ def pin_mask_intervals(orc):
     closed form of each rule gives, with nothing across sequences."""
     for lq, lk, _, _, _, kind in SHAPES:
         for k2 in (NONE, TOP_LEFT, BOTTOM_RIGHT):
-            m = orc.mask(cu(lq), cu(lk), sum(lq), sum(lk), k2)
-            ref = np.zeros_like(m)
-            for t, a, b in allowed_interval(k2, lq, lk):
-                ref[t, a:b] = 1
-            assert np.array_equal(m, ref), (lq, lk, k2)
+            for w in (0,) + (WINDOWS if k2 != NONE else ()):
+                m = orc.mask(cu(lq), cu(lk), sum(lq), sum(lk), k2, w)
+                ref = np.zeros_like(m)
+                for t, a, b in allowed_interval(k2, lq, lk, w):
+                    ref[t, a:b] = 1
+                assert np.array_equal(m, ref), (lq, lk, k2, w)
+
+
+def pin_window_counts(orc):
+    """Hand-counted windowed masks ("attention-algorithm-error-and-complexity-
+    tests", fifth paragraph: a bounded window makes the pair count linear in
+    the length).  Top-left, N = 6, W = 2: rows see 1, 2, 2, 2, 2, 2 keys (11
+    pairs).  Bottom-right, Nq = 3, Nk = 7, W = 3: the bounds are 4, 5, 6, so
+    every row sees 3 keys (9 pairs) starting at 2, 3, 4.  Bottom-right,
+    Nq = 5, Nk = 2, W = 1: bounds -3..1, rows 3 and 4 see key 0 and key 1."""
+    m = orc.mask(cu([6]), cu([6]), 6, 6, TOP_LEFT, 2)
+    assert list(m.sum(axis=1)) == [1, 2, 2, 2, 2, 2]
+    assert m[5, 4] == 1 and m[5, 3] == 0 and m[5, 5] == 1
+    m = orc.mask(cu([3]), cu([7]), 3, 7, BOTTOM_RIGHT, 3)
+    assert [list(np.nonzero(r)[0]) for r in m] == [[2, 3, 4], [3, 4, 5], [4, 5, 6]]
+    m = orc.mask(cu([5]), cu([2]), 5, 2, BOTTOM_RIGHT, 1)
+    assert [list(np.nonzero(r)[0]) for r in m] == [[], [], [], [0], [1]]
+    # a window needs a causal rule: without one there is no bound to end at
+    try:
+        orc.mask(cu([3]), cu([3]), 3, 3, NONE, 2)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("window without a causal rule accepted")
+
+
+def pin_window_one_key(orc):
+    """W = 1: every non-empty row sees exactly the key at its causal bound, so
+    O_i = v_bound and lse_i = scale * q_i . k_bound."""
+    rng = np.random.default_rng(14)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        if kind == NONE:
+            continue
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), 0.55, kind, window=1)
+        g = hq // hkv
+        for t, a, b in allowed_interval(kind, lq, lk, 1):
+            for h in range(hq):
+                if b == a:
+                    assert np.all(o[t, h] == 0.0) and lse[h, t] == -math.inf
+                    continue
+                assert b == a + 1
+                np.testing.assert_allclose(o[t, h], v[a, h // g], rtol=1e-14, atol=1e-14)
+                ref = 0.55 * float(q[t, h] @ k[a, h // g])
+                assert abs(lse[h, t] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def pin_window_covering_is_causal(orc):
+    """A window at least as long as every key sequence removes nothing: the
+    result equals the unbounded causal one exactly."""
+    rng = np.random.default_rng(15)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        if kind == NONE:
+            continue
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        a = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind)
+        b = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind, window=max(lk))
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
 
 
 def pin_golden_mask_counts(orc):
@@ -108,12 +180,13 @@ def pin_uniform_logits(orc):
     """Q = 0: every allowed logit is 0, so O_i is the mean of the allowed V
     rows and lse_i = ln |A_i|; empty rows give exact zeros and -inf."""
     rng = np.random.default_rng(1)
-    for lq, lk, hq, hkv, d, kind in SHAPES:
+    cases = [(s, 0) for s in SHAPES] + [(s, 3) for s in SHAPES if s[5] != NONE]
+    for (lq, lk, hq, hkv, d, kind), w in cases:
         q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
         q[:] = 0.0
-        o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), 0.37, kind)
+        o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), 0.37, kind, window=w)
         g = hq // hkv
-        for t, a, b in allowed_interval(kind, lq, lk):
+        for t, a, b in allowed_interval(kind, lq, lk, w):
             for h in range(hq):
                 if b == a:
                     assert np.all(o[t, h] == 0.0) and lse[h, t] == -math.inf
@@ -255,20 +328,22 @@ def pin_packed_vs_separate(orc):
 # --------------------------------------------------------------------------
 def pin_torch_sdpa_fp64(orc):
     rng = np.random.default_rng(8)
-    for lq, lk, hq, hkv, d, kind in SHAPES:
+    cases = [(s, 0) for s in SHAPES] + [(s, 2) for s in SHAPES if s[5] != NONE]
+    for (lq, lk, hq, hkv, d, kind), w in cases:
         q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
         do = rng.standard_normal(q.shape)
         scale = 1.0 / math.sqrt(d)
-        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind, window=w)
         g = hq // hkv
         cq, ck = cu(lq), cu(lk)
         for s, (nq, nk) in enumerate(zip(lq, lk)):
             if nq == 0:
                 continue
-            rows = [i for i in range(nq) if row_count(kind, i, nq, nk) > 0]
+            rows = [i for i in range(nq) if row_count(kind, i, nq, nk, w) > 0]
             mask = np.zeros((nq, nk), bool)
             for i in range(nq):
-                mask[i, :row_count(kind, i, nq, nk)] = True
+                a, b = row_range(kind, i, nq, nk, w)
+                mask[i, a:b] = True
             qs = torch.tensor(q[cq[s]:cq[s + 1]].transpose(1, 0, 2), requires_grad=True)
             ks = torch.tensor(k[ck[s]:ck[s + 1]].transpose(1, 0, 2), requires_grad=True)
             vs = torch.tensor(v[ck[s]:ck[s + 1]].transpose(1, 0, 2), requires_grad=True)
@@ -304,37 +379,38 @@ def pin_finite_differences(orc):
     hq, hkv, d, scale = 2, 1, 3, 0.7
     q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
     do = rng.standard_normal(q.shape)
-    kind = BOTTOM_RIGHT
-    dq, dk, dv, _, _ = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind)
+    for kind, w in ((BOTTOM_RIGHT, 0), (TOP_LEFT, 2)):
+        dq, dk, dv, _, _ = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind, window=w)
 
-    def loss(qq, kk, vv):
-        o, _ = orc.fwd(qq, kk, vv, cu(lq), cu(lk), scale, kind)
-        return float((o * do).sum())
+        def loss(qq, kk, vv):
+            o, _ = orc.fwd(qq, kk, vv, cu(lq), cu(lk), scale, kind, window=w)
+            return float((o * do).sum())
 
-    h = 1e-5
-    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
-        fd = np.zeros_like(x)
-        for idx in np.ndindex(x.shape):
-            xs = []
-            for sign in (1.0, -1.0):
-                xx = x.copy()
-                xx[idx] += sign * h
-                xs.append({"q": (xx, k, v), "k": (q, xx, v), "v": (q, k, xx)}[name])
-            fd[idx] = (loss(*xs[0]) - loss(*xs[1])) / (2 * h)
-        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=name)
+        h = 1e-5
+        for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xs = []
+                for sign in (1.0, -1.0):
+                    xx = x.copy()
+                    xx[idx] += sign * h
+                    xs.append({"q": (xx, k, v), "k": (q, xx, v), "v": (q, k, xx)}[name])
+                fd[idx] = (loss(*xs[0]) - loss(*xs[1])) / (2 * h)
+            np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=(name, w))
 
 
 def pin_dv_column_sum(orc):
     """Softmax rows sum to one, so sum_j dV_j of a KV head equals the sum of
     dO over every non-empty row of its query heads."""
     rng = np.random.default_rng(10)
-    for lq, lk, hq, hkv, d, kind in SHAPES:
+    cases = [(s, 0) for s in SHAPES] + [(s, 2) for s in SHAPES if s[5] != NONE]
+    for (lq, lk, hq, hkv, d, kind), w in cases:
         q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
         do = rng.standard_normal(q.shape)
-        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind, window=w)
         g = hq // hkv
         nonempty = np.zeros((sum(lq), hq), bool)
-        for t, a, b in allowed_interval(kind, lq, lk):
+        for t, a, b in allowed_interval(kind, lq, lk, w):
             nonempty[t, :] = b > a
         for hk in range(hkv):
             ref = np.zeros(d)
@@ -388,6 +464,7 @@ def pin_empty_rows_backward(orc):
 
 ALL_PINS = [
     pin_token_meta, pin_mask_intervals, pin_golden_mask_counts,
+    pin_window_counts, pin_window_one_key, pin_window_covering_is_causal,
     pin_uniform_logits, pin_single_dominant_score, pin_masked_dominant_score,
     pin_row_shift, pin_permutation_noncausal, pin_gqa_vs_repeat,
     pin_packed_vs_separate, pin_torch_sdpa_fp64, pin_finite_differences,

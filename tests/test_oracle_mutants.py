@@ -2,8 +2,9 @@
 compile the copy on the CPU, and check that at least one pin rejects it.
 
 This is the evidence that the pins constrain every part of the oracle: a
-dropped scale, a wrong alignment offset, a global offset used as a position,
-a wrong head grouping, a missing denominator term in the backward and so on
+dropped scale, a wrong alignment offset, a window off by one, a global
+offset used as a position, a wrong head grouping, a missing denominator term
+in the backward and so on
 ("attention-algorithm-error-and-complexity-tests", first and fourth
 paragraphs; "formal-correctness", "The Counterexample": a missing rescale is
 correct whenever the maximum does not move, so pins must hit the slice where
@@ -24,9 +25,14 @@ MUTANTS = {
     "lse_without_max": ("double lse_i = m + log(l);", "double lse_i = log(l);"),
     "no_max_subtraction": ("if (mrow[u]) l += exp(srow[u] - m);",
                            "if (mrow[u]) l += exp(srow[u]);"),
-    "top_left_strict": ("return j <= i;", "return j < i;"),
-    "bottom_right_off_by_one": ("return j <= i + nk - nq;", "return j <= i + nk - nq + 1;"),
-    "bottom_right_as_top_left": ("return j <= i + nk - nq;", "return j <= i;"),
+    "top_left_strict": ("bound = i;", "bound = i - 1;"),
+    "bottom_right_off_by_one": ("bound = i + nk - nq;", "bound = i + nk - nq + 1;"),
+    "bottom_right_as_top_left": ("bound = i + nk - nq;", "bound = i;"),
+    "window_off_by_one": ("bound - j >= p->window", "bound - j > p->window"),
+    "window_ignored": ("if (p->window > 0 && bound - j >= p->window) return 0;", ""),
+    "window_from_query_position": ("bound - j >= p->window", "i - j >= p->window"),
+    "window_accepted_without_causal": (
+        "if (window > 0 && mask_kind == ORACLE_MASK_NONE) return -1;", ""),
     "global_offset_as_position": ("pos[t] = t - cu[s];", "pos[t] = t;"),
     "cross_sequence_pairs": ("if (s < 0 || p->seq_k[tk] != s) return 0;", "if (s < 0) return 0;"),
     "interleaved_gqa": ("int hk = h / (p->hq / p->hkv);", "int hk = h % p->hkv;"),

@@ -7,7 +7,8 @@ that are already resident in HBM:
                   (the headline: ``value`` is its TFLOP/s);
   decode_q1/q16   split-KV decode, B=32, Nk=32768, Nq=1 / 16, bottom-right;
   train_fwd_bwd   forward + backward, B=2, N=8192, 16/4 heads, d=128;
-  varlen_causal   packed ragged forward, 12 sequences, 16 heads, d=128.
+  varlen_causal   packed ragged forward, 12 sequences, 16 heads, d=128;
+  window_prefill  the gqa_prefill shape under a bounded 1024-key causal window.
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -53,15 +54,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # --------------------------------------------------------------------------
 # work accounting (closed-form pair counts of the alignment rules)
 # --------------------------------------------------------------------------
-def row_keys(mask, i, nq, nk):
+def row_keys(mask, i, nq, nk, window=0):
+    """Allowed keys of in-sequence row i (closed form)."""
     if mask == inputs.MASK_NONE:
         return nk
     off = 0 if mask == inputs.MASK_TOP_LEFT else nk - nq
-    return max(0, min(i + off + 1, nk))
+    end = max(0, min(i + off + 1, nk))
+    begin = max(0, min(i + off + 1 - window, nk)) if window > 0 else 0
+    return end - begin
 
 
 def allowed_pairs(w) -> int:
-    """Allowed (query, key) pairs over all sequences and query heads."""
+    """Allowed (query, key) pairs over all sequences and query heads: row i
+    sees the keys in [clip(b + 1 - W), clip(b + 1)) with causal bound b
+    (W unbounded without a window)."""
     total = 0
     for nq, nk in zip(w.seqlens_q, w.seqlens_k):
         i = np.arange(nq, dtype=np.int64)
@@ -69,7 +75,9 @@ def allowed_pairs(w) -> int:
             total += nq * nk
         else:
             off = 0 if w.mask == inputs.MASK_TOP_LEFT else nk - nq
-            total += int(np.clip(i + off + 1, 0, nk).sum())
+            end = np.clip(i + off + 1, 0, nk)
+            begin = np.clip(i + off + 1 - w.window, 0, nk) if w.window > 0 else 0
+            total += int((end - begin).sum())
     return total * w.hq
 
 
@@ -189,7 +197,7 @@ class Runner:
         self.o32 = torch.empty(x["q"].shape, dtype=torch.float32, device=device) \
             if w.backward else None
         ws = attn.fwd_workspace_size(w.batch, w.max_q, w.max_k, w.total_q, w.hq, w.hkv, w.d,
-                                     attn.DTYPE_BF16)
+                                     attn.DTYPE_BF16, w.window)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
         if w.backward:
             self.dq = torch.empty_like(x["q"])
@@ -203,12 +211,13 @@ class Runner:
     def run(self):
         a, w, x = self.attn, self.w, self.x
         a.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q, w.max_k,
-              w.mask, w.scale, out=self.o, lse=self.lse, workspace=self.ws, o_f32=self.o32)
+              w.mask, w.scale, out=self.o, lse=self.lse, workspace=self.ws, o_f32=self.o32,
+              window=w.window)
         plans = [a.last_plan()]
         if w.backward:
             a.bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["dout"], x["cu_seqlens_q"],
                   x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, dq=self.dq, dk=self.dk,
-                  dv=self.dv, workspace=self.bws, o_f32=self.o32)
+                  dv=self.dv, workspace=self.bws, o_f32=self.o32, window=w.window)
             plans.append(a.last_plan())
         self.plans = plans
 
@@ -232,7 +241,7 @@ def validate(r: Runner, n_rows=24):
     rows = np.stack([rng.integers(w.total_q, size=n_rows), rng.integers(w.hq, size=n_rows)], 1)
     host = {k: (t.cpu() if hasattr(t, "cpu") else t) for k, t in r.x.items()}
     o_ref, l_ref = oracle.fwd(host["q"], host["k"], host["v"], host["cu_seqlens_q"],
-                              host["cu_seqlens_k"], w.scale, w.mask, rows=rows)
+                              host["cu_seqlens_k"], w.scale, w.mask, rows=rows, window=w.window)
     on = r.o.double().cpu().numpy()[rows[:, 0], rows[:, 1]]
     ln = r.lse.double().cpu().numpy()[rows[:, 1], rows[:, 0]]
     err = np.abs(on - o_ref)
@@ -335,7 +344,8 @@ def e2e_headline(args, r: Runner, device):
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
         r.attn.fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
-                   w.max_q, w.max_k, w.mask, w.scale, out=r.o, lse=r.lse, workspace=r.ws)
+                   w.max_q, w.max_k, w.mask, w.scale, out=r.o, lse=r.lse, workspace=r.ws,
+                   window=w.window)
         o_h.copy_(r.o, non_blocking=True)
         l_h.copy_(r.lse, non_blocking=True)
 
@@ -368,14 +378,14 @@ def cpu_baseline(workload: str, budget_s: float = 12.0):
     def sample(n):
         rows = np.stack([rng.integers(w.total_q, size=n), rng.integers(w.hq, size=n)], 1)
         t0 = time.perf_counter()
-        orc.fwd(q, k, v, cq, ck, w.scale, w.mask, rows=rows)
+        orc.fwd(q, k, v, cq, ck, w.scale, w.mask, rows=rows, window=w.window)
         dt = time.perf_counter() - t0
         # allowed pairs of the sampled rows, by the closed form
         seq = np.searchsorted(cq, rows[:, 0], side="right") - 1
         pairs = 0
         for t, s in zip(rows[:, 0], seq):
             nq, nk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
-            pairs += row_keys(w.mask, int(t - cq[s]), int(nq), int(nk))
+            pairs += row_keys(w.mask, int(t - cq[s]), int(nq), int(nk), w.window)
         return dt, 4.0 * w.d * pairs
 
     dt, fl = sample(64)
@@ -401,16 +411,18 @@ def run_sweep(args):
     lengths = [int(x) for x in args.sweep.split(",")]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     points = []
+    win = args.sweep_window
+    mask_name = f"causal_top_left_window_{win}" if win > 0 else "causal_top_left"
     for n in lengths:
         w = inputs.custom(f"sweep_{n}", (n,) * args.sweep_batch, (n,) * args.sweep_batch, 32, 8,
-                          128, "bf16", inputs.MASK_TOP_LEFT, seed=2000 + n)
+                          128, "bf16", inputs.MASK_TOP_LEFT, seed=2000 + n, window=win)
         x = inputs.make_inputs(w, device=device, gen_device=device)
         o = torch.empty_like(x["q"])
         lse = torch.empty((w.hq, w.total_q), dtype=torch.float32, device=device)
 
         def run():
             attn.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q,
-                     w.max_k, w.mask, w.scale, out=o, lse=lse)
+                     w.max_k, w.mask, w.scale, out=o, lse=lse, window=win)
         for _ in range(args.warmup):
             run()
         ms = []
@@ -427,7 +439,7 @@ def run_sweep(args):
         points.append((n, med))
         print(json.dumps({"sweep": "prefill_fwd", "seq_len": n, "batch": w.batch, "heads_q": w.hq,
                           "heads_kv": w.hkv, "head_dim": w.d, "dtype": "bf16",
-                          "mask": "causal_top_left", "allowed_pairs": allowed_pairs(w),
+                          "mask": mask_name, "allowed_pairs": allowed_pairs(w),
                           "ms_median": med, "tflops": fl / (med * 1e-3) / 1e12,
                           "plan": attn.last_plan()}))
     if len(points) >= 2:
@@ -437,7 +449,7 @@ def run_sweep(args):
             float((ly[-1] - ly[0]) / (lx[-1] - lx[0]))
         print(json.dumps({"sweep": "prefill_fwd", "fit": "time ~ N^a over the three longest",
                           "a": slope, "batch": args.sweep_batch, "heads_q": 32, "heads_kv": 8,
-                          "head_dim": 128}))
+                          "head_dim": 128, "mask": mask_name}))
 
 
 def main():
@@ -447,7 +459,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads",
-                    default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal")
+                    default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
+                            "window_prefill")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -458,6 +471,9 @@ def main():
                     help="comma-separated sequence lengths: prefill-forward length sweep "
                          "(one JSON line per length) instead of the benchmark")
     ap.add_argument("--sweep-batch", type=int, default=1)
+    ap.add_argument("--sweep-window", type=int, default=0,
+                    help="bounded causal window for the sweep (0: unbounded causal); a bounded "
+                         "window has linear pair work, so the fitted exponent tends to 1")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -56,15 +56,15 @@ def library() -> ctypes.CDLL:
                            "(run exact_tiled_attention_online_gb300.build.build())")
     L = ctypes.CDLL(path)
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    L.attn_fwd.argtypes = [P, P, P, P, P, P, P, P] + [I] * 8 + [F, I, I, P, SZ, P]
+    L.attn_fwd.argtypes = [P, P, P, P, P, P, P, P] + [I] * 8 + [F, I, I, I, P, SZ, P]
     L.attn_fwd.restype = I
-    L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, P, SZ, P]
+    L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, I, P, SZ, P]
     L.attn_bwd.restype = I
-    L.attn_fwd_workspace_size.argtypes = [I] * 8
+    L.attn_fwd_workspace_size.argtypes = [I] * 9
     L.attn_fwd_workspace_size.restype = SZ
     L.attn_bwd_workspace_size.argtypes = [I] * 9
     L.attn_bwd_workspace_size.restype = SZ
-    L.attn_mask_probe.argtypes = [P, P] + [I] * 7 + [P, P]
+    L.attn_mask_probe.argtypes = [P, P] + [I] * 8 + [P, P]
     L.attn_mask_probe.restype = I
     L.attn_get_device_error.argtypes = [P]
     L.attn_get_device_error.restype = I
@@ -105,8 +105,9 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code) -> int:
-    n = library().attn_fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code)
+def fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code, window=0) -> int:
+    n = library().attn_fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, int(window),
+                                          dtype_code)
     if n == ctypes.c_size_t(-1).value:
         raise AttnError("attn_fwd_workspace_size", 1)
     return n
@@ -124,8 +125,11 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
         mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
         workspace: Optional[torch.Tensor] = None, stream=None, want_lse: bool = True,
-        o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False):
+        o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False, window: int = 0):
     """Attention forward on packed ragged tensors (layouts in include/attn.h).
+
+    ``window`` > 0 (causal masks only) bounds every row to the ``window`` key
+    positions that end at its causal bound.
 
     Returns (o, lse), or (o, lse, o_f32) when ``want_o_f32`` is set or an
     ``o_f32`` buffer is given.  lse is [n_heads_q, total_q] fp32 (None when
@@ -151,15 +155,16 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
     ret_f32 = want_o_f32 or o_f32 is not None
     if o_f32 is None and want_o_f32:
         o_f32 = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    ws_bytes = fwd_workspace_size(batch, max_seqlen_q, max_seqlen_k, total_q, hq, hkv, d, dt)
+    ws_bytes = fwd_workspace_size(batch, max_seqlen_q, max_seqlen_k, total_q, hq, hkv, d, dt,
+                                  window)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     st = library().attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(o_f32), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k),
         batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv, d, float(scale),
-        int(mask), dt, _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _stream(stream))
+        int(mask), int(window), dt, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
     if st != 0:
         raise AttnError("attn_fwd", st)
     return (out, lse, o_f32) if ret_f32 else (out, lse)
@@ -168,10 +173,11 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
 def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         max_seqlen_k: int, mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
         dq=None, dk=None, dv=None, workspace=None, stream=None,
-        o_f32: Optional[torch.Tensor] = None):
+        o_f32: Optional[torch.Tensor] = None, window: int = 0):
     """Attention backward; returns (dq, dk, dv) with dk/dv summed over each
     KV head's group of query heads.  Pass the forward's ``o_f32`` when it was
-    kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding."""
+    kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding; pass the
+    forward's mask and ``window``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n, 3)
     _check(lse, "lse", 2)
@@ -192,7 +198,7 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_f32), _ptr(dout), _ptr(dq),
         _ptr(dk), _ptr(dv),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, max_seqlen_q, max_seqlen_k, total_q,
-        total_k, hq, hkv, d, float(scale), int(mask), dt, _ptr(workspace),
+        total_k, hq, hkv, d, float(scale), int(mask), int(window), dt, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream))
     if st != 0:
         raise AttnError("attn_bwd", st)
@@ -200,12 +206,12 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
 
 
 def mask_probe(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k,
-               mask, tile_rows=128, stream=None) -> torch.Tensor:
+               mask, tile_rows=128, stream=None, window: int = 0) -> torch.Tensor:
     out = torch.empty((total_q, total_k), dtype=torch.uint8, device=cu_seqlens_q.device)
     st = library().attn_mask_probe(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                    cu_seqlens_q.numel() - 1, max_seqlen_q, max_seqlen_k,
-                                   total_q, total_k, int(mask), int(tile_rows), _ptr(out),
-                                   _stream(stream))
+                                   total_q, total_k, int(mask), int(window), int(tile_rows),
+                                   _ptr(out), _stream(stream))
     if st != 0:
         raise AttnError("attn_mask_probe", st)
     return out

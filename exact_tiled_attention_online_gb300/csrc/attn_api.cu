@@ -20,8 +20,8 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
 cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
 cudaError_t launch_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
-                              int max_k, int total_q, int total_k, int mask, int tile_rows,
-                              uint8_t *out, int *err, cudaStream_t st);
+                              int max_k, int total_q, int total_k, int mask, int window,
+                              int tile_rows, uint8_t *out, int *err, cudaStream_t st);
 
 // The per-device error flag.  Device code reaches it through a pointer kernel
 // argument; the host looks its address up once per device.
@@ -49,12 +49,13 @@ static void set_plan(const char *s) {
 // Validation shared by every entry point.
 // ---------------------------------------------------------------------------
 static attn_status check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
-                               int hq, int hkv, int d, int mask, int dtype) {
+                               int hq, int hkv, int d, int mask, int window, int dtype) {
   if (batch < 0 || max_q < 0 || max_k < 0 || total_q < 0 || total_k < 0)
     return ATTN_ERR_INVALID_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (hq > 65535 || hkv > 65535 || batch > 65535) return ATTN_ERR_UNSUPPORTED;
   if (mask < ATTN_MASK_NONE || mask > ATTN_CAUSAL_BOTTOM_RIGHT) return ATTN_ERR_INVALID_ARG;
+  if (window < 0 || (window > 0 && mask == ATTN_MASK_NONE)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (max_q > total_q || max_k > total_k) return ATTN_ERR_INVALID_ARG;
@@ -97,8 +98,8 @@ static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, in
 // Internal helpers for the other entry-point file of the library.
 int *internal_error_flag() { return device_error_ptr(); }
 attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
-                                 int hq, int hkv, int d, int mask, int dtype) {
-  return check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+                                 int hq, int hkv, int d, int mask, int window, int dtype) {
+  return check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
 }
 int internal_sm_count() { return sm_count(); }
 void internal_set_plan(const char *s) { set_plan(s); }
@@ -109,7 +110,7 @@ using namespace attn;
 
 extern "C" {
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 110; }
 
 const char *attn_status_string(attn_status s) {
   switch (s) {
@@ -129,11 +130,14 @@ const char *attn_status_string(attn_status s) {
 const char *attn_last_plan(void) { return t_plan; }
 
 size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int hq, int hkv,
-                               int d, attn_dtype dtype) {
-  if (check_sizes(batch, max_q, max_k, total_q, max_k, hq, hkv, d, ATTN_MASK_NONE, dtype) !=
-      ATTN_OK)
+                               int d, int window, attn_dtype dtype) {
+  // the window's value is checked here; its pairing with a causal kind is
+  // the forward's check
+  if (window < 0 || check_sizes(batch, max_q, max_k, total_q, max_k, hq, hkv, d,
+                                ATTN_MASK_NONE, 0, dtype) != ATTN_OK)
     return (size_t)-1;
-  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, dtype, sm_count());
+  TcPlan plan =
+      choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype, sm_count());
   if (plan.kind != PLAN_TC_SPLIT) return 0;
   return fwd_split_workspace(plan, total_q, hq, d);
 }
@@ -141,9 +145,10 @@ size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      float *o_f32, const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
-                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
+                     attn_mask_kind mask, int window, attn_dtype dtype, void *workspace,
                      size_t workspace_bytes, void *stream) {
-  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+  attn_status st =
+      check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
@@ -156,13 +161,15 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
   p.batch = batch; p.max_q = max_q; p.max_k = max_k; p.total_q = total_q; p.total_k = total_k;
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
+  p.window = window;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   if (batch == 0 || total_q == 0 || max_q == 0) {
     set_plan("empty");
     return ATTN_OK;
   }
-  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, dtype, sm_count());
+  TcPlan plan =
+      choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype, sm_count());
   if (plan.kind != PLAN_SIMT) {
     // TMA needs 16-byte aligned tensors; with no keys at all every row is
     // empty and the CUDA-core kernel writes the zeros and -inf directly.
@@ -205,7 +212,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
 
 size_t attn_bwd_workspace_size(int batch, int max_q, int max_k, int total_q, int total_k,
                                int hq, int hkv, int d, attn_dtype dtype) {
-  if (check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, ATTN_MASK_NONE, dtype) !=
+  if (check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, ATTN_MASK_NONE, 0, dtype) !=
       ATTN_OK)
     return (size_t)-1;
   return bwd_layout(total_q, total_k, hq, hkv, d, dtype).total;
@@ -215,9 +222,10 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const float *lse, const float *o_f32, const void *dout, void *dq, void *dk, void *dv,
                      const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
-                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
+                     attn_mask_kind mask, int window, attn_dtype dtype, void *workspace,
                      size_t workspace_bytes, void *stream) {
-  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, dtype);
+  attn_status st =
+      check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
@@ -234,6 +242,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   p.batch = batch; p.max_q = max_q; p.max_k = max_k; p.total_q = total_q; p.total_k = total_k;
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
+  p.window = window;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   char *ws = static_cast<char *>(workspace);
@@ -277,8 +286,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
 
 attn_status attn_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
                             int max_k, int total_q, int total_k, attn_mask_kind mask,
-                            int tile_rows, uint8_t *out, void *stream) {
-  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, 1, 1, 64, mask,
+                            int window, int tile_rows, uint8_t *out, void *stream) {
+  attn_status st = check_sizes(batch, max_q, max_k, total_q, total_k, 1, 1, 64, mask, window,
                                ATTN_DTYPE_BF16);
   if (st != ATTN_OK) return st;
   if (tile_rows != 16 && tile_rows != 32 && tile_rows != 64 && tile_rows != 128)
@@ -290,7 +299,8 @@ attn_status attn_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch,
   if (!err) return ATTN_ERR_CUDA;
   if ((long long)total_q * total_k == 0) return ATTN_OK;
   cudaError_t ce = launch_mask_probe(cu_q, cu_k, batch, max_q, max_k, total_q, total_k, mask,
-                                     tile_rows, out, err, static_cast<cudaStream_t>(stream));
+                                     window, tile_rows, out, err,
+                                     static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.z, h = blockIdx.y;
   const int i = blockIdx.x * 4 + warp;
-  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -88,11 +88,12 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   }
   const float lse2 = p.lse2[(size_t)h * p.total_q + t];
   const float D_i = p.delta[(size_t)h * p.total_q + t];
+  const int kbeg = key_begin(g.mask, g.window, i, g.nq, g.nk);
   const int kend = key_end(g.mask, i, g.nq, g.nk);
   const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const size_t stride = (size_t)p.hkv * D;
-  for (int j = 0; j < kend; j++) {
+  for (int j = kbeg; j < kend; j++) {
     float kf[E], ps = 0.f, pd = 0.f;
 #pragma unroll
     for (int e = 0; e < E; e++) {
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.z, hk = blockIdx.y;
   const int j = blockIdx.x * 4 + warp;  // in-sequence key
-  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -137,8 +138,9 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
     dv[e] = 0.f;
   }
   const int i_begin = row_begin(g.mask, j, g.nq, g.nk);
+  const int i_end = row_end(g.mask, g.window, j, g.nq, g.nk);
   for (int h = hk * grp; h < hk * grp + grp; h++) {
-    for (int i = i_begin; i < g.nq; i++) {
+    for (int i = i_begin; i < i_end; i++) {
       const int t = g.q0 + i;
       const size_t row = (size_t)t * p.hq + h;
       const T *qp = reinterpret_cast<const T *>(p.q) + row * D + lane * E;

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = (int)blockIdx.x / per_rank;
   const int hk = (int)blockIdx.x % p.hkv;
   const int seq = ((int)blockIdx.x % per_rank) / p.hkv;
-  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && n == 0 && hk == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j0 = n * kKeysA;
   if (j0 >= g.nk) return;
   // 64-row query tiles with at least one row that sees a key of this tile
+  // (rows [row_begin(j), row_end(j)) see key j; both ends grow with j)
+  const int j_last = (j0 + kKeysA < g.nk ? j0 + kKeysA : g.nk) - 1;
   const int m_begin = row_begin(g.mask, j0, g.nq, g.nk) / kRowsA;
-  const int m_end = (g.nq + kRowsA - 1) / kRowsA;
+  const int m_end = (row_end(g.mask, g.window, j_last, g.nq, g.nk) + kRowsA - 1) / kRowsA;
   const int n_m = m_end > m_begin ? m_end - m_begin : 0;
   const int n_it = n_m * a.group;
 
@@ -254,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;      // key lane
     const int tid = threadIdx.x - 64;  // 0 .. 255; threads below 128 fetch row terms
     const int j = j0 + r;          // in-sequence key
-    const int rb = key_row_begin(g.mask, j, g.nq, g.nk);  // rows [rb, nq) see key j
+    const int rb = key_row_begin(g.mask, j, g.nq, g.nk);  // rows [rb, re) see key j
+    const int re = key_row_end(g.mask, g.window, j, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     bool ok = true;
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) continue;
       tc_fence_after();
-      const int c_lo = rb - i0, c_hi = g.nq - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
+      const int c_lo = rb - i0, c_hi = re - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
       const bool full = c_lo <= 0 && c_hi >= kRowsA;
       const uint64_t c2x2 = f2(c2, c2);
       uint32_t pp[16], dd[16];
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = (int)blockIdx.x % p.hq;
   const int seq = ((int)blockIdx.x % per_rank) / p.hq;
   const int m_tile = a.n_row_tiles - 1 - rank;
-  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && rank == 0 && h == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -424,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int i0 = m_tile * kTileRows;
   if (i0 >= g.nq) return;
-  const KvRange kr = plan_kv_tiles(g.mask, g.nq, g.nk, i0, kTileRows, kTileKeys);
-  const int n_tiles = kr.n_end;
+  const KvRange kr = plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0, kTileRows, kTileKeys);
+  const int n_first = kr.n_begin;              // key tiles [n_first, n_first + n_tiles)
+  const int n_tiles = kr.n_end - kr.n_begin;
   const int hk = h / a.group;
 
   if (threadIdx.x == 0) {
@@ -468,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int jj = 0; jj < n_tiles; jj++) {
         const int st = jj & 1, u = jj >> 1;
-        const int key_row = g.k0 + jj * kTileKeys;
+        const int key_row = g.k0 + (n_first + jj) * kTileKeys;
         if (jj >= 2 && !wait_bar(&b->sync, &b->k_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
         for (int c = 0; c < L::kChunks; c++)
@@ -552,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
+    const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
     const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
     const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
     const uint64_t c2x2 = f2(c2, c2), nl2 = f2(-lse2, -lse2), nd2 = f2(-D_i, -D_i);
@@ -565,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const bool boundary = jj >= kr.n_full;
-      const int jb = jj * kTileKeys;
+      const bool boundary = !kr.full(n_first + jj);
+      const int jb = (n_first + jj) * kTileKeys;
       // dS (fp16 pairs) of this warp's 64 keys goes over the first 32 of the
       // S columns it read.
       uint32_t dd[32];
@@ -583,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, nl2), x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           if (boundary) {
-            if (jb + c >= row_limit) p0 = 0.f;
-            if (jb + c + 1 >= row_limit) p1 = 0.f;
+            if (jb + c >= row_limit || jb + c < row_first) p0 = 0.f;
+            if (jb + c + 1 >= row_limit || jb + c + 1 < row_first) p1 = 0.f;
           }
           float d0, d1;
           f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)),

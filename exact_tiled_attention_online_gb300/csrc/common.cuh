@@ -17,21 +17,25 @@ constexpr float kLn2 = 0.6931471805599453f;
 // ---------------------------------------------------------------------------
 // Sequence geometry ("causal-mask-and-ragged-sequence-layouts", first and
 // third paragraphs).  Every alignment rule allows, for query row i of a
-// sequence, a prefix of that sequence's keys: j < key_end(i).  Tiles take
-// in-sequence coordinates (row i, key j) before any comparison, so a packed
-// global offset never becomes a position.
+// sequence, one interval of that sequence's keys: key_begin(i) <= j <
+// key_end(i), a prefix (key_begin = 0) unless a bounded window keeps only
+// the last `window` positions up to the causal bound ("attention-algorithm-
+// error-and-complexity-tests", fifth paragraph).  Both ends are
+// non-decreasing in i.  Tiles take in-sequence coordinates (row i, key j)
+// before any comparison, so a packed global offset never becomes a position.
 // ---------------------------------------------------------------------------
 struct SeqGeom {
   int q0, nq;  // first packed query token, number of queries
   int k0, nk;  // first packed key token, number of keys
   int mask;    // attn_mask_kind
+  int window;  // > 0: bounded window of that many keys (causal kinds only)
   bool ok;     // cu_seqlens consistent with the sizes passed
 };
 
 __device__ __forceinline__ SeqGeom load_seq(const int32_t *__restrict__ cu_q,
                                             const int32_t *__restrict__ cu_k,
                                             int s, int total_q, int total_k,
-                                            int max_q, int max_k, int mask) {
+                                            int max_q, int max_k, int mask, int window) {
   SeqGeom g;
   g.q0 = __ldg(cu_q + s);
   int q1 = __ldg(cu_q + s + 1);
@@ -40,6 +44,7 @@ __device__ __forceinline__ SeqGeom load_seq(const int32_t *__restrict__ cu_q,
   g.nq = q1 - g.q0;
   g.nk = k1 - g.k0;
   g.mask = mask;
+  g.window = window;
   g.ok = g.q0 >= 0 && g.k0 >= 0 && g.nq >= 0 && g.nk >= 0 && q1 <= total_q &&
          k1 <= total_k && g.nq <= max_q && g.nk <= max_k;
   if (!g.ok) {
@@ -61,6 +66,14 @@ __host__ __device__ __forceinline__ int key_end(int mask, int i, int nq, int nk)
   return e < 0 ? 0 : (e > nk ? nk : e);
 }
 
+// First allowed key of in-sequence row i: 0 without a window, else the
+// first of the `window` positions that end at the causal bound i + off.
+__host__ __device__ __forceinline__ int key_begin(int mask, int window, int i, int nq, int nk) {
+  if (mask == ATTN_MASK_NONE || window <= 0) return 0;
+  int b = i + causal_offset(mask, nq, nk) + 1 - window;
+  return b < 0 ? 0 : (b > nk ? nk : b);
+}
+
 // First in-sequence query row that is allowed to see key j (rows below it do
 // not); rows >= nq are out of range.
 __host__ __device__ __forceinline__ int row_begin(int mask, int j, int nq, int nk) {
@@ -69,56 +82,82 @@ __host__ __device__ __forceinline__ int row_begin(int mask, int j, int nq, int n
   return b < 0 ? 0 : b;
 }
 
+// Exclusive end of the query rows that see key j: a window drops every row
+// whose causal bound lies `window` or more positions past j.
+__host__ __device__ __forceinline__ int row_end(int mask, int window, int j, int nq, int nk) {
+  if (mask == ATTN_MASK_NONE || window <= 0) return nq;
+  int e = j - causal_offset(mask, nq, nk) + window;
+  return e < 0 ? 0 : (e > nq ? nq : e);
+}
+
 // ---------------------------------------------------------------------------
 // Tile planner.  A tile holds in-sequence query rows [i0, i0 + rows) (rows
-// past nq are out-of-range lanes) against key tiles of bn keys.  Because
-// key_end() is non-decreasing in i, the tile needs key tiles [0, n_end) with
-// n_end from its last in-range row, and key tiles below n_full lie entirely
-// inside the smallest row bound, so they need no per-element mask.
+// past nq are out-of-range lanes) against key tiles of bn keys.  Because both
+// ends of a row's key interval are non-decreasing in i, the tile needs key
+// tiles [n_begin, n_end): n_begin from its first row's start and n_end from
+// its last in-range row's end.  Key tiles in [n_full_begin, n_full_end) lie
+// inside every in-range row's interval, so they need no per-element mask.
 // ---------------------------------------------------------------------------
 struct KvRange {
-  int n_end;   // key tiles [0, n_end) hold every allowed key of the tile
-  int n_full;  // key tiles [0, n_full) are allowed for every in-range row
+  int n_begin, n_end;            // key tiles holding every allowed key of the tile
+  int n_full_begin, n_full_end;  // key tiles allowed for every in-range row
+  __host__ __device__ bool full(int n) const { return n >= n_full_begin && n < n_full_end; }
 };
 
-__host__ __device__ __forceinline__ KvRange plan_kv_tiles(int mask, int nq, int nk, int i0,
-                                                           int rows, int bn) {
-  KvRange r{0, 0};
+__host__ __device__ __forceinline__ KvRange plan_kv_tiles(int mask, int window, int nq, int nk,
+                                                           int i0, int rows, int bn) {
+  KvRange r{0, 0, 0, 0};
   int i_last = (i0 + rows < nq ? i0 + rows : nq) - 1;
   if (i_last < i0) return r;
-  int kend_max = key_end(mask, i_last, nq, nk);
-  int kend_min = key_end(mask, i0, nq, nk);
-  r.n_end = (kend_max + bn - 1) / bn;
-  r.n_full = kend_min / bn;
+  const int kb_first = key_begin(mask, window, i0, nq, nk);
+  const int kb_last = key_begin(mask, window, i_last, nq, nk);
+  const int ke_first = key_end(mask, i0, nq, nk);
+  const int ke_last = key_end(mask, i_last, nq, nk);
+  r.n_begin = kb_first / bn;
+  r.n_end = (ke_last + bn - 1) / bn;
+  if (r.n_end < r.n_begin) r.n_end = r.n_begin;
+  r.n_full_begin = (kb_last + bn - 1) / bn;
+  r.n_full_end = ke_first / bn;
   return r;
 }
 
-// Key tiles [*a, *b) of split `split` out of n_splits over [0, n_end).
-__host__ __device__ __forceinline__ void split_tiles(int n_end, int split, int n_splits, int *a,
-                                                     int *b) {
-  int per = (n_end + n_splits - 1) / n_splits;
+// Key tiles [*a, *b) of split `split` out of n_splits over [n_begin, n_end).
+__host__ __device__ __forceinline__ void split_tiles(int n_begin, int n_end, int split,
+                                                     int n_splits, int *a, int *b) {
+  const int n = n_end - n_begin;
+  int per = (n + n_splits - 1) / n_splits;
   int lo = split * per;
-  *a = lo < n_end ? lo : n_end;
-  *b = lo + per < n_end ? lo + per : n_end;
+  *a = n_begin + (lo < n ? lo : n);
+  *b = n_begin + (lo + per < n ? lo + per : n);
 }
 
 // Per-lane predicate on a boundary tile, hoisted per row: lane (row i, key j)
-// is allowed iff j < row_key_limit(i).  Out-of-range rows get 0, so none of
-// their lanes are allowed; keys past the sequence end are never allowed
-// because key_end() <= nk.
+// is allowed iff row_key_first(i) <= j < row_key_limit(i).  Out-of-range rows
+// get a limit of 0, so none of their lanes are allowed; keys past the
+// sequence end are never allowed because key_end() <= nk.
 __host__ __device__ __forceinline__ int row_key_limit(int mask, int i, int nq, int nk) {
   return i < nq ? key_end(mask, i, nq, nk) : 0;
 }
 
-__host__ __device__ __forceinline__ bool lane_allowed(int mask, int i, int j, int nq, int nk) {
-  return j < row_key_limit(mask, i, nq, nk);
+__host__ __device__ __forceinline__ int row_key_first(int mask, int window, int i, int nq,
+                                                      int nk) {
+  return i < nq ? key_begin(mask, window, i, nq, nk) : 0;
+}
+
+__host__ __device__ __forceinline__ bool lane_allowed(int mask, int window, int i, int j, int nq,
+                                                      int nk) {
+  return j >= row_key_first(mask, window, i, nq, nk) && j < row_key_limit(mask, i, nq, nk);
 }
 
 // The same predicate hoisted per key (the backward's transposed tiles): lane
-// (row i, key j) is allowed iff key_row_begin(j) <= i < nq.  For j >= nk no
-// row is allowed.
+// (row i, key j) is allowed iff key_row_begin(j) <= i < key_row_end(j).  For
+// j >= nk no row is allowed.
 __host__ __device__ __forceinline__ int key_row_begin(int mask, int j, int nq, int nk) {
   return j < nk ? row_begin(mask, j, nq, nk) : nq;
+}
+
+__host__ __device__ __forceinline__ int key_row_end(int mask, int window, int j, int nq, int nk) {
+  return j < nk ? row_end(mask, window, j, nq, nk) : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -163,6 +202,7 @@ struct FwdParams {
   int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
   float scale, scale_log2;  // scale and scale * log2(e)
   int mask;
+  int window;  // > 0: bounded window (causal kinds only)
   int *err;
   // split-KV partial outputs (NULL when the plan writes o/lse directly)
   float *o_part, *lse_part;
@@ -178,6 +218,7 @@ struct BwdParams {
   int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
   float scale, scale_log2;
   int mask;
+  int window;  // > 0: bounded window (causal kinds only)
   int *err;
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i
   float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)

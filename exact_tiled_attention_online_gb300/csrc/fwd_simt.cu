@@ -1,5 +1,5 @@
 // fwd_simt.cu -- CUDA-core forward: one warp per (query row, head), the keys
-// of the row's allowed prefix streamed in order through the online-softmax
+// of the row's allowed interval streamed in order through the online-softmax
 // recurrence ("formal-correctness", "The FlashAttention Proof": running max,
 // rescale of denominator and accumulator when the max moves, final divide).
 //
@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s = blockIdx.z, h = blockIdx.y;
   const int i = blockIdx.x * 4 + warp;  // in-sequence query row
-  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  SeqGeom g = load_seq(p.cu_q, p.cu_k, s, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -33,12 +33,13 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     qf[e] = Elem<T>::to_f(qp[e]) * p.scale_log2;
     acc[e] = 0.f;
   }
+  const int kbeg = key_begin(g.mask, g.window, i, g.nq, g.nk);
   const int kend = key_end(g.mask, i, g.nq, g.nk);
   float m = -INFINITY, l = 0.f;
   const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const size_t stride = (size_t)p.hkv * D;
-  for (int j = 0; j < kend; j++) {
+  for (int j = kbeg; j < kend; j++) {
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * stride + e]);
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     m = m_new;
   }
   T *op = reinterpret_cast<T *>(p.o) + ((size_t)t * p.hq + h) * D + lane * E;
-  const float inv = kend > 0 ? 1.f / l : 0.f;
+  const float inv = kend > kbeg ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; e++) op[e] = Elem<T>::from_f(acc[e] * inv);
   if (p.o_f32) {
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     for (int e = 0; e < E; e++) of[e] = acc[e] * inv;
   }
   if (p.lse && lane == 0)
-    p.lse[(size_t)h * p.total_q + t] = kend > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+    p.lse[(size_t)h * p.total_q + t] = kend > kbeg ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t st) {

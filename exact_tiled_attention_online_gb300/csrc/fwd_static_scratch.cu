@@ -16,7 +16,7 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
 int *internal_error_flag();
 attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
-                                 int hq, int hkv, int d, int mask, int dtype);
+                                 int hq, int hkv, int d, int mask, int window, int dtype);
 int internal_sm_count();
 void internal_set_plan(const char *s);
 
@@ -48,17 +48,17 @@ using namespace attn;
 extern "C" attn_status attn_fwd_static_scratch(
     const void *q, const void *k, const void *v, void *o, float *lse, float *o_f32,
     const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
-    int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask, attn_dtype dtype,
-    void *stream) {
+    int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask, int window,
+    attn_dtype dtype, void *stream) {
   attn_status st = internal_check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask,
-                                        dtype);
+                                        window, dtype);
   if (st != ATTN_OK) return st;
-  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, dtype,
+  TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype,
                                 internal_sm_count());
   if (plan.kind != PLAN_TC_SPLIT || total_k == 0) {
     // Nothing to keep in scratch: the workspace-free attn_fwd path.
     return attn_fwd(q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q, total_k,
-                    hq, hkv, d, scale, mask, dtype, nullptr, 0, stream);
+                    hq, hkv, d, scale, mask, window, dtype, nullptr, 0, stream);
   }
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (!cu_q || !cu_k || !q || !o || !k || !v) return ATTN_ERR_INVALID_ARG;
@@ -78,6 +78,7 @@ extern "C" attn_status attn_fwd_static_scratch(
   p.batch = batch; p.max_q = max_q; p.max_k = max_k; p.total_q = total_q; p.total_k = total_k;
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
+  p.window = window;
   p.err = err;
   // Same carving as the caller-provided workspace of attn_fwd: partial
   // outputs first, partial logsumexps after them.

@@ -21,11 +21,12 @@
 // reference, so O / l and lse = m + log2(l) are exact either way, and P stays
 // below 2^kRescaleLog2.
 //
-// Masking follows the tile planner of common.cuh: key tiles below n_full are
-// allowed for every in-range row and skip the per-lane test; boundary tiles
-// set the scores of disallowed lanes (other sequence, past the key range,
-// past the causal bound, out-of-range rows) to -inf before the row max
-// ("causal-mask-and-ragged-sequence-layouts", second paragraph).
+// Masking follows the tile planner of common.cuh: key tiles in the planner's
+// full range are allowed for every in-range row and skip the per-lane test;
+// boundary tiles set the scores of disallowed lanes (other sequence, past the
+// key range, past the causal bound, before a bounded window's start,
+// out-of-range rows) to -inf before the row max ("causal-mask-and-ragged-
+// sequence-layouts", second paragraph).
 #include <cudaTypedefs.h>
 #include <stdio.h>
 
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = (rem / n_heads) % a.n_splits;
   const int seq = rem / (n_heads * a.n_splits);
   const int m_tile = a.n_m_tiles - 1 - rank;
-  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && rank == 0 && head_idx == 0 && split == 0)
       raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
@@ -130,9 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int i0 = m_tile * a.tile_tokens;
   if (i0 >= g.nq) return;  // the whole CTA leaves together
-  const KvRange kr = plan_kv_tiles(g.mask, g.nq, g.nk, i0, a.tile_tokens, kTileKeys);
-  int n_begin = 0, n_stop = kr.n_end;
-  if (a.n_splits > 1) split_tiles(kr.n_end, split, a.n_splits, &n_begin, &n_stop);
+  const KvRange kr = plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0, a.tile_tokens, kTileKeys);
+  int n_begin = kr.n_begin, n_stop = kr.n_end;
+  if (a.n_splits > 1) split_tiles(kr.n_begin, kr.n_end, split, a.n_splits, &n_begin, &n_stop);
   const int n_tiles = n_stop - n_begin;
   const int kvh = a.pack ? head_idx : head_idx / a.group;
 
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_in = i < g.nq;
     const int t = g.q0 + i;
     const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
+    const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
@@ -268,11 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e++) raw[c * 32 + e] = u32[e];
       }
       tmem_wait_ld();
-      if (n >= kr.n_full) {  // boundary tile: keys at or past this row's limit
+      if (!kr.full(n)) {  // boundary tile: keys outside this row's interval
         const int limit = row_limit - n * kTileKeys;
+        const int first = row_first - n * kTileKeys;
 #pragma unroll
         for (int c = 0; c < kTileKeys; c++)
-          if (c >= limit) raw[c] = 0xff800000u;  // -inf
+          if (c >= limit || c < first) raw[c] = 0xff800000u;  // -inf
       }
       float mt;
       if constexpr (kPosScale) {  // the max of the raw scores scales to the max of the logits

@@ -93,17 +93,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int rank = (int)blockIdx.x / per_rank;
   const int h = (int)blockIdx.x % p.hq;
   const int seq = ((int)blockIdx.x % per_rank) / p.hq;
-  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask);
+  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
     if (threadIdx.x == 0 && rank == 0 && h == 0) raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
     return;
   }
   const int i0 = (a.n_pairs - 1 - rank) * 2 * kTileRows;  // first row of tile A
   if (i0 >= g.nq) return;
-  const KvRange kra = plan_kv_tiles(g.mask, g.nq, g.nk, i0, kTileRows, kTileKeys);
-  const KvRange krb = plan_kv_tiles(g.mask, g.nq, g.nk, i0 + kTileRows, kTileRows, kTileKeys);
-  const int na = kra.n_end, nb = krb.n_end;  // tile X is active on key tiles [0, n_X)
-  const int N = na > nb ? na : nb;
+  const KvRange kra = plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0, kTileRows, kTileKeys);
+  const KvRange krb =
+      plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0 + kTileRows, kTileRows, kTileKeys);
+  // Key tiles run n = n0 + u for u in [0, N).  Tile X is active on the u in
+  // [lo_X, hi_X) (an empty range when none of its rows sees a key); the two
+  // ranges overlap or touch, because tile B's first row starts its keys no
+  // later than tile A's last row ends them, so [0, N) has no unused tile.
+  const bool act_a = kra.n_end > kra.n_begin, act_b = krb.n_end > krb.n_begin;
+  const int n0 = act_a ? kra.n_begin : krb.n_begin;
+  const int lo_a = act_a ? kra.n_begin - n0 : 0, hi_a = act_a ? kra.n_end - n0 : 0;
+  const int lo_b = act_b ? krb.n_begin - n0 : 0, hi_b = act_b ? krb.n_end - n0 : 0;
+  const int N = hi_a > hi_b ? hi_a : hi_b;
   const int hk = h / a.group;
 
   if (threadIdx.x == 0) {
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                       g.q0 + i0 + t2 * kTileRows);
       for (int n = 0; n < N; n++) {
         const int st = n & 1, u = n >> 1;
-        const int key_row = g.k0 + n * kTileKeys;
+        const int key_row = g.k0 + (n0 + n) * kTileKeys;
         if (n >= 2 && !wait2(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
         for (int c = 0; c < L::kChunks; c++)
@@ -188,14 +196,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
           mma_bf16_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
                       (acc || kk > 0) ? 1u : 0u);
       };
+      // Tile X's c-th product (c = n - lo_X) completes phase c of its
+      // s_full / p_full / pv_done barriers.
+      auto in_a = [&](int n) { return n >= lo_a && n < hi_a; };
+      auto in_b = [&](int n) { return n >= lo_b && n < hi_b; };
       bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
-        if (na > 0) {
+        if (in_a(0)) {
           issue_qk(0, 0);
           mma_commit(&b->s_full[0]);
         }
-        if (nb > 0) {
+        if (in_b(0)) {
           issue_qk(1, 0);
           mma_commit(&b->s_full[1]);
         }
@@ -204,30 +216,30 @@ __global__ void __launch_bounds__(kThreads2, 1)
       for (int n = 0; ok && n < N; n++) {
         const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
         bool v_ready = false, k1_ready = false;
-        if (n < na) {
-          if (!(ok = wait2(b, &b->p_full[0], n & 1, p.err))) break;
+        if (in_a(n)) {
+          if (!(ok = wait2(b, &b->p_full[0], (n - lo_a) & 1, p.err))) break;
           if (!(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
           v_ready = true;
           tc_fence_after();
-          issue_pv(0, st, n > 0);
+          issue_pv(0, st, n > lo_a);
           mma_commit(&b->pv_done[0]);
         }
-        if (n1 < na) {
+        if (in_a(n1)) {
           if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           k1_ready = true;
           tc_fence_after();
           issue_qk(0, st1);
           mma_commit(&b->s_full[0]);
         }
-        if (n < nb) {
-          if (!(ok = wait2(b, &b->p_full[1], n & 1, p.err))) break;
+        if (in_b(n)) {
+          if (!(ok = wait2(b, &b->p_full[1], (n - lo_b) & 1, p.err))) break;
           if (!v_ready && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
           tc_fence_after();
-          issue_pv(1, st, n > 0);
+          issue_pv(1, st, n > lo_b);
           mma_commit(&b->pv_done[1]);
         }
         mma_commit(&b->v_empty[st]);
-        if (n1 < nb) {
+        if (in_b(n1)) {
           if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           tc_fence_after();
           issue_qk(1, st1);
@@ -245,8 +257,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const bool row_in = i < g.nq;
     const int t = g.q0 + i;
     const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
-    const int n_mine = x ? nb : na;
-    const int n_full = x ? krb.n_full : kra.n_full;
+    const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
+    const KvRange &kr = x ? krb : kra;
+    const int n_mine = kr.n_end - kr.n_begin;  // products of this tile
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_col = t_lane + (uint32_t)(x * kTileKeys);
     const uint32_t o_col = t_lane + 256u + (uint32_t)(x * D);
@@ -256,7 +269,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
     bool ok = true;
     // Scores of `nc` consecutive 32-column chunks starting at chunk c0, loaded
     // with one TMEM wait: raw (kPosScale) or scaled, masked to -inf.
-    auto load_chunks = [&](auto nc_tag, int c0, int limit, bool boundary, uint32_t *v) {
+    auto load_chunks = [&](auto nc_tag, int c0, int limit, int first, bool boundary,
+                           uint32_t *v) {
       constexpr int nc = decltype(nc_tag)::value;
 #pragma unroll
       for (int c = 0; c < nc; c++)
@@ -265,7 +279,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
       if (boundary) {
 #pragma unroll
         for (int e = 0; e < 32 * nc; e++)
-          if (c0 * 32 + e >= limit) v[e] = 0xff800000u;
+          // first <= limit, so one unsigned compare tests first <= key < limit
+          if ((unsigned)(c0 * 32 + e - first) >= (unsigned)(limit - first)) v[e] = 0xff800000u;
       }
       if constexpr (!kPosScale) {
 #pragma unroll
@@ -275,26 +290,28 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
       }
     };
-    for (int n = 0; n < n_mine; n++) {
-      ok = wait2(b, &b->s_full[x], n & 1, p.err);
+    for (int it = 0; it < n_mine; it++) {
+      const int n = kr.n_begin + it;  // key tile in the sequence
+      ok = wait2(b, &b->s_full[x], it & 1, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool boundary = n >= n_full;
+      const bool boundary = !kr.full(n);
       const int limit = row_limit - n * kTileKeys;
+      const int first = row_first - n * kTileKeys;
       // pass 1: row max, 64 scores per TMEM wait; the second half stays in
       // registers for pass 2
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       uint32_t v1[64];
       {
         uint32_t v0[64];
-        load_chunks(std::integral_constant<int, 2>{}, 0, limit, boundary, v0);
+        load_chunks(std::integral_constant<int, 2>{}, 0, limit, first, boundary, v0);
 #pragma unroll
         for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v0[e]));
       }
-      load_chunks(std::integral_constant<int, 2>{}, 2, limit, boundary, v1);
+      load_chunks(std::integral_constant<int, 2>{}, 2, limit, first, boundary, v1);
 #pragma unroll
       for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v1[e]));
       float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -332,7 +349,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       }
       {
         uint32_t v0[64], pk[32];
-        load_chunks(std::integral_constant<int, 2>{}, 0, limit, boundary, v0);
+        load_chunks(std::integral_constant<int, 2>{}, 0, limit, first, boundary, v0);
         exp_half(v0, pk);
         tmem_st32(s_col + 64, pk);
       }
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       m_ref = m_new;
       // S_x(n) landed after every earlier product of this thread, so the
       // previous P V into O_x is complete: O_x may be rescaled now.
-      if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c = 0; c < D / 32; c++) {
           uint32_t o32[32];

@@ -34,7 +34,7 @@ struct TcPlan {
 // all of them, and the keys are split across CTAs until the grid covers the
 // GPU several times over; the splits are merged by a combine kernel.
 inline TcPlan choose_fwd_plan(int batch, int max_q, int max_k, int total_q, int hq, int hkv,
-                              int d, attn_dtype dtype, int sms) {
+                              int d, int window, attn_dtype dtype, int sms) {
   (void)total_q;
   (void)d;
   TcPlan p{};
@@ -55,7 +55,12 @@ inline TcPlan choose_fwd_plan(int batch, int max_q, int max_k, int total_q, int 
   }
   p.n_m_tiles = (max_q + p.tile_tokens - 1) / p.tile_tokens;
   const long long ctas = (long long)batch * (p.pack ? hkv : hq) * p.n_m_tiles;
-  const int kv_tiles = (max_k + kTileKeys - 1) / kTileKeys;
+  int kv_tiles = (max_k + kTileKeys - 1) / kTileKeys;
+  if (window > 0) {  // a bounded window: a tile's keys span window + tile_tokens - 1
+    const long long span = (long long)window + p.tile_tokens - 1;
+    const long long w_tiles = (span + kTileKeys - 1) / kTileKeys + 1;
+    if (w_tiles < kv_tiles) kv_tiles = (int)w_tiles;
+  }
   // Split the keys across CTAs for decode (packed heads), or when even the
   // prefill kernel's 256-row CTAs would leave most SMs idle.
   const long long prefill_ctas = (long long)batch * hq * ((max_q + 2 * kTileRows - 1) / (2 * kTileRows));

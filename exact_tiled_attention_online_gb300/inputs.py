@@ -90,6 +90,9 @@ WORKLOADS = {
                                   32, 8, 128, "bf16", MASK_BOTTOM_RIGHT, 1003),
     "train_fwd_bwd": Workload("train_fwd_bwd", (8192,) * 2, (8192,) * 2, 16, 4,
                               128, "bf16", MASK_TOP_LEFT, 1004, backward=True),
+    # the prefill shape under a bounded causal window (linear pair work)
+    "window_prefill": Workload("window_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
+                               128, "bf16", MASK_TOP_LEFT, 1002, window=1024),
 }
 
 

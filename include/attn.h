@@ -31,6 +31,13 @@
  *   ATTN_MASK_NONE           every key of the sequence;
  *   ATTN_CAUSAL_TOP_LEFT     j <= i;
  *   ATTN_CAUSAL_BOTTOM_RIGHT j <= i + Nk - Nq.
+ * window (every call that takes a mask): 0 leaves the rule as it is; W > 0
+ * bounds it to the W key positions that end at the causal bound, i.e. it
+ * also requires j > i - W (top-left) or j > i + Nk - Nq - W (bottom-right),
+ * so every row sees at most W keys and the pair count grows linearly with
+ * the sequence length ("attention-algorithm-error-and-complexity-tests",
+ * fifth paragraph).  W > 0 needs a causal kind; a negative W, or W > 0 with
+ * ATTN_MASK_NONE, is ATTN_ERR_INVALID_ARG.
  * Pairs from different sequences are never allowed; tile lanes past a
  * sequence's end never enter the max, the denominator or a gradient sum
  * (same page, second paragraph).  A row with no allowed key gets O = 0 and
@@ -89,7 +96,7 @@ typedef enum {
  */
 size_t attn_fwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
                                int total_q, int n_heads_q, int n_heads_kv,
-                               int head_dim, attn_dtype dtype);
+                               int head_dim, int window, attn_dtype dtype);
 
 /*
  * Forward ("formal-correctness", "The FlashAttention Proof": the online
@@ -116,8 +123,8 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
                      const int32_t *cu_seqlens_k, int batch, int max_seqlen_q,
                      int max_seqlen_k, int total_q, int total_k, int n_heads_q,
                      int n_heads_kv, int head_dim, float scale,
-                     attn_mask_kind mask, attn_dtype dtype, void *workspace,
-                     size_t workspace_bytes, void *stream);
+                     attn_mask_kind mask, int window, attn_dtype dtype,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Workspace bytes attn_bwd needs: the per-row terms D_i = dO_i . O_i and the
@@ -133,7 +140,7 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
 
 /*
  * Backward at upstream gradient dout, recomputing the probabilities from q, k
- * and the saved lse with the same mask rule as the forward
+ * and the saved lse with the same mask rule and window as the forward
  * ("causal-mask-and-ragged-sequence-layouts", sixth paragraph):
  *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - dO_i . O_i),
  *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
@@ -156,8 +163,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
                      int batch, int max_seqlen_q, int max_seqlen_k,
                      int total_q, int total_k, int n_heads_q, int n_heads_kv,
                      int head_dim, float scale, attn_mask_kind mask,
-                     attn_dtype dtype, void *workspace, size_t workspace_bytes,
-                     void *stream);
+                     int window, attn_dtype dtype, void *workspace,
+                     size_t workspace_bytes, void *stream);
 
 /*
  * Mask probe (diagnostic): writes, for one query head, the packed allowed-pair
@@ -173,8 +180,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
 attn_status attn_mask_probe(const int32_t *cu_seqlens_q,
                             const int32_t *cu_seqlens_k, int batch,
                             int max_seqlen_q, int max_seqlen_k, int total_q,
-                            int total_k, attn_mask_kind mask, int tile_rows,
-                            uint8_t *out, void *stream);
+                            int total_k, attn_mask_kind mask, int window,
+                            int tile_rows, uint8_t *out, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
@@ -216,8 +223,8 @@ attn_status attn_fwd_static_scratch(const void *q, const void *k, const void *v,
                                     int max_seqlen_q, int max_seqlen_k,
                                     int total_q, int total_k, int n_heads_q,
                                     int n_heads_kv, int head_dim, float scale,
-                                    attn_mask_kind mask, attn_dtype dtype,
-                                    void *stream);
+                                    attn_mask_kind mask, int window,
+                                    attn_dtype dtype, void *stream);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status status);

@@ -11,7 +11,8 @@ def run_fwd(x, mask=None):
     w = x["workload"]
     dev = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
     o, lse = attn.fwd(dev["q"], dev["k"], dev["v"], dev["cu_seqlens_q"], dev["cu_seqlens_k"],
-                      w.max_q, w.max_k, w.mask if mask is None else mask, w.scale)
+                      w.max_q, w.max_k, w.mask if mask is None else mask, w.scale,
+                      window=w.window)
     torch.cuda.synchronize()
     assert attn.get_device_error() == 0
     return o, lse, dev
@@ -20,7 +21,7 @@ def run_fwd(x, mask=None):
 def oracle_fwd(x, rows=None):
     w = x["workload"]
     return oracle.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.scale,
-                      w.mask, rows=rows)
+                      w.mask, rows=rows, window=w.window)
 
 
 def sample_rows(w, n, seed):

@@ -39,7 +39,7 @@ def test_version_and_strings(lib):
 
 def _fwd(lib, **over):
     args = dict(q=1, k=1, v=1, o=1, lse=1, o_f32=None, cu_q=1, cu_k=1, batch=1, max_q=4, max_k=4,
-                total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, dtype=0,
+                total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, window=0, dtype=0,
                 ws=None, ws_bytes=0, stream=None)
     args.update(over)
     return lib.attn_fwd(*args.values())
@@ -53,6 +53,8 @@ def _fwd(lib, **over):
     ({"total_q": -5}, 1),
     ({"max_q": 8}, 1),                   # max_seqlen above total
     ({"mask": 7}, 1),
+    ({"window": -1}, 1),                 # negative window
+    ({"mask": 0, "window": 4}, 1),       # a window needs a causal rule
     ({"dtype": 9}, 1),
     ({"scale": float("nan")}, 1),
     ({"scale": float("inf")}, 1),
@@ -64,7 +66,8 @@ def test_fwd_rejects_bad_arguments(lib, over, code):
 
 
 def test_workspace_size_rejects_bad_arguments(lib):
-    assert lib.attn_fwd_workspace_size(1, 4, 4, 4, 3, 2, 64, 0) == ctypes.c_size_t(-1).value
+    assert lib.attn_fwd_workspace_size(1, 4, 4, 4, 3, 2, 64, 0, 0) == ctypes.c_size_t(-1).value
+    assert lib.attn_fwd_workspace_size(1, 4, 4, 4, 2, 1, 64, -3, 0) == ctypes.c_size_t(-1).value
     assert lib.attn_bwd_workspace_size(1, 4, 4, 4, 4, 2, 1, 80, 0) == ctypes.c_size_t(-1).value
 
 
@@ -78,9 +81,16 @@ def test_bwd_workspace_covers_rows_and_fp16_copies(lib):
 
 def test_bwd_rejects_missing_workspace(lib):
     st = lib.attn_bwd(1, 1, 1, 1, 1, None, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.1, 1, 0,
-                      None, 0, None)
+                      0, None, 0, None)
     assert st == 3
 
 
+def test_bwd_rejects_window_without_causal_rule(lib):
+    st = lib.attn_bwd(1, 1, 1, 1, 1, None, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.1, 0, 5,
+                      0, None, 0, None)
+    assert st == 1
+
+
 def test_probe_rejects_bad_tile_rows(lib):
-    assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, 48, 1, None) == 1
+    assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, 0, 48, 1, None) == 1
+    assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, -2, 128, 1, None) == 1

@@ -18,9 +18,10 @@ def run_fwd_bwd(x):
     w = x["workload"]
     d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
     o, lse, o32 = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"],
-                           w.max_q, w.max_k, w.mask, w.scale, want_o_f32=True)
+                           w.max_q, w.max_k, w.mask, w.scale, want_o_f32=True, window=w.window)
     dq, dk, dv = attn.bwd(d["q"], d["k"], d["v"], o, lse, d["dout"], d["cu_seqlens_q"],
-                          d["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, o_f32=o32)
+                          d["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, o_f32=o32,
+                          window=w.window)
     torch.cuda.synchronize()
     assert attn.get_device_error() == 0
     return o, lse, dq, dk, dv

@@ -15,9 +15,9 @@ SRC = r'''
 #include "exact_tiled_attention_online_gb300/csrc/plan.h"
 using namespace attn;
 int main() {
-  int b, mq, mk, hq, hkv, sms;
-  while (scanf("%d %d %d %d %d %d", &b, &mq, &mk, &hq, &hkv, &sms) == 6) {
-    TcPlan p = choose_fwd_plan(b, mq, mk, b * mq, hq, hkv, 128, ATTN_DTYPE_BF16, sms);
+  int b, mq, mk, hq, hkv, sms, w;
+  while (scanf("%d %d %d %d %d %d %d", &b, &mq, &mk, &hq, &hkv, &sms, &w) == 7) {
+    TcPlan p = choose_fwd_plan(b, mq, mk, b * mq, hq, hkv, 128, w, ATTN_DTYPE_BF16, sms);
     printf("%d %d %d %d\n", p.kind, p.pack, p.tile_tokens, p.n_splits);
   }
 }
@@ -36,9 +36,9 @@ def plan_bin(tmp_path_factory):
     return str(exe)
 
 
-def plan(exe, *shape):
-    out = subprocess.run([exe], input=" ".join(map(str, shape)), capture_output=True, text=True,
-                         check=True).stdout.split()
+def plan(exe, *shape, window=0):
+    out = subprocess.run([exe], input=" ".join(map(str, shape + (window,))), capture_output=True,
+                         text=True, check=True).stdout.split()
     return tuple(int(x) for x in out)
 
 
@@ -57,6 +57,14 @@ def test_prefill_one_head_per_tile_no_split(plan_bin):
 def test_long_single_query_mha_splits(plan_bin):
     kind, pack, tokens, splits = plan(plan_bin, 1, 1, 100000, 32, 32, 152)
     assert kind == 2 and pack == 0 and splits > 1
+
+
+def test_short_window_decode_does_not_split(plan_bin):
+    """A bounded window of 512 keys leaves a decode tile six key tiles, too few
+    to split; a long window still splits like the unbounded decode."""
+    assert plan(plan_bin, 32, 1, 32768, 32, 8, 152, window=512) == (1, 1, 32, 1)
+    kind, pack, tokens, splits = plan(plan_bin, 32, 1, 32768, 32, 8, 152, window=8192)
+    assert (kind, pack) == (2, 1) and splits >= 2
 
 
 def test_fp32_takes_cuda_cores(plan_bin, tmp_path):

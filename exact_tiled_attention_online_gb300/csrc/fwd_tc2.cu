@@ -9,15 +9,17 @@
 //   QK_A(n), QK_B(n), PV_A(n), QK_A(n+1), PV_B(n), QK_B(n+1), PV_A(n+1), ...
 //
 // so that while one softmax warpgroup turns its S into P, the tensor core is
-// busy with the other tile.  Warps: 0 TMA producer, 1 TMEM allocation and MMA
-// issue, 2..5 softmax of tile A, 6..9 softmax of tile B (thread = row = TMEM
-// lane).  TMEM: S_A, S_B, O_A, O_B; each tile's bf16 P overwrites the second
-// half of its S and feeds P V from tensor memory, so P never passes through
-// shared memory.  Shared memory: Q_A, Q_B and a 2-stage K/V ring.
+// busy with the other tile.  Warpgroups: the first holds warp 0 (TMA
+// producer) and warp 1 (TMEM allocation and MMA issue) and gives most of its
+// registers to the other two, which run the softmax of tile A (warps 4..7)
+// and tile B (warps 8..11), thread = row = TMEM lane.  TMEM: S_A, S_B, O_A,
+// O_B; each tile's bf16 P overwrites the second half of its S and feeds P V
+// from tensor memory, so P never passes through shared memory.  Shared
+// memory: Q_A, Q_B and a 2-stage K/V ring.
 //
-// The softmax reads S from TMEM twice (once for the row max, once for the
-// exponentials) 32 columns at a time, so a thread holds at most 32 scores and
-// the 64 packed probabilities.
+// With the extra registers a softmax thread loads its whole 128-score row
+// from TMEM with one wait, takes the max, and writes the 64 packed
+// probabilities back.
 #include <stdio.h>
 
 #include <type_traits>
@@ -32,7 +34,14 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads2 = 320;
+constexpr int kThreads2 = 384;
+// Registers per thread: the launch gives every thread kRegsLaunch (the most
+// 384 threads can have); the control warpgroup drops to kRegsCtl and the two
+// softmax warpgroups rise to kRegsSoftmax.
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 80, kRegsSoftmax = 208;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads2 * kRegsLaunch,
+              "the increases must not exceed what the decreases free");
+static_assert(kThreads2 * kRegsLaunch <= 65536, "register file");
 constexpr float kRescale2 = 8.0f;
 constexpr uint32_t kCols2 = 512;
 
@@ -141,7 +150,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
 
-  if (warp == 0) {
+  if (warp < 4) {
+    reg_dealloc<kRegsCtl>();
+    if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && N > 0) {
       tma_prefetch_desc(&tm_q);
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                       hk, key_row);
       }
     }
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && N > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
@@ -248,9 +259,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (n1 < N) mma_commit(&b->k_empty[st1]);
       }
     }
+    }
   } else {
+    reg_alloc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int x = warp >= 6 ? 1 : 0;  // tile A (0) or B (1)
+    const int x = warp >= 8 ? 1 : 0;  // tile A (0) or B (1)
     const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;
     const int i = i0 + x * kTileRows + r;
@@ -267,29 +280,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
-    // Scores of `nc` consecutive 32-column chunks starting at chunk c0, loaded
-    // with one TMEM wait: raw (kPosScale) or scaled, masked to -inf.
-    auto load_chunks = [&](auto nc_tag, int c0, int limit, int first, bool boundary,
-                           uint32_t *v) {
-      constexpr int nc = decltype(nc_tag)::value;
-#pragma unroll
-      for (int c = 0; c < nc; c++)
-        tmem_ld32(s_col + (c0 + c) * 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-      tmem_wait_ld();
-      if (boundary) {
-#pragma unroll
-        for (int e = 0; e < 32 * nc; e++)
-          // first <= limit, so one unsigned compare tests first <= key < limit
-          if ((unsigned)(c0 * 32 + e - first) >= (unsigned)(limit - first)) v[e] = 0xff800000u;
-      }
-      if constexpr (!kPosScale) {
-#pragma unroll
-        for (int e = 0; e < 32 * nc; e++) {
-          const float y = __uint_as_float(v[e]);
-          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : y * c2);
-        }
-      }
-    };
     for (int it = 0; it < n_mine; it++) {
       const int n = kr.n_begin + it;  // key tile in the sequence
       ok = wait2(b, &b->s_full[x], it & 1, p.err);
@@ -298,41 +288,53 @@ __global__ void __launch_bounds__(kThreads2, 1)
         break;
       }
       tc_fence_after();
-      const bool boundary = !kr.full(n);
-      const int limit = row_limit - n * kTileKeys;
-      const int first = row_first - n * kTileKeys;
-      // pass 1: row max, 64 scores per TMEM wait; the second half stays in
-      // registers for pass 2
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      uint32_t v1[64];
-      {
-        uint32_t v0[64];
-        load_chunks(std::integral_constant<int, 2>{}, 0, limit, first, boundary, v0);
+      // the whole row of 128 scores, one TMEM wait
+      uint32_t v[kTileKeys];
 #pragma unroll
-        for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v0[e]));
+      for (int c = 0; c < kTileKeys / 32; c++)
+        tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_wait_ld();
+      if (!kr.full(n)) {
+        // lanes outside [first, limit) of this row: first <= limit, so one
+        // unsigned compare tests both ends
+        const int first = row_first - n * kTileKeys;
+        const unsigned span = (unsigned)(row_limit - row_first);
+#pragma unroll
+        for (int e = 0; e < kTileKeys; e++)
+          if ((unsigned)(e - first) >= span) v[e] = 0xff800000u;
       }
-      load_chunks(std::integral_constant<int, 2>{}, 2, limit, first, boundary, v1);
+      if constexpr (!kPosScale) {
 #pragma unroll
-      for (int e = 0; e < 64; e++) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(v1[e]));
+        for (int e = 0; e < kTileKeys; e++) {
+          const float y = __uint_as_float(v[e]);
+          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : y * c2);
+        }
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int e = 0; e < kTileKeys; e += 2)
+        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
       float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       if (kPosScale) mt *= c2;
       const float m_new = mt > m_ref + kRescale2 ? mt : m_ref;
       const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
       const float base = m_new == -INFINITY ? 0.f : m_new;
-      // pass 2: P = 2^(raw * c - base), two lanes per instruction; l sums fp32
-      // P (for lse), lr the bf16-rounded P that P V uses (so O / lr is an
-      // exact convex combination of V rows).
+      // P = 2^(raw * c - base), two lanes per instruction; l sums fp32 P (for
+      // lse), lr the bf16-rounded P that P V uses (so O / lr is an exact
+      // convex combination of V rows).  Each half of 64 scores becomes 32
+      // packed bf16 pairs over S columns [64, 128): keys [0, 64) at 64, keys
+      // [64, 128) at 96.
       const uint64_t cx2 = f2(cm, cm), nb2 = f2(-base, -base);
       uint64_t s2[2] = {0, 0}, r2[2] = {0, 0};
-      // Each half of 64 scores becomes 32 packed bf16 pairs; P goes over S
-      // columns [64, 128), whose scores pass 1 left in registers: half 1
-      // first, then half 0 reloaded from columns [0, 64), which P never
-      // touches.
-      auto exp_half = [&](const uint32_t (&v)[64], uint32_t (&pk)[32]) {
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           float x0, x1;
-          f2_split(ffma2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), cx2, nb2), x0, x1);
+          f2_split(ffma2(f2(__uint_as_float(v[64 * hh + e]), __uint_as_float(v[64 * hh + e + 1])),
+                         cx2, nb2),
+                   x0, x1);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           const int k = e / 2;
           s2[k & 1] = fadd2(s2[k & 1], f2(p0, p1));
@@ -341,17 +343,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             r2[k & 1] = fadd2(r2[k & 1], f2(__uint_as_float(pk[k] << 16),
                                             __uint_as_float(pk[k] & 0xffff0000u)));
         }
-      };
-      {
-        uint32_t pk[32];
-        exp_half(v1, pk);
-        tmem_st32(s_col + 96, pk);
-      }
-      {
-        uint32_t v0[64], pk[32];
-        load_chunks(std::integral_constant<int, 2>{}, 0, limit, first, boundary, v0);
-        exp_half(v0, pk);
-        tmem_st32(s_col + 64, pk);
+        tmem_st32(s_col + 64 + 32 * hh, pk);
       }
       {
         float a0, a1, b0, b1;

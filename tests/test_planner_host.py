@@ -5,7 +5,8 @@ bounded windows: "attention-algorithm-error-and-complexity-tests", fifth
 paragraph).
 
 Three views of the same rule must each equal the oracle bit for bit:
-  * forward tiles: a tile of query rows visits key tiles [n_begin, n_end),
+  * forward tiles: a tile of query rows visits key blocks [n_begin, n_end)
+    (128 keys, or 64 in the two-tile prefill),
     treats the planner's full tiles as allowed without a test, and applies
     the per-row interval test on the others;
   * backward dK/dV tiles: a 128-key tile visits 64-row query tiles from
@@ -34,12 +35,12 @@ SRC = r'''
 #include "exact_tiled_attention_online_gb300/csrc/common.cuh"
 #include "exact_tiled_attention_online_gb300/csrc/plan.h"
 using namespace attn;
-// stdin: batch mask window tile_rows, then batch pairs (nq nk)
+// stdin: batch mask window tile_rows key_block, then batch pairs (nq nk)
 // stdout: forward-view matrix, backward-view matrix (one row per line),
 //         then "contiguous <0|1>" and "oob <count>"
 int main() {
-  int batch, mask, window, tr;
-  if (scanf("%d %d %d %d", &batch, &mask, &window, &tr) != 4) return 1;
+  int batch, mask, window, tr, bn;
+  if (scanf("%d %d %d %d %d", &batch, &mask, &window, &tr, &bn) != 5) return 1;
   std::vector<int> nq(batch), nk(batch), cq(batch + 1, 0), ck(batch + 1, 0);
   for (int s = 0; s < batch; s++) {
     if (scanf("%d %d", &nq[s], &nk[s]) != 2) return 1;
@@ -52,13 +53,13 @@ int main() {
   for (int s = 0; s < batch; s++) {
     const int q = nq[s], k = nk[s];
     for (int i0 = 0; i0 < q; i0 += tr) {  // forward view
-      const KvRange kr = plan_kv_tiles(mask, window, q, k, i0, tr, kTileKeys);
+      const KvRange kr = plan_kv_tiles(mask, window, q, k, i0, tr, bn);
       for (int r = 0; r < tr; r++) {
         const int i = i0 + r;
         if (i >= q) continue;
         for (int n = kr.n_begin; n < kr.n_end; n++)
-          for (int c = 0; c < kTileKeys; c++) {
-            const int j = n * kTileKeys + c;
+          for (int c = 0; c < bn; c++) {
+            const int j = n * bn + c;
             const bool ok = kr.full(n) || lane_allowed(mask, window, i, j, q, k);
             if (!ok) continue;
             if (j >= k) { oob++; continue; }
@@ -67,8 +68,8 @@ int main() {
       }
     }
     for (int i0 = 0; i0 < q; i0 += 2 * kTileRows) {  // two-tile CTA
-      const KvRange a = plan_kv_tiles(mask, window, q, k, i0, kTileRows, kTileKeys);
-      const KvRange b = plan_kv_tiles(mask, window, q, k, i0 + kTileRows, kTileRows, kTileKeys);
+      const KvRange a = plan_kv_tiles(mask, window, q, k, i0, kTileRows, bn);
+      const KvRange b = plan_kv_tiles(mask, window, q, k, i0 + kTileRows, kTileRows, bn);
       if (a.n_end > a.n_begin && b.n_end > b.n_begin &&
           (b.n_begin > a.n_end || b.n_begin < a.n_begin || b.n_end < a.n_end))
         contiguous = 0;
@@ -110,8 +111,8 @@ def planner(tmp_path_factory):
     return str(exe)
 
 
-def run_planner(exe, lq, lk, mask, window, tile_rows):
-    text = f"{len(lq)} {mask} {window} {tile_rows}\n" + "\n".join(
+def run_planner(exe, lq, lk, mask, window, tile_rows, key_block=128):
+    text = f"{len(lq)} {mask} {window} {tile_rows} {key_block}\n" + "\n".join(
         f"{a} {b}" for a, b in zip(lq, lk)) + "\n"
     out = subprocess.run([exe], input=text, capture_output=True, text=True,
                          check=True).stdout.split("\n")
@@ -143,9 +144,10 @@ WINDOWS = [0, 1, 2, 64, 127, 128, 129, 300]
 def test_planner_matches_oracle(planner, lq, lk, mask):
     for window in WINDOWS if mask != pins.NONE else [0]:
         ref = oracle.mask(pins.cu(lq), pins.cu(lk), sum(lq), sum(lk), mask, window)
-        for tile_rows in (128, 32):
-            fw, bw, contiguous, oob = run_planner(planner, lq, lk, mask, window, tile_rows)
-            tag = (mask, window, tile_rows)
+        for tile_rows, key_block in ((128, 128), (32, 128), (128, 64)):
+            fw, bw, contiguous, oob = run_planner(planner, lq, lk, mask, window, tile_rows,
+                                                  key_block)
+            tag = (mask, window, tile_rows, key_block)
             assert oob == 0, tag
             assert np.array_equal(fw, ref), tag
             assert np.array_equal(bw, ref), tag

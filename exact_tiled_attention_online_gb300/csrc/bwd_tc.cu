@@ -56,6 +56,7 @@ struct Sync {
 };
 
 __device__ __forceinline__ bool wait_bar(Sync *sy, uint64_t *bar, uint32_t parity, int *err) {
+  if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (*reinterpret_cast<volatile int *>(&sy->abort)) return false;
   if (mbar_wait(bar, parity)) return true;
   *reinterpret_cast<volatile int *>(&sy->abort) = 1;

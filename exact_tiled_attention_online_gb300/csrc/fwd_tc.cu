@@ -78,6 +78,7 @@ __device__ __forceinline__ bool aborted(Bars *b) {
 }
 
 __device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err) {
+  if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (aborted(b)) return false;
   if (mbar_wait(bar, parity)) return true;
   *reinterpret_cast<volatile int *>(&b->abort) = 1;

@@ -72,6 +72,7 @@ struct Bars2 {
 };
 
 __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, int *err) {
+  if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (*reinterpret_cast<volatile int *>(&b->abort)) return false;
   if (mbar_wait(bar, parity)) return true;
   *reinterpret_cast<volatile int *>(&b->abort) = 1;

@@ -15,7 +15,8 @@ follows:
   sequence-layouts", first and third paragraphs), optionally bounded to the
   last ``window`` keys up to that causal bound (``window > 0``; the bounded
   window of "attention-algorithm-error-and-complexity-tests", fifth
-  paragraph);
+  paragraph), and optionally a linear positional bias -slope_h |i + off - j|
+  on every allowed logit (``slopes``);
 * forward: two-pass stable softmax over the allowed set, empty rows give
   O = 0 and lse = -inf (same page, fourth paragraph; "formal-correctness",
   "The FlashAttention Proof", online recurrence equals recomputed softmax);
@@ -89,6 +90,22 @@ def _i32(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
 
 
+_keep = []  # slope arrays handed to the C library stay alive until process exit
+
+
+def _slopes(slopes, hq: int):
+    """NULL, or a pointer to ``hq`` fp64 slopes."""
+    if slopes is None:
+        return None
+    a = _f64(slopes).reshape(-1)
+    if a.shape[0] != hq:
+        raise ValueError("one slope per query head")
+    _keep.append(a)
+    if len(_keep) > 64:
+        del _keep[:32]
+    return _ptr(a, _F64)
+
+
 class Oracle:
     """ctypes front end to one compiled copy of ``attn_oracle.c``.
 
@@ -106,7 +123,7 @@ class Oracle:
         L.oracle_mask.restype = ctypes.c_int
         common = [_F64, _F64, _F64]
         sizes = ([_I32, _I32] + [ctypes.c_int] * 6
-                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int])
+                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int, _F64])
         L.oracle_fwd.argtypes = common + sizes + [_I64, ctypes.c_int64, _F64, _F64]
         L.oracle_fwd.restype = ctypes.c_int
         L.oracle_bwd.argtypes = common + [_F64] + sizes + [_F64] * 5
@@ -143,7 +160,7 @@ class Oracle:
 
     # -- forward ------------------------------------------------------------
     def fwd(self, q, k, v, cu_q, cu_k, scale: float, mask_kind: int, rows=None,
-            window: int = 0):
+            window: int = 0, slopes=None):
         """Forward.  q [Tq, Hq, d], k/v [Tk, Hkv, d].
 
         rows None -> (o [Tq, Hq, d], lse [Hq, Tq]); rows = int array [n, 2] of
@@ -166,7 +183,7 @@ class Oracle:
         rc = self.lib.oracle_fwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1,
                                  tq, tk, hq, hkv, d, float(scale), mask_kind,
-                                 int(window), rp, n, _ptr(o, _F64),
+                                 int(window), _slopes(slopes, hq), rp, n, _ptr(o, _F64),
                                  _ptr(lse, _F64))
         if rc != 0:
             raise ValueError("invalid oracle_fwd arguments")
@@ -176,7 +193,7 @@ class Oracle:
 
     # -- backward -----------------------------------------------------------
     def bwd(self, q, k, v, dout, cu_q, cu_k, scale: float, mask_kind: int,
-            window: int = 0):
+            window: int = 0, slopes=None):
         """Full backward -> (dq, dk, dv, o, lse), fp64."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
         cq, ck = _i32(cu_q), _i32(cu_k)
@@ -190,7 +207,7 @@ class Oracle:
         rc = self.lib.oracle_bwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(dout, _F64), _ptr(cq, _I32), _ptr(ck, _I32),
                                  len(cq) - 1, tq, tk, hq, hkv, d, float(scale),
-                                 mask_kind, int(window), _ptr(dq, _F64),
+                                 mask_kind, int(window), _slopes(slopes, hq), _ptr(dq, _F64),
                                  _ptr(dk, _F64),
                                  _ptr(dv, _F64), _ptr(o, _F64), _ptr(lse, _F64))
         if rc != 0:
@@ -198,7 +215,7 @@ class Oracle:
         return dq, dk, dv, o, lse
 
     def bwd_sampled(self, q, k, v, dout, cu_q, cu_k, scale: float,
-                    mask_kind: int, q_rows, k_rows, window: int = 0):
+                    mask_kind: int, q_rows, k_rows, window: int = 0, slopes=None):
         """dQ at sampled (token, head) rows and dK, dV at sampled
         (key token, kv head) rows -> (dq [nq, d], dk [nk, d], dv [nk, d])."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -213,7 +230,7 @@ class Oracle:
         rc = self.lib.oracle_bwd_sampled(
             _ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64), _ptr(dout, _F64),
             _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1, tq, tk, hq, hkv, d,
-            float(scale), mask_kind, int(window), _ptr(qr, _I64), len(qr),
+            float(scale), mask_kind, int(window), _slopes(slopes, hq), _ptr(qr, _I64), len(qr),
             _ptr(dq, _F64),
             _ptr(kr, _I64), len(kr), _ptr(dk, _F64), _ptr(dv, _F64))
         if rc != 0:

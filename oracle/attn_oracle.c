@@ -34,6 +34,13 @@
  *     bounded window ("attention-algorithm-error-and-complexity-tests",
  *     fifth paragraph).
  *   - Pairs in different sequences are never allowed.
+ *   - slopes != NULL adds a linear positional bias to every allowed logit:
+ *     b_ij = -slopes[h] * |i + off - j|, the distance between key position j
+ *     and the row's causal bound i + off (off = Nk - Nq for bottom-right, 0
+ *     otherwise), so the key at the bound gets no bias ("attention-algorithm-
+ *     error-and-complexity-tests", third paragraph, and "causal-mask-and-
+ *     ragged-sequence-layouts", sixth paragraph: biases move with the
+ *     positions and are rebuilt the same way in the backward).
  *   - A row whose allowed set is empty has O = 0 exactly and lse = -inf
  *     (same page, fourth paragraph).
  *
@@ -64,6 +71,7 @@ typedef struct {
   double scale;
   int mask_kind;
   int window; /* > 0: at most `window` keys per row, the latest allowed ones */
+  const double *slopes; /* [hq] linear positional bias slopes, or NULL */
   int32_t *seq_q, *pos_q, *seq_k, *pos_k; /* per-token metadata */
 } problem_t;
 
@@ -119,6 +127,18 @@ static double dot(const double *a, const double *b, int d) {
   return acc;
 }
 
+/* The positional bias of query head h for an allowed (query token, key token)
+ * pair: 0 without slopes. */
+static double pos_bias(const problem_t *p, int tq, int tk, int h) {
+  if (!p->slopes) return 0.0;
+  int s = p->seq_q[tq];
+  int nq = p->cu_q[s + 1] - p->cu_q[s];
+  int nk = p->cu_k[s + 1] - p->cu_k[s];
+  int off = p->mask_kind == ORACLE_MASK_BOTTOM_RIGHT ? nk - nq : 0;
+  int dist = p->pos_q[tq] + off - p->pos_k[tk];
+  return -p->slopes[h] * fabs((double)dist);
+}
+
 static const double *q_row(const problem_t *p, int t, int h) {
   return p->q + ((size_t)t * p->hq + h) * p->d;
 }
@@ -149,7 +169,7 @@ static void forward_row(const problem_t *p, int t, int h, unsigned char *mrow,
   double m = -INFINITY;
   for (int u = 0; u < p->total_k; u++) {
     if (!mrow[u]) continue;
-    srow[u] = p->scale * dot(qi, k_row(p, u, hk), p->d);
+    srow[u] = p->scale * dot(qi, k_row(p, u, hk), p->d) + pos_bias(p, t, u, h);
     if (srow[u] > m) m = srow[u];
   }
   double l = 0.0;
@@ -168,7 +188,7 @@ static void forward_row(const problem_t *p, int t, int h, unsigned char *mrow,
 static int setup(problem_t *p, const double *q, const double *k,
                  const double *v, const int32_t *cu_q, const int32_t *cu_k,
                  int batch, int total_q, int total_k, int hq, int hkv, int d,
-                 double scale, int mask_kind, int window) {
+                 double scale, int mask_kind, int window, const double *slopes) {
   p->seq_q = p->pos_q = p->seq_k = p->pos_k = NULL;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0) return -1;
   if (mask_kind < 0 || mask_kind > 2) return -1;
@@ -187,6 +207,7 @@ static int setup(problem_t *p, const double *q, const double *k,
   p->scale = scale;
   p->mask_kind = mask_kind;
   p->window = window;
+  p->slopes = slopes;
   p->seq_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->pos_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->seq_k = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_k + 1));
@@ -211,7 +232,7 @@ int oracle_mask(const int32_t *cu_q, const int32_t *cu_k, int batch,
                 unsigned char *m) {
   problem_t p;
   int rc = setup(&p, NULL, NULL, NULL, cu_q, cu_k, batch, total_q, total_k, 1,
-                 1, 1, 1.0, mask_kind, window);
+                 1, 1, 1.0, mask_kind, window, NULL);
   if (rc == 0)
     for (int t = 0; t < total_q; t++)
       for (int u = 0; u < total_k; u++)
@@ -226,11 +247,11 @@ int oracle_mask(const int32_t *cu_q, const int32_t *cu_k, int batch,
 int oracle_fwd(const double *q, const double *k, const double *v,
                const int32_t *cu_q, const int32_t *cu_k, int batch,
                int total_q, int total_k, int hq, int hkv, int d, double scale,
-               int mask_kind, int window, const int64_t *rows, int64_t nrows,
-               double *o, double *lse) {
+               int mask_kind, int window, const double *slopes,
+               const int64_t *rows, int64_t nrows, double *o, double *lse) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind, window);
+                 scale, mask_kind, window, slopes);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -280,7 +301,7 @@ static void backward_row(const problem_t *p, const double *dout, int t, int h,
   for (int u = 0; u < p->total_k; u++) {
     if (!mrow[u]) continue;
     const double *kj = k_row(p, u, hk), *vj = v_row(p, u, hk);
-    double s = p->scale * dot(qi, kj, p->d);
+    double s = p->scale * dot(qi, kj, p->d) + pos_bias(p, t, u, h);
     double pij = exp(s - lse_i);
     double dpij = dot(doi, vj, p->d);
     double ds = pij * (dpij - D_i);
@@ -301,14 +322,14 @@ static void backward_row(const problem_t *p, const double *dout, int t, int h,
 int oracle_bwd(const double *q, const double *k, const double *v,
                const double *dout, const int32_t *cu_q, const int32_t *cu_k,
                int batch, int total_q, int total_k, int hq, int hkv, int d,
-               double scale, int mask_kind, int window, double *dq, double *dk,
-               double *dv, double *o, double *lse) {
+               double scale, int mask_kind, int window, const double *slopes,
+               double *dq, double *dk, double *dv, double *o, double *lse) {
   int rc = oracle_fwd(q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                      scale, mask_kind, window, NULL, 0, o, lse);
+                      scale, mask_kind, window, slopes, NULL, 0, o, lse);
   if (rc != 0) return rc;
   problem_t p;
   rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-             scale, mask_kind, window);
+             scale, mask_kind, window, slopes);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -359,13 +380,13 @@ int oracle_bwd_sampled(const double *q, const double *k, const double *v,
                        const double *dout, const int32_t *cu_q,
                        const int32_t *cu_k, int batch, int total_q,
                        int total_k, int hq, int hkv, int d, double scale,
-                       int mask_kind, int window, const int64_t *q_rows,
-                       int64_t nq_rows,
+                       int mask_kind, int window, const double *slopes,
+                       const int64_t *q_rows, int64_t nq_rows,
                        double *dq_out, const int64_t *k_rows, int64_t nk_rows,
                        double *dk_out, double *dv_out) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind, window);
+                 scale, mask_kind, window, slopes);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -413,7 +434,7 @@ int oracle_bwd_sampled(const double *q, const double *k, const double *v,
           size_t row = (size_t)t * hq + h;
           const double *qi = q_row(&p, t, h);
           const double *doi = dout + row * d;
-          double s = scale * dot(qi, kj, d);
+          double s = scale * dot(qi, kj, d) + pos_bias(&p, t, u, h);
           double pij = exp(s - lse[row]);
           double ds = pij * (dot(doi, vj, d) - D[row]);
           for (int c = 0; c < d; c++) {

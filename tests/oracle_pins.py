@@ -462,6 +462,130 @@ def pin_empty_rows_backward(orc):
     assert np.array_equal(dk, dk2) and np.array_equal(dv, dv2)
 
 
+# --------------------------------------------------------------------------
+# linear positional bias -slope_h |i + off - j| ("attention-algorithm-error-
+# and-complexity-tests", third paragraph; "causal-mask-and-ragged-sequence-
+# layouts", sixth paragraph)
+# --------------------------------------------------------------------------
+def bias_offset(kind, nq, nk):
+    return nk - nq if kind == BOTTOM_RIGHT else 0
+
+
+def slopes_for(hq, seed=40):
+    return np.random.default_rng(seed).uniform(0.05, 0.9, hq)
+
+
+def pin_bias_uniform_logits(orc):
+    """Q = 0: the logits are the bias alone, so O_i is the average of the
+    allowed V rows weighted by exp(-slope |i + off - j|), a closed form."""
+    rng = np.random.default_rng(41)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        q[:] = 0.0
+        sl = slopes_for(hq)
+        o, lse = orc.fwd(q, k, v, cu(lq), cu(lk), 0.37, kind, slopes=sl)
+        g = hq // hkv
+        cq, ck = cu(lq), cu(lk)
+        for s_, (nq, nk) in enumerate(zip(lq, lk)):
+            off = bias_offset(kind, nq, nk)
+            for i in range(nq):
+                a, b = row_range(kind, i, nq, nk)
+                t = cq[s_] + i
+                for h in range(hq):
+                    if b == a:
+                        assert np.all(o[t, h] == 0.0) and lse[h, t] == -math.inf
+                        continue
+                    js = np.arange(a, b)
+                    w = np.exp(-sl[h] * np.abs(i + off - js))
+                    ref = (w[:, None] * v[ck[s_] + js, h // g]).sum(0) / w.sum()
+                    np.testing.assert_allclose(o[t, h], ref, rtol=1e-12, atol=1e-12)
+                    assert abs(lse[h, t] - math.log(w.sum())) < 1e-12
+
+
+def pin_bias_zero_slopes(orc):
+    """Zero slopes give the unbiased result exactly."""
+    rng = np.random.default_rng(42)
+    for lq, lk, hq, hkv, d, kind in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        a = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind)
+        b = orc.bwd(q, k, v, do, cu(lq), cu(lk), 0.5, kind, slopes=np.zeros(hq))
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+
+
+def pin_bias_torch_sdpa_fp64(orc):
+    """torch's fp64 reference attention with the bias as an additive float
+    mask (-inf on disallowed pairs), forward and every gradient; windows and
+    the noncausal rule included."""
+    rng = np.random.default_rng(43)
+    cases = [(s_, 0) for s_ in SHAPES] + [(s_, 3) for s_ in SHAPES if s_[5] != NONE]
+    for (lq, lk, hq, hkv, d, kind), w in cases:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        sl = slopes_for(hq, seed=44)
+        scale = 1.0 / math.sqrt(d)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind, window=w, slopes=sl)
+        g = hq // hkv
+        cq, ck = cu(lq), cu(lk)
+        for s_, (nq, nk) in enumerate(zip(lq, lk)):
+            rows = [i for i in range(nq) if row_count(kind, i, nq, nk, w) > 0]
+            if not rows:
+                continue
+            off = bias_offset(kind, nq, nk)
+            bias = np.full((hq, nq, nk), -np.inf)
+            for i in range(nq):
+                a, b = row_range(kind, i, nq, nk, w)
+                js = np.arange(a, b)
+                bias[:, i, a:b] = -sl[:, None] * np.abs(i + off - js)[None, :]
+            qs = torch.tensor(q[cq[s_]:cq[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            ks = torch.tensor(k[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            vs = torch.tensor(v[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            ri = torch.tensor(rows)
+            out = torch.nn.functional.scaled_dot_product_attention(
+                qs[:, ri], ks.repeat_interleave(g, dim=0), vs.repeat_interleave(g, dim=0),
+                attn_mask=torch.tensor(bias[:, rows]), scale=scale)
+            dot = torch.tensor(do[cq[s_]:cq[s_ + 1]].transpose(1, 0, 2))[:, ri]
+            (out * dot).sum().backward()
+            np.testing.assert_allclose(o[cq[s_]:cq[s_ + 1]][rows], out.detach().numpy().transpose(1, 0, 2),
+                                       rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dq[cq[s_]:cq[s_ + 1]][rows],
+                                       qs.grad.numpy().transpose(1, 0, 2)[rows], rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dk[ck[s_]:ck[s_ + 1]], ks.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dv[ck[s_]:ck[s_ + 1]], vs.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+
+
+def pin_bias_finite_differences(orc):
+    """Central differences of L = sum O * dO with a bias (the bias does not
+    depend on Q, K or V, so the gradients keep their form)."""
+    rng = np.random.default_rng(45)
+    lq, lk = (3, 4), (5, 4)
+    hq, hkv, d, scale = 2, 1, 3, 0.7
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    do = rng.standard_normal(q.shape)
+    sl = np.array([0.3, 1.1])
+    for kind in (BOTTOM_RIGHT, NONE):
+        dq, dk, dv, _, _ = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind, slopes=sl)
+
+        def loss(qq, kk, vv):
+            o, _ = orc.fwd(qq, kk, vv, cu(lq), cu(lk), scale, kind, slopes=sl)
+            return float((o * do).sum())
+
+        h = 1e-5
+        for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xs = []
+                for sign in (1.0, -1.0):
+                    xx = x.copy()
+                    xx[idx] += sign * h
+                    xs.append({"q": (xx, k, v), "k": (q, xx, v), "v": (q, k, xx)}[name])
+                fd[idx] = (loss(*xs[0]) - loss(*xs[1])) / (2 * h)
+            np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=(name, kind))
+
+
 ALL_PINS = [
     pin_token_meta, pin_mask_intervals, pin_golden_mask_counts,
     pin_window_counts, pin_window_one_key, pin_window_covering_is_causal,
@@ -469,5 +593,6 @@ ALL_PINS = [
     pin_row_shift, pin_permutation_noncausal, pin_gqa_vs_repeat,
     pin_packed_vs_separate, pin_torch_sdpa_fp64, pin_finite_differences,
     pin_dv_column_sum, pin_dq_key_shift, pin_scale_identity,
-    pin_empty_rows_backward,
+    pin_empty_rows_backward, pin_bias_uniform_logits, pin_bias_zero_slopes,
+    pin_bias_torch_sdpa_fp64, pin_bias_finite_differences,
 ]

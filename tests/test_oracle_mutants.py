@@ -31,6 +31,16 @@ MUTANTS = {
     "window_off_by_one": ("bound - j >= p->window", "bound - j > p->window"),
     "window_ignored": ("if (p->window > 0 && bound - j >= p->window) return 0;", ""),
     "window_from_query_position": ("bound - j >= p->window", "i - j >= p->window"),
+    "bias_sign_flipped": ("return -p->slopes[h] * fabs((double)dist);",
+                          "return p->slopes[h] * fabs((double)dist);"),
+    "bias_without_offset": ("int off = p->mask_kind == ORACLE_MASK_BOTTOM_RIGHT ? nk - nq : 0;",
+                            "int off = 0;"),
+    "bias_signed_distance": ("return -p->slopes[h] * fabs((double)dist);",
+                             "return -p->slopes[h] * (double)dist;"),
+    "bias_global_positions": ("int dist = p->pos_q[tq] + off - p->pos_k[tk];",
+                              "int dist = tq + off - tk;"),
+    "bias_missing_in_backward": ("double s = p->scale * dot(qi, kj, p->d) + pos_bias(p, t, u, h);",
+                                 "double s = p->scale * dot(qi, kj, p->d);"),
     "window_accepted_without_causal": (
         "if (window > 0 && mask_kind == ORACLE_MASK_NONE) return -1;", ""),
     "global_offset_as_position": ("pos[t] = t - cu[s];", "pos[t] = t;"),

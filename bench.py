@@ -8,7 +8,8 @@ that are already resident in HBM:
   decode_q1/q16   split-KV decode, B=32, Nk=32768, Nq=1 / 16, bottom-right;
   train_fwd_bwd   forward + backward, B=2, N=8192, 16/4 heads, d=128;
   varlen_causal   packed ragged forward, 12 sequences, 16 heads, d=128;
-  window_prefill  the gqa_prefill shape under a bounded 1024-key causal window.
+  window_prefill  the gqa_prefill shape under a bounded 1024-key causal window;
+  bias_prefill    the gqa_prefill shape with a linear positional bias.
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -206,18 +207,20 @@ class Runner:
             bws = attn.bwd_workspace_size(w.batch, w.max_q, w.max_k, w.total_q, w.total_k, w.hq,
                                           w.hkv, w.d, attn.DTYPE_BF16)
             self.bws = torch.empty(max(bws, 1), dtype=torch.uint8, device=device)
+        self.slopes = inputs.bias_slopes(w.hq).to(device) if w.bias else None
         self.plans = []
 
     def run(self):
         a, w, x = self.attn, self.w, self.x
         a.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q, w.max_k,
               w.mask, w.scale, out=self.o, lse=self.lse, workspace=self.ws, o_f32=self.o32,
-              window=w.window)
+              window=w.window, bias_slopes=self.slopes)
         plans = [a.last_plan()]
         if w.backward:
             a.bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["dout"], x["cu_seqlens_q"],
                   x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, dq=self.dq, dk=self.dk,
-                  dv=self.dv, workspace=self.bws, o_f32=self.o32, window=w.window)
+                  dv=self.dv, workspace=self.bws, o_f32=self.o32, window=w.window,
+                  bias_slopes=self.slopes)
             plans.append(a.last_plan())
         self.plans = plans
 
@@ -241,7 +244,8 @@ def validate(r: Runner, n_rows=24):
     rows = np.stack([rng.integers(w.total_q, size=n_rows), rng.integers(w.hq, size=n_rows)], 1)
     host = {k: (t.cpu() if hasattr(t, "cpu") else t) for k, t in r.x.items()}
     o_ref, l_ref = oracle.fwd(host["q"], host["k"], host["v"], host["cu_seqlens_q"],
-                              host["cu_seqlens_k"], w.scale, w.mask, rows=rows, window=w.window)
+                              host["cu_seqlens_k"], w.scale, w.mask, rows=rows, window=w.window,
+                              slopes=inputs.bias_slopes(w.hq).double().numpy() if w.bias else None)
     on = r.o.double().cpu().numpy()[rows[:, 0], rows[:, 1]]
     ln = r.lse.double().cpu().numpy()[rows[:, 1], rows[:, 0]]
     err = np.abs(on - o_ref)
@@ -460,7 +464,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads",
                     default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
-                            "window_prefill")
+                            "window_prefill,bias_prefill")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

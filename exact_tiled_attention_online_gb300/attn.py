@@ -56,9 +56,9 @@ def library() -> ctypes.CDLL:
                            "(run exact_tiled_attention_online_gb300.build.build())")
     L = ctypes.CDLL(path)
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    L.attn_fwd.argtypes = [P, P, P, P, P, P, P, P] + [I] * 8 + [F, I, I, I, P, SZ, P]
+    L.attn_fwd.argtypes = [P, P, P, P, P, P, P, P] + [I] * 8 + [F, I, I, P, I, P, SZ, P]
     L.attn_fwd.restype = I
-    L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, I, P, SZ, P]
+    L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, P, I, P, SZ, P]
     L.attn_bwd.restype = I
     L.attn_fwd_workspace_size.argtypes = [I] * 9
     L.attn_fwd_workspace_size.restype = SZ
@@ -105,6 +105,15 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _slopes_ptr(slopes: Optional[torch.Tensor], hq: int) -> Optional[int]:
+    if slopes is None:
+        return None
+    _check(slopes, "bias_slopes", 1)
+    if slopes.dtype != torch.float32 or slopes.numel() != hq:
+        raise ValueError("bias_slopes must be fp32 with one slope per query head")
+    return slopes.data_ptr()
+
+
 def fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code, window=0) -> int:
     n = library().attn_fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, int(window),
                                           dtype_code)
@@ -125,11 +134,14 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
         mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
         workspace: Optional[torch.Tensor] = None, stream=None, want_lse: bool = True,
-        o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False, window: int = 0):
+        o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False, window: int = 0,
+        bias_slopes: Optional[torch.Tensor] = None):
     """Attention forward on packed ragged tensors (layouts in include/attn.h).
 
     ``window`` > 0 (causal masks only) bounds every row to the ``window`` key
-    positions that end at its causal bound.
+    positions that end at its causal bound.  ``bias_slopes`` (fp32 CUDA
+    tensor, one slope per query head) adds the linear positional bias
+    -slope_h * |i + off - j|.
 
     Returns (o, lse), or (o, lse, o_f32) when ``want_o_f32`` is set or an
     ``o_f32`` buffer is given.  lse is [n_heads_q, total_q] fp32 (None when
@@ -163,7 +175,7 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(o_f32), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k),
         batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv, d, float(scale),
-        int(mask), int(window), dt, _ptr(workspace),
+        int(mask), int(window), _slopes_ptr(bias_slopes, hq), dt, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream))
     if st != 0:
         raise AttnError("attn_fwd", st)
@@ -173,11 +185,12 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
 def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         max_seqlen_k: int, mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
         dq=None, dk=None, dv=None, workspace=None, stream=None,
-        o_f32: Optional[torch.Tensor] = None, window: int = 0):
+        o_f32: Optional[torch.Tensor] = None, window: int = 0,
+        bias_slopes: Optional[torch.Tensor] = None):
     """Attention backward; returns (dq, dk, dv) with dk/dv summed over each
     KV head's group of query heads.  Pass the forward's ``o_f32`` when it was
     kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding; pass the
-    forward's mask and ``window``."""
+    forward's mask, ``window`` and ``bias_slopes``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n, 3)
     _check(lse, "lse", 2)
@@ -198,7 +211,8 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_f32), _ptr(dout), _ptr(dq),
         _ptr(dk), _ptr(dv),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, max_seqlen_q, max_seqlen_k, total_q,
-        total_k, hq, hkv, d, float(scale), int(mask), int(window), dt, _ptr(workspace),
+        total_k, hq, hkv, d, float(scale), int(mask), int(window),
+        _slopes_ptr(bias_slopes, hq), dt, _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream))
     if st != 0:
         raise AttnError("attn_bwd", st)

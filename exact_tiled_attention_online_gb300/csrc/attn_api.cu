@@ -110,7 +110,7 @@ using namespace attn;
 
 extern "C" {
 
-int attn_version(void) { return 110; }
+int attn_version(void) { return 120; }
 
 const char *attn_status_string(attn_status s) {
   switch (s) {
@@ -145,8 +145,8 @@ size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      float *o_f32, const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
-                     attn_mask_kind mask, int window, attn_dtype dtype, void *workspace,
-                     size_t workspace_bytes, void *stream) {
+                     attn_mask_kind mask, int window, const float *bias_slopes,
+                     attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
   attn_status st =
       check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
@@ -162,6 +162,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
   p.window = window;
+  p.slopes = bias_slopes;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   if (batch == 0 || total_q == 0 || max_q == 0) {
@@ -222,8 +223,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const float *lse, const float *o_f32, const void *dout, void *dq, void *dk, void *dv,
                      const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
-                     attn_mask_kind mask, int window, attn_dtype dtype, void *workspace,
-                     size_t workspace_bytes, void *stream) {
+                     attn_mask_kind mask, int window, const float *bias_slopes,
+                     attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
   attn_status st =
       check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
@@ -243,6 +244,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
   p.window = window;
+  p.slopes = bias_slopes;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   char *ws = static_cast<char *>(workspace);

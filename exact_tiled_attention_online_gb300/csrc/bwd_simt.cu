@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   const float D_i = p.delta[(size_t)h * p.total_q + t];
   const int kbeg = key_begin(g.mask, g.window, i, g.nq, g.nk);
   const int kend = key_end(g.mask, i, g.nq, g.nk);
+  const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
+  const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
   const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const size_t stride = (size_t)p.hkv * D;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
       ps += qf[e] * kf[e];
       pd += dof[e] * Elem<T>::to_f(vb[j * stride + e]);
     }
-    const float sc = warp_sum(ps), dpij = warp_sum(pd);
+    const float sc = warp_sum(ps) + pos_bias2(slope2, bound, j), dpij = warp_sum(pd);
     const float pij = fast_exp2(sc - lse2);
     const float ds = pij * (dpij - D_i);
 #pragma unroll
@@ -139,7 +141,9 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
   }
   const int i_begin = row_begin(g.mask, j, g.nq, g.nk);
   const int i_end = row_end(g.mask, g.window, j, g.nq, g.nk);
+  const int off = causal_offset(g.mask, g.nq, g.nk);
   for (int h = hk * grp; h < hk * grp + grp; h++) {
+    const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
     for (int i = i_begin; i < i_end; i++) {
       const int t = g.q0 + i;
       const size_t row = (size_t)t * p.hq + h;
@@ -153,7 +157,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
         ps += qf[e] * kf[e];
         pd += dof[e] * vf[e];
       }
-      const float sc = warp_sum(ps), dpij = warp_sum(pd);
+      const float sc = warp_sum(ps) + pos_bias2(slope2, (float)(i + off), j),
+                  dpij = warp_sum(pd);
       const float lse2 = p.lse2[(size_t)h * p.total_q + t];
       const float D_i = p.delta[(size_t)h * p.total_q + t];
       const float pij = fast_exp2(sc - lse2);

@@ -96,7 +96,8 @@ struct BarsA {
   Sync sync;
 };
 
-template <int D>
+// kBias: add the linear positional bias to the recomputed logits.
+template <int D, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -291,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c_lo = rb - i0, c_hi = re - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
       const bool full = c_lo <= 0 && c_hi >= kRowsA;
       const uint64_t c2x2 = f2(c2, c2);
+      // positional bias of row i0 + c: -slope2 |i0 + c + off - j|
+      const float slope2 = kBias ? __ldg(p.slopes + it_head(it)) * kLog2e : 0.f;
+      const float bdist0 = (float)(j - i0 - causal_offset(g.mask, g.nq, g.nk));
       uint32_t pp[16], dd[16];
       {
         const int cc = half;  // this warp's 32 rows of the step
@@ -302,8 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           const int c0 = cc * 32 + e;
           // two lanes per instruction: x = c S - lse2, P = 2^x, dS = P (dP - D)
-          const float2 nl = *reinterpret_cast<const float2 *>(nlse2 + c0);
+          float2 nl = *reinterpret_cast<const float2 *>(nlse2 + c0);
           const float2 ndd = *reinterpret_cast<const float2 *>(nd + c0);
+          if constexpr (kBias) {
+            nl.x += pos_bias2(slope2, bdist0, c0);
+            nl.y += pos_bias2(slope2, bdist0, c0 + 1);
+          }
           float x0, x1;
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, f2(nl.x, nl.y)),
                    x0, x1);
@@ -400,7 +408,7 @@ struct BarsB {
   Sync sync;
 };
 
-template <int D>
+template <int D, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -561,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
     const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
     const uint64_t c2x2 = f2(c2, c2), nl2 = f2(-lse2, -lse2), nd2 = f2(-D_i, -D_i);
+    const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
+    const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int st = jj & 1;
@@ -585,8 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int c = cc * 32 + e;
+          uint64_t add2 = nl2;
+          if constexpr (kBias)
+            add2 = f2(pos_bias2(slope2, bound - (float)jb, c) - lse2,
+                      pos_bias2(slope2, bound - (float)jb, c + 1) - lse2);
           float x0, x1;
-          f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, nl2), x0, x1);
+          f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, add2), x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           if (boundary) {
             if (jb + c >= row_limit || jb + c < row_first) p0 = 0.f;
@@ -655,7 +669,7 @@ cudaError_t set_smem(K kernel, int bytes, bool *configured) {
   return cudaSuccess;
 }
 
-template <int D>
+template <int D, bool kBias>
 cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
   const BwdParams &p = a.p;
   // Every tensor-core product of the backward runs on the fp16 copies.
@@ -669,17 +683,17 @@ cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
       !make_map(&mv, p.v16, D, p.hkv, p.total_k, 1, kTileKeys, f16))
     return cudaErrorInvalidValue;
   static bool conf_a[64] = {false}, conf_b[64] = {false};
-  cudaError_t e = set_smem(bwd_dkdv_tc_kernel<D>, LayoutA<D>::kAlloc, conf_a);
+  cudaError_t e = set_smem(bwd_dkdv_tc_kernel<D, kBias>, LayoutA<D>::kAlloc, conf_a);
   if (e != cudaSuccess) return e;
-  e = set_smem(bwd_dq_tc_kernel<D>, LayoutB<D>::kAlloc, conf_b);
+  e = set_smem(bwd_dq_tc_kernel<D, kBias>, LayoutB<D>::kAlloc, conf_b);
   if (e != cudaSuccess) return e;
   const long long ga = (long long)a.n_key_tiles * p.hkv * p.batch;
   const long long gb = (long long)a.n_row_tiles * p.hq * p.batch;
   if (ga >= (1LL << 31) || gb >= (1LL << 31)) return cudaErrorInvalidValue;
-  bwd_dkdv_tc_kernel<D><<<(unsigned)ga, kThreads, LayoutA<D>::kAlloc, st>>>(q64, do64, mk, mv, a);
+  bwd_dkdv_tc_kernel<D, kBias><<<(unsigned)ga, kThreads, LayoutA<D>::kAlloc, st>>>(q64, do64, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<D><<<(unsigned)gb, kThreads, LayoutB<D>::kAlloc, st>>>(q128, do128, mk, mv, a);
+  bwd_dq_tc_kernel<D, kBias><<<(unsigned)gb, kThreads, LayoutB<D>::kAlloc, st>>>(q128, do128, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -696,8 +710,8 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_
            p.d, p.d, (long long)a.n_key_tiles * p.hkv * p.batch,
            (long long)a.n_row_tiles * p.hq * p.batch);
   if (a.n_key_tiles == 0 || a.n_row_tiles == 0) return cudaSuccess;
-  if (p.d == 64) return launch_d<64>(a, st);
-  return launch_d<128>(a, st);
+  if (p.slopes) return p.d == 64 ? launch_d<64, true>(a, st) : launch_d<128, true>(a, st);
+  return p.d == 64 ? launch_d<64, false>(a, st) : launch_d<128, false>(a, st);
 }
 
 }  // namespace attn

@@ -160,6 +160,14 @@ __host__ __device__ __forceinline__ int key_row_end(int mask, int window, int j,
   return j < nk ? row_end(mask, window, j, nq, nk) : 0;
 }
 
+// Linear positional bias in log2 units for in-sequence row i and key j:
+// -slope2 * |i + off - j|, the distance from the row's causal bound (0 for the
+// key at the bound), with slope2 = slope * log2(e).  `dist0` is i + off minus
+// the tile's first key, so key e of the tile is dist0 - e away.
+__device__ __forceinline__ float pos_bias2(float slope2, float dist0, int e) {
+  return -slope2 * fabsf(dist0 - (float)e);
+}
+
 // ---------------------------------------------------------------------------
 // Device error flag: the first error code sticks until the host clears it.
 // ---------------------------------------------------------------------------
@@ -202,7 +210,8 @@ struct FwdParams {
   int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
   float scale, scale_log2;  // scale and scale * log2(e)
   int mask;
-  int window;  // > 0: bounded window (causal kinds only)
+  int window;             // > 0: bounded window (causal kinds only)
+  const float *slopes;    // [hq] linear positional bias slopes, or NULL
   int *err;
   // split-KV partial outputs (NULL when the plan writes o/lse directly)
   float *o_part, *lse_part;
@@ -218,7 +227,8 @@ struct BwdParams {
   int batch, max_q, max_k, total_q, total_k, hq, hkv, d;
   float scale, scale_log2;
   int mask;
-  int window;  // > 0: bounded window (causal kinds only)
+  int window;             // > 0: bounded window (causal kinds only)
+  const float *slopes;    // [hq] linear positional bias slopes, or NULL
   int *err;
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i
   float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)

@@ -35,6 +35,9 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   }
   const int kbeg = key_begin(g.mask, g.window, i, g.nq, g.nk);
   const int kend = key_end(g.mask, i, g.nq, g.nk);
+  // positional bias: key j is |bound - j| away from the row's causal bound
+  const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
+  const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
   float m = -INFINITY, l = 0.f;
   const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
@@ -43,7 +46,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * stride + e]);
-    const float sc = warp_sum(part);  // scaled logit in log2 units
+    const float sc = warp_sum(part) + pos_bias2(slope2, bound, j);  // logit in log2 units
     const float m_new = fmaxf(m, sc);
     const float alpha = fast_exp2(m - m_new);
     const float pj = fast_exp2(sc - m_new);

@@ -49,7 +49,7 @@ extern "C" attn_status attn_fwd_static_scratch(
     const void *q, const void *k, const void *v, void *o, float *lse, float *o_f32,
     const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
     int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask, int window,
-    attn_dtype dtype, void *stream) {
+    const float *bias_slopes, attn_dtype dtype, void *stream) {
   attn_status st = internal_check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask,
                                         window, dtype);
   if (st != ATTN_OK) return st;
@@ -58,7 +58,7 @@ extern "C" attn_status attn_fwd_static_scratch(
   if (plan.kind != PLAN_TC_SPLIT || total_k == 0) {
     // Nothing to keep in scratch: the workspace-free attn_fwd path.
     return attn_fwd(q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q, total_k,
-                    hq, hkv, d, scale, mask, window, dtype, nullptr, 0, stream);
+                    hq, hkv, d, scale, mask, window, bias_slopes, dtype, nullptr, 0, stream);
   }
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (!cu_q || !cu_k || !q || !o || !k || !v) return ATTN_ERR_INVALID_ARG;
@@ -79,6 +79,7 @@ extern "C" attn_status attn_fwd_static_scratch(
   p.hq = hq; p.hkv = hkv; p.d = d; p.scale = scale; p.scale_log2 = scale * kLog2e;
   p.mask = mask;
   p.window = window;
+  p.slopes = bias_slopes;
   p.err = err;
   // Same carving as the caller-provided workspace of attn_fwd: partial
   // outputs first, partial logsumexps after them.

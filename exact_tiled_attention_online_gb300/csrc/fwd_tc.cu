@@ -100,7 +100,7 @@ __device__ __forceinline__ void row_map(const TcArgs &a, int head_idx, int i0, i
 
 // kPosScale: scale > 0, so the max of the raw scores gives the max of the
 // logits (the common case); otherwise the scores are scaled before the max.
-template <int D, bool kPosScale>
+template <int D, bool kPosScale, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const TcArgs a) {
@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
+    static_assert(!(kBias && kPosScale), "the bias needs the logits before the max");
+    const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
+    const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
@@ -284,12 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kTileKeys; c++) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(raw[c]));
         mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;
-      } else {  // scale <= 0: scale first, keep masked lanes at -inf
+      } else {  // scale <= 0 or a bias: logits first, keep masked lanes at -inf
         mt = -INFINITY;
+        const float dist0 = bound - (float)(n * kTileKeys);
 #pragma unroll
         for (int c = 0; c < kTileKeys; c++) {
           const float x = __uint_as_float(raw[c]);
-          const float y = x == -INFINITY ? -INFINITY : x * c2;
+          float z = x * c2;
+          if constexpr (kBias) z += pos_bias2(slope2, dist0, c);
+          const float y = x == -INFINITY ? -INFINITY : z;
           raw[c] = __float_as_uint(y);
           mt = fmaxf(mt, y);
         }
@@ -439,20 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kPos>
+template <int D, bool kPos, bool kBias>
 cudaError_t launch_d(const TcArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
                      const CUtensorMap &mv, dim3 grid, cudaStream_t st) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, kPos>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, kPos, kBias>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc_kernel<D, kPos><<<grid, kThreads, Layout<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc_kernel<D, kPos, kBias><<<grid, kThreads, Layout<D>::kAlloc, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -481,10 +487,13 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
            plan.pack ? "_packgqa" : "", ctas, plan.tile_tokens, plan.n_splits,
            plan.n_splits > 1 ? " +combine" : "");
   const bool pos = p.scale_log2 > 0.f;
-  if (p.d == 64) return pos ? launch_d<64, true>(a, mq, mk, mv, grid, st)
-                            : launch_d<64, false>(a, mq, mk, mv, grid, st);
-  return pos ? launch_d<128, true>(a, mq, mk, mv, grid, st)
-             : launch_d<128, false>(a, mq, mk, mv, grid, st);
+  if (p.slopes)  // the bias goes into the logits before the max
+    return p.d == 64 ? launch_d<64, false, true>(a, mq, mk, mv, grid, st)
+                     : launch_d<128, false, true>(a, mq, mk, mv, grid, st);
+  if (p.d == 64) return pos ? launch_d<64, true, false>(a, mq, mk, mv, grid, st)
+                            : launch_d<64, false, false>(a, mq, mk, mv, grid, st);
+  return pos ? launch_d<128, true, false>(a, mq, mk, mv, grid, st)
+             : launch_d<128, false, false>(a, mq, mk, mv, grid, st);
 }
 
 }  // namespace attn

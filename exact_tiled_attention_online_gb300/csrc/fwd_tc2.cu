@@ -84,8 +84,9 @@ __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, 
 // logits).  kRoundedSum: also sum the bf16-rounded probabilities so the fp32
 // output is an exact convex combination of V rows (wanted when the caller
 // keeps that output for the backward); without it O is normalised by the
-// fp32 sum.
-template <int D, bool kPosScale, bool kRoundedSum>
+// fp32 sum.  kBias: add the linear positional bias (with kPosScale false:
+// the bias must be in the logits before the max).
+template <int D, bool kPosScale, bool kRoundedSum, bool kBias>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
@@ -279,6 +280,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t o_col = t_lane + 256u + (uint32_t)(x * D);
     const float c2 = p.scale_log2;
     const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
+    static_assert(!(kBias && kPosScale), "the bias needs the logits before the max");
+    const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
+    const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
     for (int it = 0; it < n_mine; it++) {
@@ -305,10 +309,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
           if ((unsigned)(e - first) >= span) v[e] = 0xff800000u;
       }
       if constexpr (!kPosScale) {
+        const float dist0 = bound - (float)(n * kTileKeys);
 #pragma unroll
         for (int e = 0; e < kTileKeys; e++) {
           const float y = __uint_as_float(v[e]);
-          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : y * c2);
+          float z = y * c2;
+          if constexpr (kBias) z += pos_bias2(slope2, dist0, e);
+          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : z);
         }
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -422,20 +429,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-template <int D, bool kPos, bool kRs>
+template <int D, bool kPos, bool kRs, bool kBias>
 cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                     const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs, kBias>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout2<D>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc2_kernel<D, kPos, kRs><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc2_kernel<D, kPos, kRs, kBias><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -443,10 +450,12 @@ template <int D>
 cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                       const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
   const bool pos = a.p.scale_log2 > 0.f, rs = a.p.o_f32 != nullptr;
-  if (pos) return rs ? launch2<D, true, true>(a, mq, mk, mv, ctas, st)
-                     : launch2<D, true, false>(a, mq, mk, mv, ctas, st);
-  return rs ? launch2<D, false, true>(a, mq, mk, mv, ctas, st)
-            : launch2<D, false, false>(a, mq, mk, mv, ctas, st);
+  if (a.p.slopes) return rs ? launch2<D, false, true, true>(a, mq, mk, mv, ctas, st)
+                            : launch2<D, false, false, true>(a, mq, mk, mv, ctas, st);
+  if (pos) return rs ? launch2<D, true, true, false>(a, mq, mk, mv, ctas, st)
+                     : launch2<D, true, false, false>(a, mq, mk, mv, ctas, st);
+  return rs ? launch2<D, false, true, false>(a, mq, mk, mv, ctas, st)
+            : launch2<D, false, false, false>(a, mq, mk, mv, ctas, st);
 }
 
 }  // namespace

@@ -45,6 +45,7 @@ class Workload:
     backward: bool = False
     v_shift_per_seq: float = 0.0
     window: int = 0  # > 0: bounded causal window of that many keys per row
+    bias: bool = False  # linear positional bias with slopes bias_slopes(hq)
 
     @property
     def batch(self) -> int:
@@ -93,7 +94,17 @@ WORKLOADS = {
     # the prefill shape under a bounded causal window (linear pair work)
     "window_prefill": Workload("window_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
                                128, "bf16", MASK_TOP_LEFT, 1002, window=1024),
+    # the prefill shape with a linear positional bias on every logit
+    "bias_prefill": Workload("bias_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
+                             128, "bf16", MASK_TOP_LEFT, 1002, bias=True),
 }
+
+
+def bias_slopes(hq: int) -> torch.Tensor:
+    """Slopes of the positional-bias workloads: head h gets 2^(-8 (h + 1) / hq),
+    a geometric sequence from steep to nearly flat (a stated choice; the pages
+    fix no slopes)."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / hq) for h in range(hq)], dtype=torch.float32)
 
 
 def cu_seqlens(lengths: Sequence[int]) -> torch.Tensor:

@@ -38,6 +38,14 @@
  * the sequence length ("attention-algorithm-error-and-complexity-tests",
  * fifth paragraph).  W > 0 needs a causal kind; a negative W, or W > 0 with
  * ATTN_MASK_NONE, is ATTN_ERR_INVALID_ARG.
+ * bias_slopes (every call that takes a mask): NULL for none, or a device
+ * array of n_heads_q finite fp32 slopes m_h that add the linear positional
+ * bias  -m_h * |i + off - j|  to every allowed logit of query head h, where
+ * off = Nk - Nq for ATTN_CAUSAL_BOTTOM_RIGHT and 0 otherwise: the distance of
+ * key j from the row's causal bound.  It follows the in-sequence positions
+ * (so it is the same for a sequence packed anywhere) and the backward
+ * rebuilds it from the same positions ("causal-mask-and-ragged-sequence-
+ * layouts", sixth paragraph).
  * Pairs from different sequences are never allowed; tile lanes past a
  * sequence's end never enter the max, the denominator or a gradient sum
  * (same page, second paragraph).  A row with no allowed key gets O = 0 and
@@ -123,8 +131,9 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
                      const int32_t *cu_seqlens_k, int batch, int max_seqlen_q,
                      int max_seqlen_k, int total_q, int total_k, int n_heads_q,
                      int n_heads_kv, int head_dim, float scale,
-                     attn_mask_kind mask, int window, attn_dtype dtype,
-                     void *workspace, size_t workspace_bytes, void *stream);
+                     attn_mask_kind mask, int window, const float *bias_slopes,
+                     attn_dtype dtype, void *workspace, size_t workspace_bytes,
+                     void *stream);
 
 /*
  * Workspace bytes attn_bwd needs: the per-row terms D_i = dO_i . O_i and the
@@ -140,7 +149,7 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
 
 /*
  * Backward at upstream gradient dout, recomputing the probabilities from q, k
- * and the saved lse with the same mask rule and window as the forward
+ * and the saved lse with the same mask rule, window and bias as the forward
  * ("causal-mask-and-ragged-sequence-layouts", sixth paragraph):
  *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - dO_i . O_i),
  *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
@@ -163,8 +172,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
                      int batch, int max_seqlen_q, int max_seqlen_k,
                      int total_q, int total_k, int n_heads_q, int n_heads_kv,
                      int head_dim, float scale, attn_mask_kind mask,
-                     int window, attn_dtype dtype, void *workspace,
-                     size_t workspace_bytes, void *stream);
+                     int window, const float *bias_slopes, attn_dtype dtype,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Mask probe (diagnostic): writes, for one query head, the packed allowed-pair
@@ -224,7 +233,8 @@ attn_status attn_fwd_static_scratch(const void *q, const void *k, const void *v,
                                     int total_q, int total_k, int n_heads_q,
                                     int n_heads_kv, int head_dim, float scale,
                                     attn_mask_kind mask, int window,
-                                    attn_dtype dtype, void *stream);
+                                    const float *bias_slopes, attn_dtype dtype,
+                                    void *stream);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status status);

@@ -39,7 +39,7 @@ def test_version_and_strings(lib):
 
 def _fwd(lib, **over):
     args = dict(q=1, k=1, v=1, o=1, lse=1, o_f32=None, cu_q=1, cu_k=1, batch=1, max_q=4, max_k=4,
-                total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, window=0, dtype=0,
+                total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, window=0, slopes=None, dtype=0,
                 ws=None, ws_bytes=0, stream=None)
     args.update(over)
     return lib.attn_fwd(*args.values())
@@ -81,13 +81,13 @@ def test_bwd_workspace_covers_rows_and_fp16_copies(lib):
 
 def test_bwd_rejects_missing_workspace(lib):
     st = lib.attn_bwd(1, 1, 1, 1, 1, None, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.1, 1, 0,
-                      0, None, 0, None)
+                      None, 0, None, 0, None)
     assert st == 3
 
 
 def test_bwd_rejects_window_without_causal_rule(lib):
     st = lib.attn_bwd(1, 1, 1, 1, 1, None, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.1, 0, 5,
-                      0, None, 0, None)
+                      None, 0, None, 0, None)
     assert st == 1
 
 

@@ -30,7 +30,7 @@ def _entry():
     lib = attn.library()
     f = lib.attn_fwd_static_scratch
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    f.argtypes = [P] * 8 + [I] * 8 + [F, I, I, I, P]
+    f.argtypes = [P] * 8 + [I] * 8 + [F, I, I, P, I, P]
     f.restype = I
     return f
 
@@ -40,7 +40,7 @@ def _call_static(x, w, o, lse, o32):
     return f(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
              lse.data_ptr(), o32.data_ptr(), x["cu_seqlens_q"].data_ptr(),
              x["cu_seqlens_k"].data_ptr(), w.batch, w.max_q, w.max_k, w.total_q, w.total_k,
-             w.hq, w.hkv, w.d, w.scale, w.mask, w.window, attn.DTYPE_BF16,
+             w.hq, w.hkv, w.d, w.scale, w.mask, w.window, None, attn.DTYPE_BF16,
              torch.cuda.current_stream().cuda_stream)
 
 

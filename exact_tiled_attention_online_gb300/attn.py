@@ -27,9 +27,14 @@ DTYPE_FP32 = 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
           4: "CUDA error", 5: "device wait timed out", 6: "cu_seqlens out of bounds"}
 
-_SYMBOLS = ["attn_fwd", "attn_bwd", "attn_fwd_workspace_size", "attn_bwd_workspace_size",
+_SYMBOLS = ["attn_fwd", "attn_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_workspace_size", "attn_bwd_workspace_size",
             "attn_mask_probe", "attn_get_device_error", "attn_status_string",
             "attn_last_plan", "attn_version"]
+
+
+class AttnStrides(ctypes.Structure):
+    """``attn_strides``: {token stride, head stride} in elements per tensor."""
+    _fields_ = [(n, ctypes.c_int64 * 2) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")]
 
 
 class AttnError(RuntimeError):
@@ -60,6 +65,10 @@ def library() -> ctypes.CDLL:
     L.attn_fwd.restype = I
     L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, P, I, P, SZ, P]
     L.attn_bwd.restype = I
+    L.attn_fwd_ex.argtypes = [ctypes.POINTER(AttnStrides)] + L.attn_fwd.argtypes
+    L.attn_fwd_ex.restype = I
+    L.attn_bwd_ex.argtypes = [ctypes.POINTER(AttnStrides)] + L.attn_bwd.argtypes
+    L.attn_bwd_ex.restype = I
     L.attn_fwd_workspace_size.argtypes = [I] * 9
     L.attn_fwd_workspace_size.restype = SZ
     L.attn_bwd_workspace_size.argtypes = [I] * 9
@@ -86,13 +95,27 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32 expected")
 
 
-def _check(t: torch.Tensor, name: str, dims: int):
+def _check(t: torch.Tensor, name: str, dims: int, strided: bool = False):
+    """``strided``: a [tokens, heads, d] tensor whose features are contiguous
+    and whose token and head strides the library takes as they are."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dim() != dims:
         raise ValueError(f"{name} must have {dims} dimensions")
-    if not t.is_contiguous():
+    if strided:
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name}: the last dimension must be contiguous")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _strides(**tensors) -> AttnStrides:
+    s = AttnStrides()
+    for name, t in tensors.items():
+        if t is not None:
+            getattr(s, name)[0] = t.stride(0)
+            getattr(s, name)[1] = t.stride(1)
+    return s
 
 
 def _stream(stream) -> int:
@@ -148,7 +171,7 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
     ``want_lse`` is False and no ``lse`` buffer is given); o_f32 is the fp32
     output before rounding, which ``bwd`` uses for the D term.
     """
-    _check(q, "q", 3), _check(k, "k", 3), _check(v, "v", 3)
+    _check(q, "q", 3, True), _check(k, "k", 3, True), _check(v, "v", 3, True)
     _check(cu_seqlens_q, "cu_seqlens_q", 1), _check(cu_seqlens_k, "cu_seqlens_k", 1)
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
@@ -161,7 +184,8 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    _check(out, "out", 3, True)
     if lse is None and want_lse:
         lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
     ret_f32 = want_o_f32 or o_f32 is not None
@@ -171,7 +195,9 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
                                   window)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    st = library().attn_fwd(
+    strides = _strides(q=q, k=k, v=v, o=out)
+    st = library().attn_fwd_ex(
+        ctypes.byref(strides),
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(o_f32), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k),
         batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv, d, float(scale),
@@ -192,7 +218,7 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding; pass the
     forward's mask, ``window`` and ``bias_slopes``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
-        _check(t, n, 3)
+        _check(t, n, 3, True)
     _check(lse, "lse", 2)
     dt = _dtype_code(q)
     total_q, hq, d = q.shape
@@ -200,14 +226,18 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     batch = cu_seqlens_q.numel() - 1
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty(q.shape, dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, device=v.device) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, 3, True)
     ws_bytes = bwd_workspace_size(batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv,
                                   d, dt)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    st = library().attn_bwd(
+    strides = _strides(q=q, k=k, v=v, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
+    st = library().attn_bwd_ex(
+        ctypes.byref(strides),
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_f32), _ptr(dout), _ptr(dq),
         _ptr(dk), _ptr(dv),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, max_seqlen_q, max_seqlen_k, total_q,

@@ -19,6 +19,8 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
                           char *desc, size_t desc_len);
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
 cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
+cudaError_t launch_zero_rows(void *base, int T, int H, int d, Strides s, int elem,
+                             cudaStream_t st);
 cudaError_t launch_mask_probe(const int32_t *cu_q, const int32_t *cu_k, int batch, int max_q,
                               int max_k, int total_q, int total_k, int mask, int window,
                               int tile_rows, uint8_t *out, int *err, cudaStream_t st);
@@ -60,6 +62,19 @@ static attn_status check_sizes(int batch, int max_q, int max_k, int total_q, int
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (max_q > total_q || max_k > total_k) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
+}
+
+// The layout of one tensor: the caller's strides, or contiguous THD.  false
+// for a stride that is not positive or not a multiple of 16 bytes.
+static bool pick_strides(const int64_t *given, int heads, int d, int elem, Strides *out) {
+  if (!given) {
+    out->ts = (long long)heads * d;
+    out->hs = d;
+    return true;
+  }
+  out->ts = given[0];
+  out->hs = given[1];
+  return out->ts > 0 && out->hs > 0 && (out->ts * elem) % 16 == 0 && (out->hs * elem) % 16 == 0;
 }
 
 static int sm_count() {
@@ -147,6 +162,17 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
                      attn_mask_kind mask, int window, const float *bias_slopes,
                      attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  return attn_fwd_ex(nullptr, q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q,
+                     total_k, hq, hkv, d, scale, mask, window, bias_slopes, dtype, workspace,
+                     workspace_bytes, stream);
+}
+
+attn_status attn_fwd_ex(const attn_strides *strides, const void *q, const void *k,
+                        const void *v, void *o, float *lse, float *o_f32, const int32_t *cu_q,
+                        const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
+                        int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask,
+                        int window, const float *bias_slopes, attn_dtype dtype,
+                        void *workspace, size_t workspace_bytes, void *stream) {
   attn_status st =
       check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
@@ -163,6 +189,12 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
   p.mask = mask;
   p.window = window;
   p.slopes = bias_slopes;
+  const int elem = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+  if (!pick_strides(strides ? strides->q : nullptr, hq, d, elem, &p.sq) ||
+      !pick_strides(strides ? strides->k : nullptr, hkv, d, elem, &p.sk) ||
+      !pick_strides(strides ? strides->v : nullptr, hkv, d, elem, &p.sv) ||
+      !pick_strides(strides ? strides->o : nullptr, hq, d, elem, &p.so))
+    return ATTN_ERR_INVALID_ARG;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   if (batch == 0 || total_q == 0 || max_q == 0) {
@@ -225,6 +257,18 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
                      attn_mask_kind mask, int window, const float *bias_slopes,
                      attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  return attn_bwd_ex(nullptr, q, k, v, o, lse, o_f32, dout, dq, dk, dv, cu_q, cu_k, batch, max_q,
+                     max_k, total_q, total_k, hq, hkv, d, scale, mask, window, bias_slopes, dtype,
+                     workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *k,
+                        const void *v, const void *o, const float *lse, const float *o_f32,
+                        const void *dout, void *dq, void *dk, void *dv, const int32_t *cu_q,
+                        const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
+                        int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask,
+                        int window, const float *bias_slopes, attn_dtype dtype,
+                        void *workspace, size_t workspace_bytes, void *stream) {
   attn_status st =
       check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
   if (st != ATTN_OK) return st;
@@ -245,6 +289,20 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   p.mask = mask;
   p.window = window;
   p.slopes = bias_slopes;
+  const int elem = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
+  if (!pick_strides(strides ? strides->q : nullptr, hq, d, elem, &p.sq) ||
+      !pick_strides(strides ? strides->k : nullptr, hkv, d, elem, &p.sk) ||
+      !pick_strides(strides ? strides->v : nullptr, hkv, d, elem, &p.sv) ||
+      !pick_strides(strides ? strides->o : nullptr, hq, d, elem, &p.so) ||
+      !pick_strides(strides ? strides->dout : nullptr, hq, d, elem, &p.sdo) ||
+      !pick_strides(strides ? strides->dq : nullptr, hq, d, elem, &p.sdq) ||
+      !pick_strides(strides ? strides->dk : nullptr, hkv, d, elem, &p.sdk) ||
+      !pick_strides(strides ? strides->dv : nullptr, hkv, d, elem, &p.sdv))
+    return ATTN_ERR_INVALID_ARG;
+  // the gradients are zeroed and written 16 bytes at a time
+  if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+       reinterpret_cast<uintptr_t>(dv)) & 15)
+    return ATTN_ERR_INVALID_ARG;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
   char *ws = static_cast<char *>(workspace);
@@ -259,10 +317,9 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
   // max_k are covered by the kernels; a zero fill first keeps dk/dv defined
   // even when the device flags inconsistent cu_seqlens.
   cudaError_t ce = cudaSuccess;
-  if (total_k > 0) {
-    size_t es = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
-    ce = cudaMemsetAsync(dk, 0, (size_t)total_k * hkv * d * es, cs);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(dv, 0, (size_t)total_k * hkv * d * es, cs);
+  if (total_k > 0) {  // every (token, head) row of dk and dv, whatever the strides
+    ce = launch_zero_rows(dk, total_k, hkv, d, p.sdk, elem, cs);
+    if (ce == cudaSuccess) ce = launch_zero_rows(dv, total_k, hkv, d, p.sdv, elem, cs);
   }
   char desc[256];
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |

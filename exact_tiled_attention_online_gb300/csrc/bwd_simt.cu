@@ -25,8 +25,8 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
   const long long row = (long long)blockIdx.x * 4 + warp;  // t * hq + h
   if (row >= (long long)p.total_q * p.hq) return;
   const int t = (int)(row / p.hq), h = (int)(row % p.hq);
-  const T *op = reinterpret_cast<const T *>(p.o) + (size_t)row * D + lane * E;
-  const T *dp = reinterpret_cast<const T *>(p.dout) + (size_t)row * D + lane * E;
+  const T *op = reinterpret_cast<const T *>(p.o) + toff(p.so, t, h) + lane * E;
+  const T *dp = reinterpret_cast<const T *>(p.dout) + toff(p.sdo, t, h) + lane * E;
   float part = 0.f;
   if (p.o_f32) {
     const float *of = p.o_f32 + (size_t)row * D + lane * E;
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
   if (p.q16) {
     // fp16 copies for the tensor-core backward; bf16 -> fp16 is exact inside
     // the fp16 normal range, larger magnitudes are reported.
-    const T *qp = reinterpret_cast<const T *>(p.q) + (size_t)row * D + lane * E;
+    const T *qp = reinterpret_cast<const T *>(p.q) + toff(p.sq, t, h) + lane * E;
     __half *q16 = reinterpret_cast<__half *>(p.q16) + (size_t)row * D + lane * E;
     __half *d16 = reinterpret_cast<__half *>(p.do16) + (size_t)row * D + lane * E;
     bool bad = false;
@@ -76,9 +76,8 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   if (i >= g.nq) return;
   const int hk = h / (p.hq / p.hkv);
   const int t = g.q0 + i;
-  const size_t row = (size_t)t * p.hq + h;
-  const T *qp = reinterpret_cast<const T *>(p.q) + row * D + lane * E;
-  const T *dop = reinterpret_cast<const T *>(p.dout) + row * D + lane * E;
+  const T *qp = reinterpret_cast<const T *>(p.q) + toff(p.sq, t, h) + lane * E;
+  const T *dop = reinterpret_cast<const T *>(p.dout) + toff(p.sdo, t, h) + lane * E;
   float qf[E], dof[E], dq[E];
 #pragma unroll
   for (int e = 0; e < E; e++) {
@@ -92,16 +91,16 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   const int kend = key_end(g.mask, i, g.nq, g.nk);
   const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
   const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
-  const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
-  const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
-  const size_t stride = (size_t)p.hkv * D;
+  const T *kb = reinterpret_cast<const T *>(p.k) + toff(p.sk, g.k0, hk) + lane * E;
+  const T *vb = reinterpret_cast<const T *>(p.v) + toff(p.sv, g.k0, hk) + lane * E;
+  const size_t kstride = (size_t)p.sk.ts, vstride = (size_t)p.sv.ts;  // one key to the next
   for (int j = kbeg; j < kend; j++) {
     float kf[E], ps = 0.f, pd = 0.f;
 #pragma unroll
     for (int e = 0; e < E; e++) {
-      kf[e] = Elem<T>::to_f(kb[j * stride + e]);
+      kf[e] = Elem<T>::to_f(kb[j * kstride + e]);
       ps += qf[e] * kf[e];
-      pd += dof[e] * Elem<T>::to_f(vb[j * stride + e]);
+      pd += dof[e] * Elem<T>::to_f(vb[j * vstride + e]);
     }
     const float sc = warp_sum(ps) + pos_bias2(slope2, bound, j), dpij = warp_sum(pd);
     const float pij = fast_exp2(sc - lse2);
@@ -109,7 +108,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
 #pragma unroll
     for (int e = 0; e < E; e++) dq[e] += ds * kf[e];
   }
-  T *out = reinterpret_cast<T *>(p.dq) + row * D + lane * E;
+  T *out = reinterpret_cast<T *>(p.dq) + toff(p.sdq, t, h) + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e++) out[e] = Elem<T>::from_f(dq[e] * p.scale);
 }
@@ -128,9 +127,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
   }
   if (j >= g.nk) return;
   const int grp = p.hq / p.hkv;
-  const size_t krow = ((size_t)(g.k0 + j)) * p.hkv + hk;
-  const T *kp = reinterpret_cast<const T *>(p.k) + krow * D + lane * E;
-  const T *vp = reinterpret_cast<const T *>(p.v) + krow * D + lane * E;
+  const T *kp = reinterpret_cast<const T *>(p.k) + toff(p.sk, g.k0 + j, hk) + lane * E;
+  const T *vp = reinterpret_cast<const T *>(p.v) + toff(p.sv, g.k0 + j, hk) + lane * E;
   float kf[E], vf[E], dk[E], dv[E];
 #pragma unroll
   for (int e = 0; e < E; e++) {
@@ -146,9 +144,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
     const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
     for (int i = i_begin; i < i_end; i++) {
       const int t = g.q0 + i;
-      const size_t row = (size_t)t * p.hq + h;
-      const T *qp = reinterpret_cast<const T *>(p.q) + row * D + lane * E;
-      const T *dop = reinterpret_cast<const T *>(p.dout) + row * D + lane * E;
+      const T *qp = reinterpret_cast<const T *>(p.q) + toff(p.sq, t, h) + lane * E;
+      const T *dop = reinterpret_cast<const T *>(p.dout) + toff(p.sdo, t, h) + lane * E;
       float qf[E], dof[E], ps = 0.f, pd = 0.f;
 #pragma unroll
       for (int e = 0; e < E; e++) {
@@ -170,8 +167,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
       }
     }
   }
-  T *dkp = reinterpret_cast<T *>(p.dk) + krow * D + lane * E;
-  T *dvp = reinterpret_cast<T *>(p.dv) + krow * D + lane * E;
+  T *dkp = reinterpret_cast<T *>(p.dk) + toff(p.sdk, g.k0 + j, hk) + lane * E;
+  T *dvp = reinterpret_cast<T *>(p.dv) + toff(p.sdv, g.k0 + j, hk) + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e++) {
     dkp[e] = Elem<T>::from_f(dk[e] * p.scale);
@@ -189,18 +186,24 @@ static void launch_all(const BwdParams &p, cudaStream_t st) {
     bwd_dkdv_simt_kernel<T, D><<<dim3((p.max_k + 3) / 4, p.hkv, p.batch), 128, 0, st>>>(p);
 }
 
-// K and V -> fp16 copies for the tensor-core backward, 8 elements a thread.
+// K and V (any token / head strides) -> contiguous fp16 copies for the
+// tensor-core backward, 8 elements a thread.
 __global__ void __launch_bounds__(256) kv_to_f16_kernel(const __nv_bfloat16 *__restrict__ k,
                                                         const __nv_bfloat16 *__restrict__ v,
                                                         __half *__restrict__ k16,
                                                         __half *__restrict__ v16, size_t n8,
+                                                        int hkv, int d, Strides sk, Strides sv,
                                                         int *err) {
   bool bad = false;
+  const int per_row = d / 8;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * n8;
        i += (size_t)gridDim.x * blockDim.x) {
     const bool is_v = i >= n8;
-    const size_t j = is_v ? i - n8 : i;
-    const uint4 in = reinterpret_cast<const uint4 *>(is_v ? v : k)[j];
+    const size_t j = is_v ? i - n8 : i;              // 8-element unit of the copy
+    const size_t row = j / per_row, c8 = j % per_row;  // row = token * hkv + head
+    const long long t = (long long)(row / hkv), hk = (long long)(row % hkv);
+    const __nv_bfloat16 *src = (is_v ? v + toff(sv, t, hk) : k + toff(sk, t, hk)) + c8 * 8;
+    const uint4 in = *reinterpret_cast<const uint4 *>(src);
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&in);
     uint4 out;
     __half *y = reinterpret_cast<__half *>(&out);
@@ -222,7 +225,32 @@ cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st) {
   if (blocks > 4096) blocks = 4096;
   kv_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16 *>(p.k), reinterpret_cast<const __nv_bfloat16 *>(p.v),
-      reinterpret_cast<__half *>(p.k16), reinterpret_cast<__half *>(p.v16), n8, p.err);
+      reinterpret_cast<__half *>(p.k16), reinterpret_cast<__half *>(p.v16), n8, p.hkv, p.d, p.sk,
+      p.sv, p.err);
+  return cudaGetLastError();
+}
+
+// Zero every (token, head) row of a [T, H, d] tensor with any strides, 16
+// bytes a thread (d * element size is a multiple of 16 for d = 64 or 128).
+__global__ void __launch_bounds__(256) zero_rows_kernel(char *base, size_t n16, int h, int row_bytes,
+                                                        Strides s, int elem) {
+  const int per_row = row_bytes / 16;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = i / per_row, c16 = i % per_row;
+    const long long t = (long long)(row / h), hh = (long long)(row % h);
+    *reinterpret_cast<uint4 *>(base + toff(s, t, hh) * elem + c16 * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_zero_rows(void *base, int T, int H, int d, Strides s, int elem,
+                             cudaStream_t st) {
+  const size_t n16 = (size_t)T * H * d * elem / 16;
+  if (n16 == 0) return cudaSuccess;
+  size_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  zero_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<char *>(base), n16, H, d * elem,
+                                                      s, elem);
   return cudaGetLastError();
 }
 

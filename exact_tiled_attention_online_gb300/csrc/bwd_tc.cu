@@ -347,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool have = __all_sync(0xffffffffu, ok) && n_it > 0;
     // this warp writes output columns [half D / 2, half D / 2 + D / 2)
-    const size_t krow = ((size_t)(g.k0 + (j < g.nk ? j : 0)) * p.hkv + hk) * D + half * (D / 2);
-    __nv_bfloat16 *dkp = reinterpret_cast<__nv_bfloat16 *>(p.dk) + krow;
-    __nv_bfloat16 *dvp = reinterpret_cast<__nv_bfloat16 *>(p.dv) + krow;
+    const int jt = g.k0 + (j < g.nk ? j : 0);
+    __nv_bfloat16 *dkp = reinterpret_cast<__nv_bfloat16 *>(p.dk) + toff(p.sdk, jt, hk) + half * (D / 2);
+    __nv_bfloat16 *dvp = reinterpret_cast<__nv_bfloat16 *>(p.dv) + toff(p.sdv, jt, hk) + half * (D / 2);
 #pragma unroll
     for (int c = 0; c < D / 64; c++) {
       uint32_t kv32[32], vv32[32];
@@ -625,8 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool have = __all_sync(0xffffffffu, ok) && n_tiles > 0;
     // this warp writes dQ columns [half D / 2, half D / 2 + D / 2)
-    __nv_bfloat16 *dst =
-        reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)t * p.hq + h) * D + half * (D / 2);
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.dq) + toff(p.sdq, t, h) + half * (D / 2);
 #pragma unroll
     for (int c = 0; c < D / 64; c++) {
       uint32_t q32[32];

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.o) + (size_t)row * D + lane * E;
+  __nv_bfloat16 *op = reinterpret_cast<__nv_bfloat16 *>(p.o) + toff(p.so, t, h) + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e += 2)
     *reinterpret_cast<__nv_bfloat162 *>(op + e) =

@@ -200,6 +200,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Element strides of one [tokens, heads, d] tensor: (token t, head h) starts
+// t * ts + h * hs elements from the base; the d features are contiguous.
+struct Strides {
+  long long ts, hs;
+};
+__host__ __device__ __forceinline__ size_t toff(const Strides &s, long long t, long long h) {
+  return (size_t)(t * s.ts + h * s.hs);
+}
+
 // Kernel launch parameters common to the forward kernels.
 struct FwdParams {
   const void *q, *k, *v;
@@ -212,6 +221,7 @@ struct FwdParams {
   int mask;
   int window;             // > 0: bounded window (causal kinds only)
   const float *slopes;    // [hq] linear positional bias slopes, or NULL
+  Strides sq, sk, sv, so;  // layouts of q, k, v, o
   int *err;
   // split-KV partial outputs (NULL when the plan writes o/lse directly)
   float *o_part, *lse_part;
@@ -229,6 +239,7 @@ struct BwdParams {
   int mask;
   int window;             // > 0: bounded window (causal kinds only)
   const float *slopes;    // [hq] linear positional bias slopes, or NULL
+  Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;  // layouts of the eight [T, H, d] tensors
   int *err;
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i
   float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)

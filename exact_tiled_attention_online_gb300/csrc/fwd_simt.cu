@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   if (i >= g.nq) return;
   const int hk = h / (p.hq / p.hkv);
   const int t = g.q0 + i;
-  const T *qp = reinterpret_cast<const T *>(p.q) + ((size_t)t * p.hq + h) * D + lane * E;
+  const T *qp = reinterpret_cast<const T *>(p.q) + toff(p.sq, t, h) + lane * E;
   float qf[E], acc[E];
 #pragma unroll
   for (int e = 0; e < E; e++) {
@@ -39,23 +39,23 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
   const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
   float m = -INFINITY, l = 0.f;
-  const T *kb = reinterpret_cast<const T *>(p.k) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
-  const T *vb = reinterpret_cast<const T *>(p.v) + ((size_t)g.k0 * p.hkv + hk) * D + lane * E;
-  const size_t stride = (size_t)p.hkv * D;
+  const T *kb = reinterpret_cast<const T *>(p.k) + toff(p.sk, g.k0, hk) + lane * E;
+  const T *vb = reinterpret_cast<const T *>(p.v) + toff(p.sv, g.k0, hk) + lane * E;
+  const size_t kstride = (size_t)p.sk.ts, vstride = (size_t)p.sv.ts;  // one key to the next
   for (int j = kbeg; j < kend; j++) {
     float part = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * stride + e]);
+    for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * kstride + e]);
     const float sc = warp_sum(part) + pos_bias2(slope2, bound, j);  // logit in log2 units
     const float m_new = fmaxf(m, sc);
     const float alpha = fast_exp2(m - m_new);
     const float pj = fast_exp2(sc - m_new);
     l = l * alpha + pj;
 #pragma unroll
-    for (int e = 0; e < E; e++) acc[e] = acc[e] * alpha + pj * Elem<T>::to_f(vb[j * stride + e]);
+    for (int e = 0; e < E; e++) acc[e] = acc[e] * alpha + pj * Elem<T>::to_f(vb[j * vstride + e]);
     m = m_new;
   }
-  T *op = reinterpret_cast<T *>(p.o) + ((size_t)t * p.hq + h) * D + lane * E;
+  T *op = reinterpret_cast<T *>(p.o) + toff(p.so, t, h) + lane * E;
   const float inv = kend > kbeg ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; e++) op[e] = Elem<T>::from_f(acc[e] * inv);

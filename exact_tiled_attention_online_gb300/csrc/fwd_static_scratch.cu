@@ -80,6 +80,10 @@ extern "C" attn_status attn_fwd_static_scratch(
   p.mask = mask;
   p.window = window;
   p.slopes = bias_slopes;
+  p.sq = {(long long)hq * d, d};  // contiguous layouts
+  p.sk = {(long long)hkv * d, d};
+  p.sv = {(long long)hkv * d, d};
+  p.so = {(long long)hq * d, d};
   p.err = err;
   // Same carving as the caller-provided workspace of attn_fwd: partial
   // outputs first, partial logsumexps after them.

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row_in) p.lse_part[((size_t)split * p.hq + h) * p.total_q + t] = have ? lse2 : -INFINITY;
     } else {
-      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t * p.hq + h) * D;
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + toff(p.so, t, h);
 #pragma unroll
       for (int c = 0; c < D / 32; c++) {
         uint32_t o32[32];
@@ -475,9 +475,10 @@ cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t s
   a.n_splits = plan.n_splits;
   CUtensorMap mq, mk, mv;
   const int box_h = plan.pack ? plan.group : 1;
-  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, box_h, plan.tile_tokens) ||
-      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys) ||
-      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys))
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, box_h, plan.tile_tokens, bf, p.sq.hs, p.sq.ts) ||
+      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sk.hs, p.sk.ts) ||
+      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sv.hs, p.sv.ts))
     return cudaErrorInvalidValue;
   const long long ctas = (long long)plan.n_m_tiles * (plan.pack ? p.hkv : p.hq) * p.batch *
                          plan.n_splits;

@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const bool have = __all_sync(0xffffffffu, ok) && n_mine > 0;
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
     const float lse2 = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + ((size_t)t * p.hq + h) * D;
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + toff(p.so, t, h);
 #pragma unroll
     for (int c = 0; c < D / 32; c++) {
       uint32_t o32[32];
@@ -467,9 +467,10 @@ cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size
   a.group = p.hq / p.hkv;
   a.n_pairs = (p.max_q + 2 * kTileRows - 1) / (2 * kTileRows);
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, 1, kTileRows) ||
-      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys) ||
-      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys))
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, 1, kTileRows, bf, p.sq.hs, p.sq.ts) ||
+      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sk.hs, p.sk.ts) ||
+      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sv.hs, p.sv.ts))
     return cudaErrorInvalidValue;
   const long long ctas = (long long)a.n_pairs * p.hq * p.batch;
   if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;

@@ -26,13 +26,18 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 64 features x box_h heads x box_t tokens with the 128-byte swizzle (one
 // 128-byte row per (token, head), the K-major layout tcgen05 descriptors
 // expect).
+// head_stride and token_stride are in elements (contiguous THD when they are
+// D and H * D); the encoder checks that they are multiples of 16 bytes.
 inline bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int box_h,
                      int box_t,
-                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     long long head_stride = -1, long long token_stride = -1) {
   auto enc = tensor_map_encoder();
   if (!enc || T <= 0) return false;
+  if (head_stride < 0) head_stride = D;
+  if (token_stride < 0) token_stride = (long long)H * D;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)head_stride * 2, (cuuint64_t)token_stride * 2};
   cuuint32_t box[3] = {64u, (cuuint32_t)box_h, (cuuint32_t)box_t};
   cuuint32_t es[3] = {1u, 1u, 1u};
   CUresult r = enc(m, dt, 3, const_cast<void *>(base), dims, strides,

@@ -97,6 +97,25 @@ typedef enum {
 } attn_dtype;
 
 /*
+ * Layouts other than contiguous THD ("causal-mask-and-ragged-sequence-
+ * layouts", fifth paragraph: noncontiguous layouts where supported).  For
+ * each [tokens, heads, head_dim] tensor, {token stride, head stride} in
+ * elements: element c of (token t, head h) is at t * s[0] + h * s[1] + c, the
+ * head_dim features contiguous.  Contiguous THD is {n_heads * head_dim,
+ * head_dim}.  Every stride must be positive and, times the element size, a
+ * multiple of 16 bytes (so 8 elements for bf16, 4 for fp32); tensors must be
+ * 16-byte aligned; outputs must not overlap each other or any input.  A
+ * typical use: q, k and v as views of one fused projection output
+ * [T, Hq + 2 Hkv, d] (token stride (Hq + 2 Hkv) d), and dq, dk, dv written
+ * into the matching fused gradient buffer.  lse, o_f32 and the workspace
+ * keep the layouts given below.
+ */
+typedef struct {
+  int64_t q[2], k[2], v[2], o[2];        /* read by both calls (o by attn_bwd)  */
+  int64_t dout[2], dq[2], dk[2], dv[2];  /* attn_bwd only                        */
+} attn_strides;
+
+/*
  * Workspace bytes attn_fwd needs for these sizes on the current device (0 when
  * the chosen plan needs none).  The split-KV decode plan keeps one partial
  * output row (fp32) and one partial logsumexp per key split in it.  Returns
@@ -136,6 +155,21 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
                      void *stream);
 
 /*
+ * attn_fwd with the layouts of q, k, v and o given by `strides` (NULL: the
+ * contiguous layouts, exactly attn_fwd).  Same results; ATTN_ERR_INVALID_ARG
+ * for a stride that breaks the rules above.
+ */
+attn_status attn_fwd_ex(const attn_strides *strides, const void *q,
+                        const void *k, const void *v, void *o, float *lse,
+                        float *o_f32, const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_k, int batch,
+                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                        int total_k, int n_heads_q, int n_heads_kv,
+                        int head_dim, float scale, attn_mask_kind mask,
+                        int window, const float *bias_slopes, attn_dtype dtype,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Workspace bytes attn_bwd needs: the per-row terms D_i = dO_i . O_i and the
  * base-2 logsumexp ([n_heads_q, total_q] fp32 each) and, for bf16, fp16
  * copies of q, dout, k and v: the tensor-core backward multiplies in fp16 so
@@ -162,7 +196,8 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
  *            head_dim]; type `dtype`.  Fully overwritten (rows no query
  *            reaches get zeros).
  * For bf16, q, k, v and dout must lie inside the fp16 range (|x| < 65504);
- * a larger value sets ATTN_ERR_DEVICE_RANGE on the device flag.
+ * a larger value sets ATTN_ERR_DEVICE_RANGE on the device flag.  dq, dk and dv
+ * must be 16-byte aligned.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v,
                      const void *o, const float *lse, const float *o_f32,
@@ -174,6 +209,23 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
                      int head_dim, float scale, attn_mask_kind mask,
                      int window, const float *bias_slopes, attn_dtype dtype,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_bwd with the layouts of q, k, v, o, dout, dq, dk and dv given by
+ * `strides` (NULL: contiguous, exactly attn_bwd).  The workspace size does
+ * not depend on the layouts (its fp16 copies are contiguous).
+ */
+attn_status attn_bwd_ex(const attn_strides *strides, const void *q,
+                        const void *k, const void *v, const void *o,
+                        const float *lse, const float *o_f32, const void *dout,
+                        void *dq, void *dk, void *dv,
+                        const int32_t *cu_seqlens_q,
+                        const int32_t *cu_seqlens_k, int batch,
+                        int max_seqlen_q, int max_seqlen_k, int total_q,
+                        int total_k, int n_heads_q, int n_heads_kv,
+                        int head_dim, float scale, attn_mask_kind mask,
+                        int window, const float *bias_slopes, attn_dtype dtype,
+                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Mask probe (diagnostic): writes, for one query head, the packed allowed-pair

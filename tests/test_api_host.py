@@ -94,3 +94,19 @@ def test_bwd_rejects_window_without_causal_rule(lib):
 def test_probe_rejects_bad_tile_rows(lib):
     assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, 0, 48, 1, None) == 1
     assert lib.attn_mask_probe(1, 1, 1, 4, 4, 4, 4, 1, -2, 128, 1, None) == 1
+
+
+def test_strided_entry_rejects_bad_strides(lib):
+    """A token stride of 3 elements (6 bytes) breaks the 16-byte rule."""
+    s = attn.AttnStrides()
+    s.k[0], s.k[1] = 64, 64   # valid: contiguous [T, 1, 64]
+    s.v[0], s.v[1] = 64, 64
+    s.o[0], s.o[1] = 128, 64
+    s.q[0], s.q[1] = 3, 64    # invalid: 6 bytes
+    lib.attn_fwd_ex.argtypes = [ctypes.POINTER(attn.AttnStrides)] + lib.attn_fwd.argtypes
+    args = dict(q=1, k=1, v=1, o=1, lse=1, o_f32=None, cu_q=1, cu_k=1, batch=1, max_q=4,
+                max_k=4, total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, window=0,
+                slopes=None, dtype=0, ws=None, ws_bytes=0, stream=None)
+    assert lib.attn_fwd_ex(ctypes.byref(s), *args.values()) == 1
+    s.q[0] = 0  # only positive strides
+    assert lib.attn_fwd_ex(ctypes.byref(s), *args.values()) == 1

@@ -61,6 +61,89 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
   }
 }
 
+// The same for bf16 inputs with 8- or 16-byte aligned rows: every lane moves
+// its D / 32 consecutive elements with one vector access per tensor.
+template <int D>
+__global__ void __launch_bounds__(128) bwd_pre_vec_kernel(BwdParams p) {
+  constexpr int E = D / 32;  // 4 (one 8-byte bf16 vector) or 2 (4 bytes)
+  static_assert(E == 2 || E == 4, "d = 64 or 128");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 4 + warp;  // t * hq + h
+  if (row >= (long long)p.total_q * p.hq) return;
+  const int t = (int)(row / p.hq), h = (int)(row % p.hq);
+  const __nv_bfloat16 *base_do = reinterpret_cast<const __nv_bfloat16 *>(p.dout);
+  const __nv_bfloat16 *base_q = reinterpret_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *base_o = reinterpret_cast<const __nv_bfloat16 *>(p.o);
+  uint32_t dw[E / 2], qw[E / 2], ow[E / 2];  // bf16 pairs
+  auto load_pairs = [&](const __nv_bfloat16 *src, uint32_t *w) {
+    if constexpr (E == 4) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(src);
+      w[0] = v.x;
+      w[1] = v.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t *>(src);
+    }
+  };
+  load_pairs(base_do + toff(p.sdo, t, h) + lane * E, dw);
+  float dof[E];
+#pragma unroll
+  for (int k = 0; k < E / 2; k++) {
+    dof[2 * k] = __uint_as_float(dw[k] << 16);
+    dof[2 * k + 1] = __uint_as_float(dw[k] & 0xFFFF0000u);
+  }
+  float part = 0.f;
+  if (p.o_f32) {
+    const float *of = p.o_f32 + (size_t)row * D + lane * E;
+    float o[E];
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(of);
+      o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2 *>(of);
+      o[0] = v.x; o[1] = v.y;
+    }
+#pragma unroll
+    for (int e = 0; e < E; e++) part += o[e] * dof[e];
+  } else {
+    load_pairs(base_o + toff(p.so, t, h) + lane * E, ow);
+#pragma unroll
+    for (int k = 0; k < E / 2; k++) {
+      part += __uint_as_float(ow[k] << 16) * dof[2 * k];
+      part += __uint_as_float(ow[k] & 0xFFFF0000u) * dof[2 * k + 1];
+    }
+  }
+  const float D_i = warp_sum(part);
+  // fp16 copies of q and dout (exact inside the fp16 normal range; larger
+  // magnitudes are reported)
+  load_pairs(base_q + toff(p.sq, t, h) + lane * E, qw);
+  uint32_t q16[E / 2], d16[E / 2];
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < E / 2; k++) {
+    const float a0 = __uint_as_float(qw[k] << 16), a1 = __uint_as_float(qw[k] & 0xFFFF0000u);
+    bad |= fabsf(a0) > 65504.f || fabsf(a1) > 65504.f || fabsf(dof[2 * k]) > 65504.f ||
+           fabsf(dof[2 * k + 1]) > 65504.f;
+    const __half2 qa = __floats2half2_rn(a0, a1), da = __floats2half2_rn(dof[2 * k], dof[2 * k + 1]);
+    q16[k] = *reinterpret_cast<const uint32_t *>(&qa);
+    d16[k] = *reinterpret_cast<const uint32_t *>(&da);
+  }
+  __half *q16p = reinterpret_cast<__half *>(p.q16) + (size_t)row * D + lane * E;
+  __half *d16p = reinterpret_cast<__half *>(p.do16) + (size_t)row * D + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(q16p) = make_uint2(q16[0], q16[1]);
+    *reinterpret_cast<uint2 *>(d16p) = make_uint2(d16[0], d16[1]);
+  } else {
+    *reinterpret_cast<uint32_t *>(q16p) = q16[0];
+    *reinterpret_cast<uint32_t *>(d16p) = d16[0];
+  }
+  if (bad) raise_error(p.err, ATTN_ERR_DEVICE_RANGE);
+  if (lane == 0) {
+    const float l = p.lse[(size_t)h * p.total_q + t];
+    p.delta[(size_t)h * p.total_q + t] = D_i;
+    p.lse2[(size_t)h * p.total_q + t] = l == -INFINITY ? INFINITY : l * kLog2e;
+  }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   constexpr int E = D / 32;
@@ -262,8 +345,19 @@ cudaError_t launch_bwd_pre(const BwdParams &p, attn_dtype dtype, cudaStream_t st
     if (p.d == 64) bwd_pre_kernel<float, 64><<<blocks, 128, 0, st>>>(p);
     else bwd_pre_kernel<float, 128><<<blocks, 128, 0, st>>>(p);
   } else {
-    if (p.d == 64) bwd_pre_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, st>>>(p);
-    else bwd_pre_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, st>>>(p);
+    // vector accesses need q, dout, o (or o_f32) aligned to a whole lane's
+    // share of a row: 8 bytes (bf16) and 16 bytes (fp32) at d = 128
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.dout) |
+                        (p.o_f32 ? 0 : reinterpret_cast<uintptr_t>(p.o));
+    const uintptr_t af = reinterpret_cast<uintptr_t>(p.o_f32);
+    const bool vec = p.q16 && (a & (p.d / 16 - 1)) == 0 && (af & (p.d / 8 - 1)) == 0;
+    if (vec) {
+      if (p.d == 64) bwd_pre_vec_kernel<64><<<blocks, 128, 0, st>>>(p);
+      else bwd_pre_vec_kernel<128><<<blocks, 128, 0, st>>>(p);
+    } else {
+      if (p.d == 64) bwd_pre_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, st>>>(p);
+      else bwd_pre_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, st>>>(p);
+    }
   }
   return cudaGetLastError();
 }

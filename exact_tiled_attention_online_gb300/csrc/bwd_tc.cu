@@ -27,6 +27,8 @@
 // forward's.
 #include <stdio.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "plan.h"
 #include "sm100.cuh"
@@ -73,6 +75,10 @@ __device__ __forceinline__ void math_group_sync() {
 // ===========================================================================
 constexpr int kRowsA = 64;   // query rows per step
 constexpr int kKeysA = 128;  // keys per CTA
+// Q / dO ring depth: a stage is refilled only once the gradient products of
+// its step have completed, so the ring must cover that round trip (MMA
+// completion, the refill's TMA latency) with the steps queued behind it.
+constexpr int kStagesA = 4;
 
 template <int D>
 struct LayoutA {
@@ -81,17 +87,17 @@ struct LayoutA {
   static constexpr int kQT = kChunks * kChunk64;   // Q or dO tile (64 rows)
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKV;
-  static constexpr int kQ = kV + kKV;         // [2] stages
-  static constexpr int kDO = kQ + 2 * kQT;    // [2]
-  static constexpr int kRow = kDO + 2 * kQT;  // [2] x {-lse2[64], -D[64]}
+  static constexpr int kQ = kV + kKV;                // [kStagesA] stages
+  static constexpr int kDO = kQ + kStagesA * kQT;    // [kStagesA]
+  static constexpr int kRow = kDO + kStagesA * kQT;  // [2] x {-lse2[64], -D[64]}
   static constexpr int kBar = kRow + 2 * 2 * kRowsA * 4;
   static constexpr int kUsed = kBar + 512;
   static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
 };
 
 struct BarsA {
-  uint64_t kv_full, q_full[2], do_full[2], q_empty[2], do_empty[2], s_full[2], dp_full[2],
-      ps_full[2], mm_done[2];
+  uint64_t kv_full, q_full[kStagesA], do_full[kStagesA], q_empty[kStagesA], do_empty[kStagesA],
+      s_full[2], dp_full[2], ps_full[2], mm_done[2];
   uint32_t tmem_base;
   Sync sync;
 };
@@ -134,11 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&b->kv_full, 1);
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < kStagesA; s++) {
       mbar_init(&b->q_full[s], 1);
       mbar_init(&b->do_full[s], 1);
       mbar_init(&b->q_empty[s], 1);
       mbar_init(&b->do_empty[s], 1);
+    }
+    for (int s = 0; s < 2; s++) {
       mbar_init(&b->s_full[s], 1);
       mbar_init(&b->dp_full[s], 1);
       mbar_init(&b->ps_full[s], 256);
@@ -175,14 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + L::kV + c * kChunk128, &tm_v, &b->kv_full, c * 64, hk, g.k0 + j0);
       }
       for (int it = 0; it < n_it; it++) {
-        const int st = it & 1, u = it >> 1;
+        const int st = it % kStagesA, u = it / kStagesA;
         const int h = it_head(it), tok = g.q0 + it_row0(it);
-        if (it >= 2 && !wait_bar(&b->sync, &b->q_empty[st], (u - 1) & 1, p.err)) break;
+        if (it >= kStagesA && !wait_bar(&b->sync, &b->q_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->q_full[st], L::kQT);
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kQ + st * L::kQT + c * kChunk64, &tm_q, &b->q_full[st], c * 64, h,
                       tok);
-        if (it >= 2 && !wait_bar(&b->sync, &b->do_empty[st], (u - 1) & 1, p.err)) break;
+        if (it >= kStagesA && !wait_bar(&b->sync, &b->do_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->do_full[st], L::kQT);
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kDO + st * L::kQT + c * kChunk64, &tm_do, &b->do_full[st], c * 64,
@@ -230,26 +238,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_st(dV0, dDOk, kColDP);
         mma_commit(&b->dp_full[0]);
       }
+      // tb: the step's TMEM buffer (two), qs: its Q / dO stage (kStagesA)
       for (int it = 0; ok && it < n_it; it++) {
-        const int st = it & 1;
+        const int tb = it & 1, qs = it % kStagesA;
         if (it + 1 < n_it) {
-          const int s1 = (it + 1) & 1, u1 = (it + 1) >> 1;
-          if (!wait_bar(&b->sync, &b->q_full[s1], u1 & 1, p.err)) break;
+          const int t1 = (it + 1) & 1, q1 = (it + 1) % kStagesA, u1 = (it + 1) / kStagesA;
+          if (!wait_bar(&b->sync, &b->q_full[q1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_st(dK0, dQk + qoff(s1), kColS + s1 * kRowsA);
-          mma_commit(&b->s_full[s1]);
-          if (!wait_bar(&b->sync, &b->do_full[s1], u1 & 1, p.err)) break;
+          issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA);
+          mma_commit(&b->s_full[t1]);
+          if (!wait_bar(&b->sync, &b->do_full[q1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_st(dV0, dDOk + qoff(s1), kColDP + s1 * kRowsA);
-          mma_commit(&b->dp_full[s1]);
+          issue_st(dV0, dDOk + qoff(q1), kColDP + t1 * kRowsA);
+          mma_commit(&b->dp_full[t1]);
         }
-        if (!wait_bar(&b->sync, &b->ps_full[st], (it >> 1) & 1, p.err)) break;
+        if (!wait_bar(&b->sync, &b->ps_full[tb], (it >> 1) & 1, p.err)) break;
         tc_fence_after();
-        issue_grad(kColS + st * kRowsA, dDOm + qoff(st), kColDV, it > 0);
-        issue_grad(kColDP + st * kRowsA, dQm + qoff(st), kColDK, it > 0);
-        mma_commit(&b->mm_done[st]);
-        mma_commit(&b->q_empty[st]);
-        mma_commit(&b->do_empty[st]);
+        issue_grad(kColS + tb * kRowsA, dDOm + qoff(qs), kColDV, it > 0);
+        issue_grad(kColDP + tb * kRowsA, dQm + qoff(qs), kColDK, it > 0);
+        mma_commit(&b->mm_done[tb]);
+        mma_commit(&b->q_empty[qs]);
+        mma_commit(&b->do_empty[qs]);
       }
     }
   } else {
@@ -260,6 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = j0 + r;          // in-sequence key
     const int rb = key_row_begin(g.mask, j, g.nq, g.nk);  // rows [rb, re) see key j
     const int re = key_row_end(g.mask, g.window, j, g.nq, g.nk);
+    // Both ends of a key's row range grow with the key, so a step's 64 rows
+    // see all 128 keys of the tile iff the last key's range starts at or
+    // before the step and the first key's range ends at or after it: then no
+    // lane is masked and the step takes the unmasked code (a uniform branch).
+    const bool tile_in = j0 + kKeysA <= g.nk;
+    const int rb_last = key_row_begin(g.mask, j0 + kKeysA - 1, g.nq, g.nk);
+    const int re_first = key_row_end(g.mask, g.window, j0, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = p.scale_log2;
     bool ok = true;
@@ -289,22 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) continue;
       tc_fence_after();
-      const int c_lo = rb - i0, c_hi = re - i0;  // rows i0 + c with c_lo <= c < c_hi see key j
-      const bool full = c_lo <= 0 && c_hi >= kRowsA;
+      const bool step_full = tile_in && rb_last <= i0 && re_first >= i0 + kRowsA;
+      // rows i0 + c with c_lo <= c < c_lo + span see key j
+      const int c_lo = rb - i0, span = re > rb ? re - rb : 0;
       const uint64_t c2x2 = f2(c2, c2);
       // positional bias of row i0 + c: -slope2 |i0 + c + off - j|
       const float slope2 = kBias ? __ldg(p.slopes + it_head(it)) * kLog2e : 0.f;
       const float bdist0 = (float)(j - i0 - causal_offset(g.mask, g.nq, g.nk));
       uint32_t pp[16], dd[16];
-      {
-        const int cc = half;  // this warp's 32 rows of the step
-        uint32_t sv[32], dv[32];
-        tmem_ld32(t_lane + kColS + st * kRowsA + cc * 32, sv);
-        tmem_ld32(t_lane + kColDP + st * kRowsA + cc * 32, dv);
-        tmem_wait_ld();
+      uint32_t sv[32], dv[32];  // this warp's 32 rows of the step
+      tmem_ld32(t_lane + kColS + st * kRowsA + half * 32, sv);
+      tmem_ld32(t_lane + kColDP + st * kRowsA + half * 32, dv);
+      tmem_wait_ld();
+      auto body = [&](auto masked) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int c0 = cc * 32 + e;
+          const int c0 = half * 32 + e;
           // two lanes per instruction: x = c S - lse2, P = 2^x, dS = P (dP - D)
           float2 nl = *reinterpret_cast<const float2 *>(nlse2 + c0);
           const float2 ndd = *reinterpret_cast<const float2 *>(nd + c0);
@@ -316,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, f2(nl.x, nl.y)),
                    x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          if (!full) {
-            if (c0 < c_lo || c0 >= c_hi) p0 = 0.f;
-            if (c0 + 1 < c_lo || c0 + 1 >= c_hi) p1 = 0.f;
+          if constexpr (decltype(masked)::value) {
+            if ((unsigned)(c0 - c_lo) >= (unsigned)span) p0 = 0.f;
+            if ((unsigned)(c0 + 1 - c_lo) >= (unsigned)span) p1 = 0.f;
           }
           const uint64_t pv = f2(p0, p1);
           float d0, d1;
@@ -328,7 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           pp[e / 2] = pack_f16x2(p0, p1);
           dd[e / 2] = pack_f16x2(d0, d1);
         }
-      }
+      };
+      if (step_full)
+        body(std::false_type{});
+      else
+        body(std::true_type{});
       // P^T over the first 16 of the 32 S^T columns this warp just read, dS^T
       // likewise over dP^T: the A operands of the two gradient products,
       // straight from tensor memory.
@@ -388,22 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // dQ
 // ===========================================================================
+// K ring depth: a K stage is refilled only after the dQ product of its tile
+// completes (V is free as soon as dP is), and the refill's TMA latency is
+// longer than the one dP product queued behind that dQ.
+constexpr int kStagesK = 3;
+
 template <int D>
 struct LayoutB {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk128;
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTile;
-  static constexpr int kK = kDO + kTile;   // [2]
-  static constexpr int kV = kK + 2 * kTile;  // [2]
+  static constexpr int kK = kDO + kTile;            // [kStagesK]
+  static constexpr int kV = kK + kStagesK * kTile;  // [2]
   static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kUsed = kBar + 256;
   static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
 };
 
 struct BarsB {
-  uint64_t qdo_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], dp_full, ds_full,
-      dq_done;
+  uint64_t qdo_full, k_full[kStagesK], v_full[2], k_empty[kStagesK], v_empty[2], s_full[2],
+      dp_full, dp_free, ds_full, dq_done;
   uint32_t tmem_base;
   Sync sync;
 };
@@ -443,14 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&b->qdo_full, 1);
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < kStagesK; s++) {
       mbar_init(&b->k_full[s], 1);
-      mbar_init(&b->v_full[s], 1);
       mbar_init(&b->k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->v_full[s], 1);
       mbar_init(&b->v_empty[s], 1);
       mbar_init(&b->s_full[s], 1);
     }
     mbar_init(&b->dp_full, 1);
+    mbar_init(&b->dp_free, 256);
     mbar_init(&b->ds_full, 256);
     mbar_init(&b->dq_done, 1);
     b->sync.abort = 0;
@@ -481,11 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int jj = 0; jj < n_tiles; jj++) {
         const int st = jj & 1, u = jj >> 1;
+        const int ks = jj % kStagesK, ku = jj / kStagesK;
         const int key_row = g.k0 + (n_first + jj) * kTileKeys;
-        if (jj >= 2 && !wait_bar(&b->sync, &b->k_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+        if (jj >= kStagesK && !wait_bar(&b->sync, &b->k_empty[ks], (ku - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->k_full[ks], L::kTile);
         for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kK + st * L::kTile + c * kChunk128, &tm_k, &b->k_full[st], c * 64,
+          tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk128, &tm_k, &b->k_full[ks], c * 64,
                       hk, key_row);
         if (jj >= 2 && !wait_bar(&b->sync, &b->v_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
@@ -511,11 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // dQ += dS K, dS in tensor memory: keys [64 h, 64 h + 64) as 32 packed
       // columns at 64 h of this tile's S buffer
-      auto issue_dq = [&](int st, bool acc) {
+      auto issue_dq = [&](int st, int ks, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; kk++)
           mma_bf16_ts(tmem + kColDQ, tmem + kColS + st * kTileKeys + 64 * (kk >> 2) + 8 * (kk & 3),
-                      dKm + toff(st) + (uint64_t)((kk * 16 * 128) >> 4), idesc_q,
+                      dKm + toff(ks) + (uint64_t)((kk * 16 * 128) >> 4), idesc_q,
                       (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bar(&b->sync, &b->qdo_full, 0, p.err) &&
@@ -532,27 +561,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&b->dp_full);
         mma_commit(&b->v_empty[0]);
       }
+      // st: the tile's S buffer and V stage (two), ks: its K stage (kStagesK)
       for (int jj = 0; ok && jj < n_tiles; jj++) {
-        const int st = jj & 1;
+        const int st = jj & 1, ks = jj % kStagesK;
         const int s1 = (jj + 1) & 1, u1 = (jj + 1) >> 1;
         if (jj + 1 < n_tiles) {
-          if (!wait_bar(&b->sync, &b->k_full[s1], u1 & 1, p.err)) break;
+          const int k1 = (jj + 1) % kStagesK;
+          if (!wait_bar(&b->sync, &b->k_full[k1], ((jj + 1) / kStagesK) & 1, p.err)) break;
           tc_fence_after();
-          issue_s(dQ0, dK0 + toff(s1), kColS + s1 * kTileKeys);
+          issue_s(dQ0, dK0 + toff(k1), kColS + s1 * kTileKeys);
           mma_commit(&b->s_full[s1]);
-        }
-        if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
-        tc_fence_after();
-        issue_dq(st, jj > 0);
-        mma_commit(&b->dq_done);
-        mma_commit(&b->k_empty[st]);
-        if (jj + 1 < n_tiles) {
-          if (!wait_bar(&b->sync, &b->v_full[s1], u1 & 1, p.err)) break;
+          // dP's single buffer is free as soon as the math warps have read
+          // this tile's dP out, well before they finish dS: the next dP
+          // product overlaps this tile's math.
+          if (!wait_bar(&b->sync, &b->dp_free, jj & 1, p.err) ||
+              !wait_bar(&b->sync, &b->v_full[s1], u1 & 1, p.err))
+            break;
           tc_fence_after();
           issue_s(dDO0, dV0 + toff(s1), kColDP);
           mma_commit(&b->dp_full);
           mma_commit(&b->v_empty[s1]);
         }
+        if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
+        tc_fence_after();
+        issue_dq(st, ks, jj > 0);
+        mma_commit(&b->dq_done);
+        mma_commit(&b->k_empty[ks]);
       }
     }
   } else {
@@ -574,8 +608,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int st = jj & 1;
-      ok = wait_bar(&b->sync, &b->s_full[st], (jj >> 1) & 1, p.err) &&
-           wait_bar(&b->sync, &b->dp_full, jj & 1, p.err);
+      ok = wait_bar(&b->sync, &b->dp_full, jj & 1, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // this warp's 64 dP columns into registers, then release the buffer
+      uint32_t dv[64];
+      tmem_ld32(t_lane + kColDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
+      tmem_ld32(t_lane + kColDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&b->dp_free);
+      ok = wait_bar(&b->sync, &b->s_full[st], (jj >> 1) & 1, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -587,10 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S columns it read.
       uint32_t dd[32];
 #pragma unroll
-      for (int cc = 2 * half; cc < 2 * half + 2; cc++) {
-        uint32_t sv[32], dv[32];
+      for (int q = 0; q < 2; q++) {
+        const int cc = 2 * half + q;
+        uint32_t sv[32];
         tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
-        tmem_ld32(t_lane + kColDP + cc * 32, dv);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -607,9 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (jb + c + 1 >= row_limit || jb + c + 1 < row_first) p1 = 0.f;
           }
           float d0, d1;
-          f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), nd2)),
+          f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dv[32 * q + e]),
+                                              __uint_as_float(dv[32 * q + e + 1])), nd2)),
                    d0, d1);
-          dd[(cc & 1) * 16 + e / 2] = pack_f16x2(d0, d1);
+          dd[q * 16 + e / 2] = pack_f16x2(d0, d1);
         }
       }
       tmem_st32(t_lane + kColS + st * kTileKeys + half * 64, dd);

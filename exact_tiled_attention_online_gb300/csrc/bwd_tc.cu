@@ -96,8 +96,11 @@ struct LayoutA {
 };
 
 struct BarsA {
-  uint64_t kv_full, q_full[kStagesA], do_full[kStagesA], q_empty[kStagesA], do_empty[kStagesA],
-      s_full[2], dp_full[2], ps_full[2], mm_done[2];
+  // qdo_full / qdo_empty: one barrier for a step's Q and dO tiles; st_full:
+  // both of a step's score products (S^T and dP^T) done; mm_done: the last
+  // gradient products done.  Few barriers keep the MMA thread's commits and
+  // waits, which the tensor pipe's short issue queue does not hide, few.
+  uint64_t kv_full, qdo_full[kStagesA], qdo_empty[kStagesA], st_full[2], ps_full[2], mm_done;
   uint32_t tmem_base;
   Sync sync;
 };
@@ -141,17 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&b->kv_full, 1);
     for (int s = 0; s < kStagesA; s++) {
-      mbar_init(&b->q_full[s], 1);
-      mbar_init(&b->do_full[s], 1);
-      mbar_init(&b->q_empty[s], 1);
-      mbar_init(&b->do_empty[s], 1);
+      mbar_init(&b->qdo_full[s], 1);
+      mbar_init(&b->qdo_empty[s], 1);
     }
     for (int s = 0; s < 2; s++) {
-      mbar_init(&b->s_full[s], 1);
-      mbar_init(&b->dp_full[s], 1);
+      mbar_init(&b->st_full[s], 1);
       mbar_init(&b->ps_full[s], 256);
-      mbar_init(&b->mm_done[s], 1);
     }
+    mbar_init(&b->mm_done, 1);
     b->sync.abort = 0;
     fence_mbar_init();
   }
@@ -185,16 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_it; it++) {
         const int st = it % kStagesA, u = it / kStagesA;
         const int h = it_head(it), tok = g.q0 + it_row0(it);
-        if (it >= kStagesA && !wait_bar(&b->sync, &b->q_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->q_full[st], L::kQT);
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kQ + st * L::kQT + c * kChunk64, &tm_q, &b->q_full[st], c * 64, h,
+        if (it >= kStagesA && !wait_bar(&b->sync, &b->qdo_empty[st], (u - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&b->qdo_full[st], 2 * L::kQT);
+        for (int c = 0; c < L::kChunks; c++) {
+          tma_load_3d(smem + L::kQ + st * L::kQT + c * kChunk64, &tm_q, &b->qdo_full[st], c * 64, h,
                       tok);
-        if (it >= kStagesA && !wait_bar(&b->sync, &b->do_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->do_full[st], L::kQT);
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kDO + st * L::kQT + c * kChunk64, &tm_do, &b->do_full[st], c * 64,
+          tma_load_3d(smem + L::kDO + st * L::kQT + c * kChunk64, &tm_do, &b->qdo_full[st], c * 64,
                       h, tok);
+        }
       }
     }
   } else if (warp == 1) {
@@ -226,39 +224,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto qoff = [&](int s1) { return (uint64_t)((s1 * L::kQT) >> 4); };
       bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
-                wait_bar(&b->sync, &b->q_full[0], 0, p.err);
+                wait_bar(&b->sync, &b->qdo_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
         issue_st(dK0, dQk, kColS);
-        mma_commit(&b->s_full[0]);
-        ok = wait_bar(&b->sync, &b->do_full[0], 0, p.err);
-      }
-      if (ok) {
-        tc_fence_after();
         issue_st(dV0, dDOk, kColDP);
-        mma_commit(&b->dp_full[0]);
+        mma_commit(&b->st_full[0]);
       }
       // tb: the step's TMEM buffer (two), qs: its Q / dO stage (kStagesA)
       for (int it = 0; ok && it < n_it; it++) {
         const int tb = it & 1, qs = it % kStagesA;
         if (it + 1 < n_it) {
           const int t1 = (it + 1) & 1, q1 = (it + 1) % kStagesA, u1 = (it + 1) / kStagesA;
-          if (!wait_bar(&b->sync, &b->q_full[q1], u1 & 1, p.err)) break;
+          if (!wait_bar(&b->sync, &b->qdo_full[q1], u1 & 1, p.err)) break;
           tc_fence_after();
           issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA);
-          mma_commit(&b->s_full[t1]);
-          if (!wait_bar(&b->sync, &b->do_full[q1], u1 & 1, p.err)) break;
-          tc_fence_after();
           issue_st(dV0, dDOk + qoff(q1), kColDP + t1 * kRowsA);
-          mma_commit(&b->dp_full[t1]);
+          mma_commit(&b->st_full[t1]);
         }
         if (!wait_bar(&b->sync, &b->ps_full[tb], (it >> 1) & 1, p.err)) break;
         tc_fence_after();
         issue_grad(kColS + tb * kRowsA, dDOm + qoff(qs), kColDV, it > 0);
         issue_grad(kColDP + tb * kRowsA, dQm + qoff(qs), kColDK, it > 0);
-        mma_commit(&b->mm_done[tb]);
-        mma_commit(&b->q_empty[qs]);
-        mma_commit(&b->do_empty[qs]);
+        if (it + 1 == n_it) mma_commit(&b->mm_done);
+        if (it + kStagesA < n_it) mma_commit(&b->qdo_empty[qs]);  // a later step refills it
       }
     }
   } else {
@@ -300,8 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
       const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
       if (ok)
-        ok = wait_bar(&b->sync, &b->s_full[st], (it >> 1) & 1, p.err) &&
-             wait_bar(&b->sync, &b->dp_full[st], (it >> 1) & 1, p.err);
+        ok = wait_bar(&b->sync, &b->st_full[st], (it >> 1) & 1, p.err);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) continue;
       tc_fence_after();
@@ -359,8 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&b->ps_full[st]);
     }
     if (ok && n_it > 0) {
-      const int last = n_it - 1;
-      if (wait_bar(&b->sync, &b->mm_done[last & 1], (last >> 1) & 1, p.err))
+      if (wait_bar(&b->sync, &b->mm_done, 0, p.err))
         tc_fence_after();
       else
         ok = false;
@@ -559,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_s(dDO0, dV0, kColDP);
         mma_commit(&b->dp_full);
-        mma_commit(&b->v_empty[0]);
+        if (2 < n_tiles) mma_commit(&b->v_empty[0]);
       }
       // st: the tile's S buffer and V stage (two), ks: its K stage (kStagesK)
       for (int jj = 0; ok && jj < n_tiles; jj++) {
@@ -580,13 +567,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(dDO0, dV0 + toff(s1), kColDP);
           mma_commit(&b->dp_full);
-          mma_commit(&b->v_empty[s1]);
+          if (jj + 3 < n_tiles) mma_commit(&b->v_empty[s1]);  // tile jj + 3 refills it
         }
         if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
         tc_fence_after();
         issue_dq(st, ks, jj > 0);
-        mma_commit(&b->dq_done);
-        mma_commit(&b->k_empty[ks]);
+        if (jj + 1 == n_tiles) mma_commit(&b->dq_done);
+        if (jj + kStagesK < n_tiles) mma_commit(&b->k_empty[ks]);  // a later tile refills it
       }
     }
   } else {
@@ -665,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&b->ds_full);
     }
     if (ok && n_tiles > 0) {
-      if (wait_bar(&b->sync, &b->dq_done, (n_tiles - 1) & 1, p.err))
+      if (wait_bar(&b->sync, &b->dq_done, 0, p.err))
         tc_fence_after();
       else
         ok = false;

@@ -595,36 +595,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int jj = 0; jj < n_tiles; jj++) {
       const int st = jj & 1;
-      ok = wait_bar(&b->sync, &b->dp_full, jj & 1, p.err);
+      // S is issued before dP, so both are in once dP is
+      ok = wait_bar(&b->sync, &b->dp_full, jj & 1, p.err) &&
+           wait_bar(&b->sync, &b->s_full[st], (jj >> 1) & 1, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // this warp's 64 dP columns into registers, then release the buffer
-      uint32_t dv[64];
+      // this warp's 64 dP columns and its first 32 S columns under one wait;
+      // then the dP buffer is released
+      uint32_t dv[64], sv[32];
       tmem_ld32(t_lane + kColDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
       tmem_ld32(t_lane + kColDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_ld32(t_lane + kColS + st * kTileKeys + half * 64, sv);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&b->dp_free);
-      ok = wait_bar(&b->sync, &b->s_full[st], (jj >> 1) & 1, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const bool boundary = !kr.full(n_first + jj);
       const int jb = (n_first + jj) * kTileKeys;
       // dS (fp16 pairs) of this warp's 64 keys goes over the first 32 of the
       // S columns it read.
       uint32_t dd[32];
-#pragma unroll
-      for (int q = 0; q < 2; q++) {
+      // 32 keys from sv: masked lanes (boundary tiles only, a uniform
+      // branch) get P = dS = 0
+      auto chunk = [&](int q, auto masked) {
         const int cc = 2 * half + q;
-        uint32_t sv[32];
-        tmem_ld32(t_lane + kColS + st * kTileKeys + cc * 32, sv);
-        tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int c = cc * 32 + e;
@@ -635,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x0, x1;
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, add2), x0, x1);
           float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          if (boundary) {
+          if constexpr (decltype(masked)::value) {
             if (jb + c >= row_limit || jb + c < row_first) p0 = 0.f;
             if (jb + c + 1 >= row_limit || jb + c + 1 < row_first) p1 = 0.f;
           }
@@ -645,7 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    d0, d1);
           dd[q * 16 + e / 2] = pack_f16x2(d0, d1);
         }
-      }
+      };
+      if (boundary) chunk(0, std::true_type{}); else chunk(0, std::false_type{});
+      tmem_ld32(t_lane + kColS + st * kTileKeys + half * 64 + 32, sv);
+      tmem_wait_ld();
+      if (boundary) chunk(1, std::true_type{}); else chunk(1, std::false_type{});
       tmem_st32(t_lane + kColS + st * kTileKeys + half * 64, dd);
       tmem_wait_st();
       tc_fence_before();

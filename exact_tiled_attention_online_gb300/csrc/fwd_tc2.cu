@@ -282,6 +282,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
     static_assert(!(kBias && kPosScale), "the bias needs the logits before the max");
     const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
+    // causal mask and positive scale: the bias is linear over every allowed key
+    const bool bias_linear = g.mask != ATTN_MASK_NONE && c2 > 0.f;
     const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
@@ -310,12 +312,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
       }
       if constexpr (!kPosScale) {
         const float dist0 = bound - (float)(n * kTileKeys);
+        if (kBias && bias_linear) {
+          // Every allowed key sits at or before the causal bound, so the bias
+          // is -slope2 (dist0 - e) with dist0 - e >= 0 exact in fp32, and a
+          // masked lane's -inf stays -inf (c2 > 0): z = y c2 - slope2 (dist0 - e),
+          // two lanes per instruction.
+          const uint64_t c2x2 = f2(c2, c2), ns2 = f2(-slope2, -slope2), d2 = f2(dist0, dist0);
 #pragma unroll
-        for (int e = 0; e < kTileKeys; e++) {
-          const float y = __uint_as_float(v[e]);
-          float z = y * c2;
-          if constexpr (kBias) z += pos_bias2(slope2, dist0, e);
-          v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : z);
+          for (int e = 0; e < kTileKeys; e += 2) {
+            const uint64_t t2 = fadd2(d2, f2(-(float)e, -(float)(e + 1)));
+            const uint64_t z2 = ffma2(ns2, t2, fmul2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2x2));
+            float z0, z1;
+            f2_split(z2, z0, z1);
+            v[e] = __float_as_uint(z0);
+            v[e + 1] = __float_as_uint(z1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kTileKeys; e++) {
+            const float y = __uint_as_float(v[e]);
+            float z = y * c2;
+            if constexpr (kBias) z += pos_bias2(slope2, dist0, e);
+            v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : z);
+          }
         }
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};

@@ -15,8 +15,11 @@ follows:
   sequence-layouts", first and third paragraphs), optionally bounded to the
   last ``window`` keys up to that causal bound (``window > 0``; the bounded
   window of "attention-algorithm-error-and-complexity-tests", fifth
-  paragraph), and optionally a linear positional bias -slope_h |i + off - j|
-  on every allowed logit (``slopes``);
+  paragraph), optionally a linear positional bias -slope_h |i + off - j|
+  on every allowed logit (``slopes``), and optionally an explicit bias
+  tensor ``bias`` [B or 1, Hq or 1, rows, keys] added to the allowed logits,
+  whose -inf entries remove pairs (same page, third paragraph: bias and mask
+  terms enter the logits before the softmax);
 * forward: two-pass stable softmax over the allowed set, empty rows give
   O = 0 and lse = -inf (same page, fourth paragraph; "formal-correctness",
   "The FlashAttention Proof", online recurrence equals recomputed softmax);
@@ -106,6 +109,24 @@ def _slopes(slopes, hq: int):
     return _ptr(a, _F64)
 
 
+def _btab(bias, batch: int, hq: int):
+    """(NULL, NULL), or pointers to a bias tensor [Bb, Hb, Mq, Mk] (Bb in
+    {1, batch}, Hb in {1, hq}; a dimension of 1 broadcasts) and its sequence,
+    head and row strides."""
+    if bias is None:
+        return None, None
+    a = _f64(bias)
+    if a.ndim != 4 or a.shape[0] not in (1, batch) or a.shape[1] not in (1, hq):
+        raise ValueError("bias tensor must be [1 or B, 1 or Hq, rows, keys]")
+    _, hb, mq, mk = a.shape
+    st = np.array([0 if a.shape[0] == 1 else hb * mq * mk, 0 if hb == 1 else mq * mk, mk],
+                  np.int64)
+    _keep.extend([a, st])
+    if len(_keep) > 64:
+        del _keep[:32]
+    return _ptr(a, _F64), _ptr(st, _I64)
+
+
 class Oracle:
     """ctypes front end to one compiled copy of ``attn_oracle.c``.
 
@@ -123,7 +144,7 @@ class Oracle:
         L.oracle_mask.restype = ctypes.c_int
         common = [_F64, _F64, _F64]
         sizes = ([_I32, _I32] + [ctypes.c_int] * 6
-                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int, _F64])
+                 + [ctypes.c_double, ctypes.c_int, ctypes.c_int, _F64, _F64, _I64])
         L.oracle_fwd.argtypes = common + sizes + [_I64, ctypes.c_int64, _F64, _F64]
         L.oracle_fwd.restype = ctypes.c_int
         L.oracle_bwd.argtypes = common + [_F64] + sizes + [_F64] * 5
@@ -160,7 +181,7 @@ class Oracle:
 
     # -- forward ------------------------------------------------------------
     def fwd(self, q, k, v, cu_q, cu_k, scale: float, mask_kind: int, rows=None,
-            window: int = 0, slopes=None):
+            window: int = 0, slopes=None, bias=None):
         """Forward.  q [Tq, Hq, d], k/v [Tk, Hkv, d].
 
         rows None -> (o [Tq, Hq, d], lse [Hq, Tq]); rows = int array [n, 2] of
@@ -183,7 +204,8 @@ class Oracle:
         rc = self.lib.oracle_fwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1,
                                  tq, tk, hq, hkv, d, float(scale), mask_kind,
-                                 int(window), _slopes(slopes, hq), rp, n, _ptr(o, _F64),
+                                 int(window), _slopes(slopes, hq), *_btab(bias, len(cq) - 1, hq),
+                                 rp, n, _ptr(o, _F64),
                                  _ptr(lse, _F64))
         if rc != 0:
             raise ValueError("invalid oracle_fwd arguments")
@@ -193,7 +215,7 @@ class Oracle:
 
     # -- backward -----------------------------------------------------------
     def bwd(self, q, k, v, dout, cu_q, cu_k, scale: float, mask_kind: int,
-            window: int = 0, slopes=None):
+            window: int = 0, slopes=None, bias=None):
         """Full backward -> (dq, dk, dv, o, lse), fp64."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
         cq, ck = _i32(cu_q), _i32(cu_k)
@@ -207,7 +229,8 @@ class Oracle:
         rc = self.lib.oracle_bwd(_ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64),
                                  _ptr(dout, _F64), _ptr(cq, _I32), _ptr(ck, _I32),
                                  len(cq) - 1, tq, tk, hq, hkv, d, float(scale),
-                                 mask_kind, int(window), _slopes(slopes, hq), _ptr(dq, _F64),
+                                 mask_kind, int(window), _slopes(slopes, hq),
+                                 *_btab(bias, len(cq) - 1, hq), _ptr(dq, _F64),
                                  _ptr(dk, _F64),
                                  _ptr(dv, _F64), _ptr(o, _F64), _ptr(lse, _F64))
         if rc != 0:
@@ -215,7 +238,8 @@ class Oracle:
         return dq, dk, dv, o, lse
 
     def bwd_sampled(self, q, k, v, dout, cu_q, cu_k, scale: float,
-                    mask_kind: int, q_rows, k_rows, window: int = 0, slopes=None):
+                    mask_kind: int, q_rows, k_rows, window: int = 0, slopes=None,
+                    bias=None):
         """dQ at sampled (token, head) rows and dK, dV at sampled
         (key token, kv head) rows -> (dq [nq, d], dk [nk, d], dv [nk, d])."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -230,7 +254,8 @@ class Oracle:
         rc = self.lib.oracle_bwd_sampled(
             _ptr(q, _F64), _ptr(k, _F64), _ptr(v, _F64), _ptr(dout, _F64),
             _ptr(cq, _I32), _ptr(ck, _I32), len(cq) - 1, tq, tk, hq, hkv, d,
-            float(scale), mask_kind, int(window), _slopes(slopes, hq), _ptr(qr, _I64), len(qr),
+            float(scale), mask_kind, int(window), _slopes(slopes, hq),
+            *_btab(bias, len(cq) - 1, hq), _ptr(qr, _I64), len(qr),
             _ptr(dq, _F64),
             _ptr(kr, _I64), len(kr), _ptr(dk, _F64), _ptr(dv, _F64))
         if rc != 0:

@@ -41,8 +41,16 @@
  *     error-and-complexity-tests", third paragraph, and "causal-mask-and-
  *     ragged-sequence-layouts", sixth paragraph: biases move with the
  *     positions and are rebuilt the same way in the backward).
- *   - A row whose allowed set is empty has O = 0 exactly and lse = -inf
- *     (same page, fourth paragraph).
+ *   - btab != NULL adds an explicit bias tensor to every allowed logit:
+ *     B[s][h][i][j] = btab[s * bss + h * bhs + i * brs + j] for sequence s,
+ *     query head h, in-sequence row i and key j (a stride of 0 broadcasts),
+ *     in the units of the scaled logits.  An entry of -inf removes the pair:
+ *     exp(-inf) = 0, so it is an explicit mask ("attention-algorithm-error-
+ *     and-complexity-tests", third paragraph: bias and mask terms enter the
+ *     logits before the softmax; "causal-mask-and-ragged-sequence-layouts",
+ *     sixth paragraph: the backward rebuilds them identically).
+ *   - A row whose allowed set is empty, or whose allowed logits are all -inf,
+ *     has O = 0 exactly and lse = -inf (same page, fourth paragraph).
  *
  * Backward (recompute form, at a given upstream gradient dO):
  *   P_ij = exp(s_ij - lse_i), dP_ij = dO_i . v_j, D_i = dO_i . O_i,
@@ -72,6 +80,8 @@ typedef struct {
   int mask_kind;
   int window; /* > 0: at most `window` keys per row, the latest allowed ones */
   const double *slopes; /* [hq] linear positional bias slopes, or NULL */
+  const double *btab;   /* explicit bias tensor, or NULL */
+  int64_t bss, bhs, brs; /* its sequence, head and row strides */
   int32_t *seq_q, *pos_q, *seq_k, *pos_k; /* per-token metadata */
 } problem_t;
 
@@ -139,6 +149,20 @@ static double pos_bias(const problem_t *p, int tq, int tk, int h) {
   return -p->slopes[h] * fabs((double)dist);
 }
 
+/* The explicit bias tensor's entry for an allowed (query token, key token)
+ * pair of query head h: 0 without a tensor. */
+static double tab_bias(const problem_t *p, int tq, int tk, int h) {
+  if (!p->btab) return 0.0;
+  int64_t s = p->seq_q[tq], i = p->pos_q[tq], j = p->pos_k[tk];
+  return p->btab[s * p->bss + (int64_t)h * p->bhs + i * p->brs + j];
+}
+
+/* The logit of an allowed pair: scaled dot product plus both biases. */
+static double logit(const problem_t *p, const double *qi, const double *kj,
+                    int tq, int tk, int h) {
+  return p->scale * dot(qi, kj, p->d) + pos_bias(p, tq, tk, h) + tab_bias(p, tq, tk, h);
+}
+
 static const double *q_row(const problem_t *p, int t, int h) {
   return p->q + ((size_t)t * p->hq + h) * p->d;
 }
@@ -169,8 +193,12 @@ static void forward_row(const problem_t *p, int t, int h, unsigned char *mrow,
   double m = -INFINITY;
   for (int u = 0; u < p->total_k; u++) {
     if (!mrow[u]) continue;
-    srow[u] = p->scale * dot(qi, k_row(p, u, hk), p->d) + pos_bias(p, t, u, h);
+    srow[u] = logit(p, qi, k_row(p, u, hk), t, u, h);
     if (srow[u] > m) m = srow[u];
+  }
+  if (m == -INFINITY) { /* every allowed logit masked by the bias tensor */
+    *lse = -INFINITY;
+    return;
   }
   double l = 0.0;
   for (int u = 0; u < p->total_k; u++)
@@ -188,8 +216,10 @@ static void forward_row(const problem_t *p, int t, int h, unsigned char *mrow,
 static int setup(problem_t *p, const double *q, const double *k,
                  const double *v, const int32_t *cu_q, const int32_t *cu_k,
                  int batch, int total_q, int total_k, int hq, int hkv, int d,
-                 double scale, int mask_kind, int window, const double *slopes) {
+                 double scale, int mask_kind, int window, const double *slopes,
+                 const double *btab, const int64_t *bstr) {
   p->seq_q = p->pos_q = p->seq_k = p->pos_k = NULL;
+  if (btab && (!bstr || bstr[0] < 0 || bstr[1] < 0 || bstr[2] < 0)) return -1;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0) return -1;
   if (mask_kind < 0 || mask_kind > 2) return -1;
   if (window > 0 && mask_kind == ORACLE_MASK_NONE) return -1;
@@ -208,6 +238,10 @@ static int setup(problem_t *p, const double *q, const double *k,
   p->mask_kind = mask_kind;
   p->window = window;
   p->slopes = slopes;
+  p->btab = btab;
+  p->bss = btab ? bstr[0] : 0;
+  p->bhs = btab ? bstr[1] : 0;
+  p->brs = btab ? bstr[2] : 0;
   p->seq_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->pos_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q + 1));
   p->seq_k = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_k + 1));
@@ -232,7 +266,7 @@ int oracle_mask(const int32_t *cu_q, const int32_t *cu_k, int batch,
                 unsigned char *m) {
   problem_t p;
   int rc = setup(&p, NULL, NULL, NULL, cu_q, cu_k, batch, total_q, total_k, 1,
-                 1, 1, 1.0, mask_kind, window, NULL);
+                 1, 1, 1.0, mask_kind, window, NULL, NULL, NULL);
   if (rc == 0)
     for (int t = 0; t < total_q; t++)
       for (int u = 0; u < total_k; u++)
@@ -248,10 +282,11 @@ int oracle_fwd(const double *q, const double *k, const double *v,
                const int32_t *cu_q, const int32_t *cu_k, int batch,
                int total_q, int total_k, int hq, int hkv, int d, double scale,
                int mask_kind, int window, const double *slopes,
+               const double *btab, const int64_t *bstr,
                const int64_t *rows, int64_t nrows, double *o, double *lse) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind, window, slopes);
+                 scale, mask_kind, window, slopes, btab, bstr);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -301,7 +336,7 @@ static void backward_row(const problem_t *p, const double *dout, int t, int h,
   for (int u = 0; u < p->total_k; u++) {
     if (!mrow[u]) continue;
     const double *kj = k_row(p, u, hk), *vj = v_row(p, u, hk);
-    double s = p->scale * dot(qi, kj, p->d) + pos_bias(p, t, u, h);
+    double s = logit(p, qi, kj, t, u, h);
     double pij = exp(s - lse_i);
     double dpij = dot(doi, vj, p->d);
     double ds = pij * (dpij - D_i);
@@ -323,13 +358,14 @@ int oracle_bwd(const double *q, const double *k, const double *v,
                const double *dout, const int32_t *cu_q, const int32_t *cu_k,
                int batch, int total_q, int total_k, int hq, int hkv, int d,
                double scale, int mask_kind, int window, const double *slopes,
+               const double *btab, const int64_t *bstr,
                double *dq, double *dk, double *dv, double *o, double *lse) {
   int rc = oracle_fwd(q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                      scale, mask_kind, window, slopes, NULL, 0, o, lse);
+                      scale, mask_kind, window, slopes, btab, bstr, NULL, 0, o, lse);
   if (rc != 0) return rc;
   problem_t p;
   rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-             scale, mask_kind, window, slopes);
+             scale, mask_kind, window, slopes, btab, bstr);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -381,12 +417,13 @@ int oracle_bwd_sampled(const double *q, const double *k, const double *v,
                        const int32_t *cu_k, int batch, int total_q,
                        int total_k, int hq, int hkv, int d, double scale,
                        int mask_kind, int window, const double *slopes,
+                       const double *btab, const int64_t *bstr,
                        const int64_t *q_rows, int64_t nq_rows,
                        double *dq_out, const int64_t *k_rows, int64_t nk_rows,
                        double *dk_out, double *dv_out) {
   problem_t p;
   int rc = setup(&p, q, k, v, cu_q, cu_k, batch, total_q, total_k, hq, hkv, d,
-                 scale, mask_kind, window, slopes);
+                 scale, mask_kind, window, slopes, btab, bstr);
   if (rc != 0) {
     teardown(&p);
     return rc;
@@ -434,7 +471,8 @@ int oracle_bwd_sampled(const double *q, const double *k, const double *v,
           size_t row = (size_t)t * hq + h;
           const double *qi = q_row(&p, t, h);
           const double *doi = dout + row * d;
-          double s = scale * dot(qi, kj, d) + pos_bias(&p, t, u, h);
+          if (lse[row] == -INFINITY) continue; /* empty row */
+          double s = logit(&p, qi, kj, t, u, h);
           double pij = exp(s - lse[row]);
           double ds = pij * (dot(doi, vj, d) - D[row]);
           for (int c = 0; c < d; c++) {

@@ -586,6 +586,105 @@ def pin_bias_finite_differences(orc):
             np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=(name, kind))
 
 
+def rand_btab(rng, lq, lk, hq, p_minf=0.2):
+    """A random explicit bias tensor [B, Hq, max Nq, max Nk]: N(0, 1) entries,
+    about ``p_minf`` of them -inf (masked pairs)."""
+    b = rng.standard_normal((len(lq), hq, max(max(lq), 1), max(max(lk), 1)))
+    b[rng.random(b.shape) < p_minf] = -np.inf
+    return b
+
+
+def pin_tab_torch_sdpa_fp64(orc):
+    """torch's fp64 reference attention with the causal rule and the explicit
+    bias tensor together as one additive float mask, forward, lse and every
+    gradient, on the rows that keep at least one finite logit."""
+    rng = np.random.default_rng(46)
+    for (lq, lk, hq, hkv, d, kind) in SHAPES:
+        q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+        do = rng.standard_normal(q.shape)
+        bt = rand_btab(rng, lq, lk, hq)
+        scale = 1.0 / math.sqrt(d)
+        dq, dk, dv, o, lse = orc.bwd(q, k, v, do, cu(lq), cu(lk), scale, kind, bias=bt)
+        g = hq // hkv
+        cq, ck = cu(lq), cu(lk)
+        for s_, (nq, nk) in enumerate(zip(lq, lk)):
+            full = np.full((hq, nq, nk), -np.inf)
+            for i in range(nq):
+                a, b = row_range(kind, i, nq, nk)
+                full[:, i, a:b] = bt[s_, :, i, a:b]
+            live = np.isfinite(full).any(axis=2)  # [hq, nq]
+            for h in range(hq):
+                for i in range(nq):
+                    t = cq[s_] + i
+                    if not live[h, i]:
+                        assert np.isneginf(lse[h, t]) and np.all(o[t, h] == 0) and np.all(dq[t, h] == 0)
+            qs = torch.tensor(q[cq[s_]:cq[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            ks = torch.tensor(k[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            vs = torch.tensor(v[ck[s_]:ck[s_ + 1]].transpose(1, 0, 2), requires_grad=True)
+            if not live.any():
+                continue
+            # dead rows get a harmless finite mask in torch and no upstream gradient
+            safe = np.where(live[:, :, None], full, 0.0)
+            wgt = torch.tensor(live[:, :, None].astype(np.float64))
+            kr, vr = ks.repeat_interleave(g, dim=0), vs.repeat_interleave(g, dim=0)
+            out = torch.nn.functional.scaled_dot_product_attention(
+                qs, kr, vr, attn_mask=torch.tensor(safe), scale=scale)
+            dot = torch.tensor(do[cq[s_]:cq[s_ + 1]].transpose(1, 0, 2))
+            (out * dot * wgt).sum().backward()
+            ref_lse = torch.logsumexp(qs.detach() @ kr.detach().transpose(1, 2) * scale
+                                      + torch.tensor(full), dim=2).numpy()
+            ot = out.detach().numpy().transpose(1, 0, 2)
+            for h in range(hq):
+                rows = np.nonzero(live[h])[0]
+                np.testing.assert_allclose(o[cq[s_] + rows, h], ot[rows, h], rtol=1e-10, atol=1e-12)
+                np.testing.assert_allclose(lse[h, cq[s_] + rows], ref_lse[h, rows], rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(dq[cq[s_] + rows, h],
+                                           qs.grad.numpy().transpose(1, 0, 2)[rows, h], rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dk[ck[s_]:ck[s_ + 1]], ks.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+            np.testing.assert_allclose(dv[ck[s_]:ck[s_ + 1]], vs.grad.numpy().transpose(1, 0, 2),
+                                       rtol=1e-9, atol=1e-11)
+
+
+def pin_tab_zero_and_broadcast(orc):
+    """A zero bias tensor changes nothing (bit for bit), and a tensor of one
+    sequence or one head gives exactly what its explicit expansion gives."""
+    rng = np.random.default_rng(47)
+    lq, lk, hq, hkv, d = (4, 6), (7, 6), 4, 2, 5
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    for kind in (NONE, TOP_LEFT, BOTTOM_RIGHT):
+        o0, l0 = orc.fwd(q, k, v, cu(lq), cu(lk), 0.4, kind)
+        o1, l1 = orc.fwd(q, k, v, cu(lq), cu(lk), 0.4, kind, bias=np.zeros((1, 1, 6, 7)))
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+        for shape in ((1, hq, 6, 7), (2, 1, 6, 7), (1, 1, 6, 7)):
+            b = rng.standard_normal(shape)
+            ob, lb = orc.fwd(q, k, v, cu(lq), cu(lk), 0.4, kind, bias=b)
+            oe, le = orc.fwd(q, k, v, cu(lq), cu(lk), 0.4, kind,
+                             bias=np.ascontiguousarray(np.broadcast_to(b, (2, hq, 6, 7))))
+            assert np.array_equal(ob, oe) and np.array_equal(lb, le)
+
+
+def pin_tab_row_constant(orc):
+    """A bias that is constant along a row's keys leaves O unchanged and adds
+    the constant to lse (softmax is shift-invariant)."""
+    rng = np.random.default_rng(48)
+    lq, lk, hq, hkv, d = (5, 3), (5, 8), 2, 1, 4
+    q, k, v = rand_case(rng, lq, lk, hq, hkv, d)
+    c = rng.uniform(-3, 3, (2, hq, 5))
+    b = np.repeat(c[:, :, :, None], 8, axis=3)
+    for kind in (TOP_LEFT, BOTTOM_RIGHT):
+        o0, l0 = orc.fwd(q, k, v, cu(lq), cu(lk), 0.6, kind)
+        o1, l1 = orc.fwd(q, k, v, cu(lq), cu(lk), 0.6, kind, bias=b)
+        np.testing.assert_allclose(o1, o0, rtol=1e-12, atol=1e-14)
+        cq = cu(lq)
+        for s_, nq in enumerate(lq):
+            for i in range(nq):
+                t = cq[s_] + i
+                for h in range(hq):
+                    if np.isfinite(l0[h, t]):
+                        np.testing.assert_allclose(l1[h, t], l0[h, t] + c[s_, h, i], rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
     pin_token_meta, pin_mask_intervals, pin_golden_mask_counts,
     pin_window_counts, pin_window_one_key, pin_window_covering_is_causal,
@@ -595,4 +694,5 @@ ALL_PINS = [
     pin_dv_column_sum, pin_dq_key_shift, pin_scale_identity,
     pin_empty_rows_backward, pin_bias_uniform_logits, pin_bias_zero_slopes,
     pin_bias_torch_sdpa_fp64, pin_bias_finite_differences,
+    pin_tab_torch_sdpa_fp64, pin_tab_zero_and_broadcast, pin_tab_row_constant,
 ]

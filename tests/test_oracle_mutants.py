@@ -21,7 +21,7 @@ from tests import oracle_pins as pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
-    "dropped_scale": ("srow[u] = p->scale * dot(", "srow[u] = dot("),
+    "dropped_scale": ("return p->scale * dot(qi, kj, p->d) +", "return dot(qi, kj, p->d) +"),
     "lse_without_max": ("double lse_i = m + log(l);", "double lse_i = log(l);"),
     "no_max_subtraction": ("if (mrow[u]) l += exp(srow[u] - m);",
                            "if (mrow[u]) l += exp(srow[u]);"),
@@ -39,8 +39,14 @@ MUTANTS = {
                              "return -p->slopes[h] * (double)dist;"),
     "bias_global_positions": ("int dist = p->pos_q[tq] + off - p->pos_k[tk];",
                               "int dist = tq + off - tk;"),
-    "bias_missing_in_backward": ("double s = p->scale * dot(qi, kj, p->d) + pos_bias(p, t, u, h);",
+    "bias_missing_in_backward": ("double s = logit(p, qi, kj, t, u, h);",
                                  "double s = p->scale * dot(qi, kj, p->d);"),
+    "tab_bias_sign_flipped": ("return p->btab[", "return -p->btab["),
+    "tab_bias_head_ignored": ("(int64_t)h * p->bhs", "0 * p->bhs"),
+    "tab_bias_sequence_ignored": ("s * p->bss", "0 * p->bss"),
+    "tab_bias_in_log2_units": ("+ tab_bias(p, tq, tk, h);", "+ 1.4426950408889634 * tab_bias(p, tq, tk, h);"),
+    "tab_masked_row_not_empty": ("if (m == -INFINITY) { /* every allowed logit masked by the bias tensor */",
+                                 "if (0) {"),
     "window_accepted_without_causal": (
         "if (window > 0 && mask_kind == ORACLE_MASK_NONE) return -1;", ""),
     "global_offset_as_position": ("pos[t] = t - cu[s];", "pos[t] = t;"),

@@ -37,6 +37,12 @@ class AttnStrides(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64 * 2) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")]
 
 
+class AttnBiasTensor(ctypes.Structure):
+    """``attn_bias_tensor``: fp32 data and its sequence, head and row strides."""
+    _fields_ = [("data", ctypes.c_void_p), ("seq_stride", ctypes.c_int64),
+                ("head_stride", ctypes.c_int64), ("row_stride", ctypes.c_int64)]
+
+
 class AttnError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn} failed: status {status} ({STATUS.get(status, '?')})")
@@ -65,9 +71,10 @@ def library() -> ctypes.CDLL:
     L.attn_fwd.restype = I
     L.attn_bwd.argtypes = [P] * 12 + [I] * 8 + [F, I, I, P, I, P, SZ, P]
     L.attn_bwd.restype = I
-    L.attn_fwd_ex.argtypes = [ctypes.POINTER(AttnStrides)] + L.attn_fwd.argtypes
+    ex = [ctypes.POINTER(AttnStrides), ctypes.POINTER(AttnBiasTensor)]
+    L.attn_fwd_ex.argtypes = ex + L.attn_fwd.argtypes
     L.attn_fwd_ex.restype = I
-    L.attn_bwd_ex.argtypes = [ctypes.POINTER(AttnStrides)] + L.attn_bwd.argtypes
+    L.attn_bwd_ex.argtypes = ex + L.attn_bwd.argtypes
     L.attn_bwd_ex.restype = I
     L.attn_fwd_workspace_size.argtypes = [I] * 9
     L.attn_fwd_workspace_size.restype = SZ
@@ -137,6 +144,22 @@ def _slopes_ptr(slopes: Optional[torch.Tensor], hq: int) -> Optional[int]:
     return slopes.data_ptr()
 
 
+def _btab(bias: Optional[torch.Tensor], batch: int, hq: int, max_q: int, max_k: int):
+    """``attn_bias_tensor`` for a 4-D fp32 CUDA tensor [1 or B, 1 or Hq,
+    >= max_seqlen_q, >= max_seqlen_k] with unit key stride (broadcast views
+    from ``expand`` are fine), or None."""
+    if bias is None:
+        return None
+    if not isinstance(bias, torch.Tensor) or not bias.is_cuda or bias.dtype != torch.float32:
+        raise ValueError("bias must be an fp32 CUDA tensor")
+    if bias.dim() != 4 or bias.shape[0] not in (1, batch) or bias.shape[1] not in (1, hq):
+        raise ValueError("bias must be [1 or B, 1 or Hq, rows, keys]")
+    if bias.shape[2] < max_q or bias.shape[3] < max_k or (bias.shape[3] > 1 and bias.stride(3) != 1):
+        raise ValueError("bias must cover max_seqlen_q rows and max_seqlen_k keys, keys contiguous")
+    st = [0 if bias.shape[i] == 1 else bias.stride(i) for i in range(3)]
+    return AttnBiasTensor(bias.data_ptr(), st[0], st[1], st[2])
+
+
 def fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, dtype_code, window=0) -> int:
     n = library().attn_fwd_workspace_size(batch, max_q, max_k, total_q, hq, hkv, d, int(window),
                                           dtype_code)
@@ -158,13 +181,15 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
         workspace: Optional[torch.Tensor] = None, stream=None, want_lse: bool = True,
         o_f32: Optional[torch.Tensor] = None, want_o_f32: bool = False, window: int = 0,
-        bias_slopes: Optional[torch.Tensor] = None):
+        bias_slopes: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None):
     """Attention forward on packed ragged tensors (layouts in include/attn.h).
 
     ``window`` > 0 (causal masks only) bounds every row to the ``window`` key
     positions that end at its causal bound.  ``bias_slopes`` (fp32 CUDA
     tensor, one slope per query head) adds the linear positional bias
-    -slope_h * |i + off - j|.
+    -slope_h * |i + off - j|.  ``bias`` (fp32 CUDA tensor [1 or B, 1 or Hq,
+    rows, keys], entry [s, h, i, j] for in-sequence row i and key j) is added
+    to the scaled logits; -inf entries mask pairs.
 
     Returns (o, lse), or (o, lse, o_f32) when ``want_o_f32`` is set or an
     ``o_f32`` buffer is given.  lse is [n_heads_q, total_q] fp32 (None when
@@ -196,8 +221,9 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: in
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     strides = _strides(q=q, k=k, v=v, o=out)
+    bt = _btab(bias, batch, hq, max_seqlen_q, max_seqlen_k)
     st = library().attn_fwd_ex(
-        ctypes.byref(strides),
+        ctypes.byref(strides), None if bt is None else ctypes.byref(bt),
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(o_f32), _ptr(cu_seqlens_q),
         _ptr(cu_seqlens_k),
         batch, max_seqlen_q, max_seqlen_k, total_q, total_k, hq, hkv, d, float(scale),
@@ -212,11 +238,11 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         max_seqlen_k: int, mask: int = CAUSAL_TOP_LEFT, scale: Optional[float] = None,
         dq=None, dk=None, dv=None, workspace=None, stream=None,
         o_f32: Optional[torch.Tensor] = None, window: int = 0,
-        bias_slopes: Optional[torch.Tensor] = None):
+        bias_slopes: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None):
     """Attention backward; returns (dq, dk, dv) with dk/dv summed over each
     KV head's group of query heads.  Pass the forward's ``o_f32`` when it was
     kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding; pass the
-    forward's mask, ``window`` and ``bias_slopes``."""
+    forward's mask, ``window``, ``bias_slopes`` and ``bias``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n, 3, True)
     _check(lse, "lse", 2)
@@ -236,8 +262,9 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     strides = _strides(q=q, k=k, v=v, o=o, dout=dout, dq=dq, dk=dk, dv=dv)
+    bt = _btab(bias, batch, hq, max_seqlen_q, max_seqlen_k)
     st = library().attn_bwd_ex(
-        ctypes.byref(strides),
+        ctypes.byref(strides), None if bt is None else ctypes.byref(bt),
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_f32), _ptr(dout), _ptr(dq),
         _ptr(dk), _ptr(dv),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, max_seqlen_q, max_seqlen_k, total_q,

@@ -162,12 +162,27 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
                      attn_mask_kind mask, int window, const float *bias_slopes,
                      attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
-  return attn_fwd_ex(nullptr, q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q,
+  return attn_fwd_ex(nullptr, nullptr, q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q,
                      total_k, hq, hkv, d, scale, mask, window, bias_slopes, dtype, workspace,
                      workspace_bytes, stream);
 }
 
-attn_status attn_fwd_ex(const attn_strides *strides, const void *q, const void *k,
+// The explicit bias tensor's fields, or false for a malformed one.
+static bool pick_btab(const attn_bias_tensor *b, const float **data, long long *ss, long long *hs,
+                      long long *rs) {
+  *data = nullptr;
+  *ss = *hs = *rs = 0;
+  if (!b) return true;
+  if (!b->data || b->seq_stride < 0 || b->head_stride < 0 || b->row_stride < 0) return false;
+  if (reinterpret_cast<uintptr_t>(b->data) & 3) return false;
+  *data = b->data;
+  *ss = b->seq_stride;
+  *hs = b->head_stride;
+  *rs = b->row_stride;
+  return true;
+}
+
+attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q, const void *k,
                         const void *v, void *o, float *lse, float *o_f32, const int32_t *cu_q,
                         const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
                         int total_k, int hq, int hkv, int d, float scale, attn_mask_kind mask,
@@ -189,6 +204,7 @@ attn_status attn_fwd_ex(const attn_strides *strides, const void *q, const void *
   p.mask = mask;
   p.window = window;
   p.slopes = bias_slopes;
+  if (!pick_btab(bias, &p.btab, &p.bss, &p.bhs, &p.brs)) return ATTN_ERR_INVALID_ARG;
   const int elem = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
   if (!pick_strides(strides ? strides->q : nullptr, hq, d, elem, &p.sq) ||
       !pick_strides(strides ? strides->k : nullptr, hkv, d, elem, &p.sk) ||
@@ -203,6 +219,7 @@ attn_status attn_fwd_ex(const attn_strides *strides, const void *q, const void *
   }
   TcPlan plan =
       choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype, sm_count());
+  if (p.btab) plan.kind = PLAN_SIMT;  // the bias tensor is read by the CUDA-core kernel only
   if (plan.kind != PLAN_SIMT) {
     // TMA needs 16-byte aligned tensors; with no keys at all every row is
     // empty and the CUDA-core kernel writes the zeros and -inf directly.
@@ -217,8 +234,9 @@ attn_status attn_fwd_ex(const attn_strides *strides, const void *q, const void *
   cudaError_t ce;
   if (plan.kind == PLAN_SIMT) {
     ce = launch_fwd_simt(p, dtype, cs);
-    snprintf(desc, sizeof(desc), "fwd_simt_%s_d%d grid=(%d,%d,%d)",
-             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d, (max_q + 3) / 4, hq, batch);
+    snprintf(desc, sizeof(desc), "fwd_simt_%s_d%d%s grid=(%d,%d,%d)",
+             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d, p.btab ? "_btab" : "",
+             (max_q + 3) / 4, hq, batch);
   } else {
     if (plan.kind == PLAN_TC_SPLIT) {
       size_t need = fwd_split_workspace(plan, total_q, hq, d);
@@ -257,12 +275,12 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      int total_q, int total_k, int hq, int hkv, int d, float scale,
                      attn_mask_kind mask, int window, const float *bias_slopes,
                      attn_dtype dtype, void *workspace, size_t workspace_bytes, void *stream) {
-  return attn_bwd_ex(nullptr, q, k, v, o, lse, o_f32, dout, dq, dk, dv, cu_q, cu_k, batch, max_q,
+  return attn_bwd_ex(nullptr, nullptr, q, k, v, o, lse, o_f32, dout, dq, dk, dv, cu_q, cu_k, batch, max_q,
                      max_k, total_q, total_k, hq, hkv, d, scale, mask, window, bias_slopes, dtype,
                      workspace, workspace_bytes, stream);
 }
 
-attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *k,
+attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q, const void *k,
                         const void *v, const void *o, const float *lse, const float *o_f32,
                         const void *dout, void *dq, void *dk, void *dv, const int32_t *cu_q,
                         const int32_t *cu_k, int batch, int max_q, int max_k, int total_q,
@@ -276,6 +294,11 @@ attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *
   if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
   if (total_q > 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_ERR_INVALID_ARG;
   if (total_k > 0 && (!k || !v || !dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  {  // a malformed bias tensor is an argument error before the workspace is looked at
+    const float *bd;
+    long long b0, b1, b2;
+    if (!pick_btab(bias, &bd, &b0, &b1, &b2)) return ATTN_ERR_INVALID_ARG;
+  }
   size_t need = attn_bwd_workspace_size(batch, max_q, max_k, total_q, total_k, hq, hkv, d, dtype);
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_INVALID_ARG;
@@ -289,6 +312,7 @@ attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *
   p.mask = mask;
   p.window = window;
   p.slopes = bias_slopes;
+  if (!pick_btab(bias, &p.btab, &p.bss, &p.bhs, &p.brs)) return ATTN_ERR_INVALID_ARG;
   const int elem = dtype == ATTN_DTYPE_FP32 ? 4 : 2;
   if (!pick_strides(strides ? strides->q : nullptr, hq, d, elem, &p.sq) ||
       !pick_strides(strides ? strides->k : nullptr, hkv, d, elem, &p.sk) ||
@@ -325,7 +349,7 @@ attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(dout);
   const bool tc = dtype == ATTN_DTYPE_BF16 && kTensorCorePath && total_k > 0 && total_q > 0 &&
-                  (mis & 15) == 0;
+                  (mis & 15) == 0 && !p.btab;
   if (tc) {
     p.q16 = ws + wl.q16;
     p.do16 = ws + wl.do16;
@@ -336,8 +360,8 @@ attn_status attn_bwd_ex(const attn_strides *strides, const void *q, const void *
     if (ce == cudaSuccess) ce = launch_bwd_tc(p, cs, desc, sizeof(desc));
   } else {
     if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);
-    snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d",
-             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d);
+    snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d%s",
+             dtype == ATTN_DTYPE_FP32 ? "fp32" : "bf16", d, p.btab ? "_btab" : "");
   }
   set_plan(desc);
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
   const int kend = key_end(g.mask, i, g.nq, g.nk);
   const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
   const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
+  const float *brow = btab_row(p.btab, p.bss, p.bhs, p.brs, s, h, i);  // explicit bias row
   const T *kb = reinterpret_cast<const T *>(p.k) + toff(p.sk, g.k0, hk) + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + toff(p.sv, g.k0, hk) + lane * E;
   const size_t kstride = (size_t)p.sk.ts, vstride = (size_t)p.sv.ts;  // one key to the next
@@ -185,7 +186,9 @@ __global__ void __launch_bounds__(128) bwd_dq_simt_kernel(BwdParams p) {
       ps += qf[e] * kf[e];
       pd += dof[e] * Elem<T>::to_f(vb[j * vstride + e]);
     }
-    const float sc = warp_sum(ps) + pos_bias2(slope2, bound, j), dpij = warp_sum(pd);
+    const float sc = warp_sum(ps) + pos_bias2(slope2, bound, j) +
+                     (brow ? __ldg(brow + j) * kLog2e : 0.f),
+                dpij = warp_sum(pd);
     const float pij = fast_exp2(sc - lse2);
     const float ds = pij * (dpij - D_i);
 #pragma unroll
@@ -237,7 +240,9 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
         ps += qf[e] * kf[e];
         pd += dof[e] * vf[e];
       }
-      const float sc = warp_sum(ps) + pos_bias2(slope2, (float)(i + off), j),
+      const float *brow = btab_row(p.btab, p.bss, p.bhs, p.brs, s, h, i);
+      const float sc = warp_sum(ps) + pos_bias2(slope2, (float)(i + off), j) +
+                       (brow ? __ldg(brow + j) * kLog2e : 0.f),
                   dpij = warp_sum(pd);
       const float lse2 = p.lse2[(size_t)h * p.total_q + t];
       const float D_i = p.delta[(size_t)h * p.total_q + t];

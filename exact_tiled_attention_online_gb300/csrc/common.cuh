@@ -168,6 +168,14 @@ __device__ __forceinline__ float pos_bias2(float slope2, float dist0, int e) {
   return -slope2 * fabsf(dist0 - (float)e);
 }
 
+// Row pointer into an explicit bias tensor for (sequence s, query head h,
+// in-sequence row i): entry j of the row is the bias of key j, in natural-log
+// units of the scaled logit.  NULL without a tensor.
+__device__ __forceinline__ const float *btab_row(const float *btab, long long bss, long long bhs,
+                                                 long long brs, int s, int h, int i) {
+  return btab ? btab + (long long)s * bss + (long long)h * bhs + (long long)i * brs : nullptr;
+}
+
 // ---------------------------------------------------------------------------
 // Device error flag: the first error code sticks until the host clears it.
 // ---------------------------------------------------------------------------
@@ -221,6 +229,8 @@ struct FwdParams {
   int mask;
   int window;             // > 0: bounded window (causal kinds only)
   const float *slopes;    // [hq] linear positional bias slopes, or NULL
+  const float *btab;      // explicit bias tensor, or NULL
+  long long bss, bhs, brs;  // its sequence, head and row strides (elements)
   Strides sq, sk, sv, so;  // layouts of q, k, v, o
   int *err;
   // split-KV partial outputs (NULL when the plan writes o/lse directly)
@@ -239,6 +249,8 @@ struct BwdParams {
   int mask;
   int window;             // > 0: bounded window (causal kinds only)
   const float *slopes;    // [hq] linear positional bias slopes, or NULL
+  const float *btab;      // explicit bias tensor, or NULL
+  long long bss, bhs, brs;  // its sequence, head and row strides (elements)
   Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;  // layouts of the eight [T, H, d] tensors
   int *err;
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i

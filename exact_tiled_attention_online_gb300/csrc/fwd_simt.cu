@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
   // positional bias: key j is |bound - j| away from the row's causal bound
   const float slope2 = p.slopes ? __ldg(p.slopes + h) * kLog2e : 0.f;
   const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));
+  // explicit bias tensor row (natural-log units), or NULL
+  const float *brow = btab_row(p.btab, p.bss, p.bhs, p.brs, s, h, i);
   float m = -INFINITY, l = 0.f;
   const T *kb = reinterpret_cast<const T *>(p.k) + toff(p.sk, g.k0, hk) + lane * E;
   const T *vb = reinterpret_cast<const T *>(p.v) + toff(p.sv, g.k0, hk) + lane * E;
@@ -46,7 +48,11 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; e++) part += qf[e] * Elem<T>::to_f(kb[j * kstride + e]);
-    const float sc = warp_sum(part) + pos_bias2(slope2, bound, j);  // logit in log2 units
+    float sc = warp_sum(part) + pos_bias2(slope2, bound, j);  // logit in log2 units
+    if (brow) {
+      sc += __ldg(brow + j) * kLog2e;
+      if (sc == -INFINITY) continue;  // masked by the tensor: P = 0, state unchanged
+    }
     const float m_new = fmaxf(m, sc);
     const float alpha = fast_exp2(m - m_new);
     const float pj = fast_exp2(sc - m_new);
@@ -56,7 +62,8 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     m = m_new;
   }
   T *op = reinterpret_cast<T *>(p.o) + toff(p.so, t, h) + lane * E;
-  const float inv = kend > kbeg ? 1.f / l : 0.f;
+  // l > 0 iff some key had a finite logit (the largest contributes 1)
+  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; e++) op[e] = Elem<T>::from_f(acc[e] * inv);
   if (p.o_f32) {
@@ -65,7 +72,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(FwdParams p) {
     for (int e = 0; e < E; e++) of[e] = acc[e] * inv;
   }
   if (p.lse && lane == 0)
-    p.lse[(size_t)h * p.total_q + t] = kend > kbeg ? (m + log2f(l)) * kLn2 : -INFINITY;
+    p.lse[(size_t)h * p.total_q + t] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t st) {

@@ -107,6 +107,23 @@ def bias_slopes(hq: int) -> torch.Tensor:
     return torch.tensor([2.0 ** (-8.0 * (h + 1) / hq) for h in range(hq)], dtype=torch.float32)
 
 
+def bias_tensor(batch: int, hb: int, rows: int, keys: int, seed: int, p_masked: float = 0.2,
+                dead_rows: int = 0) -> torch.Tensor:
+    """A seeded explicit bias tensor [batch, hb, rows, keys] (fp32, CPU):
+    N(0, 1) entries, about ``p_masked`` of them -inf, and in addition
+    ``dead_rows`` random (sequence, head, row) triples masked over every key.
+    Use ``batch`` or ``hb`` = 1 for a tensor that broadcasts."""
+    g = torch.Generator().manual_seed(seed)
+    b = torch.randn((batch, hb, rows, keys), generator=g, dtype=torch.float32)
+    b[torch.rand(b.shape, generator=g) < p_masked] = float("-inf")
+    for _ in range(dead_rows):
+        s = int(torch.randint(batch, (1,), generator=g))
+        h = int(torch.randint(hb, (1,), generator=g))
+        i = int(torch.randint(rows, (1,), generator=g))
+        b[s, h, i, :] = float("-inf")
+    return b
+
+
 def cu_seqlens(lengths: Sequence[int]) -> torch.Tensor:
     out = [0]
     for n in lengths:

@@ -155,11 +155,34 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
                      void *stream);
 
 /*
- * attn_fwd with the layouts of q, k, v and o given by `strides` (NULL: the
- * contiguous layouts, exactly attn_fwd).  Same results; ATTN_ERR_INVALID_ARG
- * for a stride that breaks the rules above.
+ * An explicit bias tensor added to the logits ("attention-algorithm-error-
+ * and-complexity-tests", third paragraph: bias and mask terms enter the
+ * logits before the softmax).  Entry (sequence s, query head h, in-sequence
+ * row i, in-sequence key j) is
+ *   data[s * seq_stride + h * head_stride + i * row_stride + j]
+ * (fp32, element strides, >= 0; a stride of 0 broadcasts, so a
+ * [B, Hq, max_seqlen_q, max_seqlen_k] tensor or any of its broadcasts over
+ * sequences or heads fits), in the units of the scaled logits: the logit of
+ * an allowed pair is scale * q.k + positional bias + entry.  An entry of
+ * -inf removes the pair (an explicit mask); a row without any finite logit
+ * is an empty row (O = 0, lse = -inf).  +inf and NaN entries are not
+ * allowed.  The caller owns the device memory, which must cover every entry
+ * of every allowed pair and stay valid until the call's kernels finish.
  */
-attn_status attn_fwd_ex(const attn_strides *strides, const void *q,
+typedef struct {
+  const float *data;
+  int64_t seq_stride, head_stride, row_stride;
+} attn_bias_tensor;
+
+/*
+ * attn_fwd with the layouts of q, k, v and o given by `strides` (NULL: the
+ * contiguous layouts) and an optional explicit bias tensor `bias` (NULL:
+ * none; both NULL is exactly attn_fwd).  Same results; ATTN_ERR_INVALID_ARG
+ * for a stride that breaks the rules above, a negative bias stride or a bias
+ * without data.  Calls with a bias tensor run on the CUDA-core kernels (one
+ * warp per query row and head).
+ */
+attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q,
                         const void *k, const void *v, void *o, float *lse,
                         float *o_f32, const int32_t *cu_seqlens_q,
                         const int32_t *cu_seqlens_k, int batch,
@@ -212,10 +235,12 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
 
 /*
  * attn_bwd with the layouts of q, k, v, o, dout, dq, dk and dv given by
- * `strides` (NULL: contiguous, exactly attn_bwd).  The workspace size does
- * not depend on the layouts (its fp16 copies are contiguous).
+ * `strides` (NULL: contiguous) and the forward's explicit bias tensor `bias`
+ * (NULL: none; both NULL is exactly attn_bwd), rebuilt in the recomputed
+ * logits.  The workspace size does not depend on either.  With a bias tensor
+ * the CUDA-core backward runs.
  */
-attn_status attn_bwd_ex(const attn_strides *strides, const void *q,
+attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q,
                         const void *k, const void *v, const void *o,
                         const float *lse, const float *o_f32, const void *dout,
                         void *dq, void *dk, void *dv,

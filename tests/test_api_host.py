@@ -103,10 +103,26 @@ def test_strided_entry_rejects_bad_strides(lib):
     s.v[0], s.v[1] = 64, 64
     s.o[0], s.o[1] = 128, 64
     s.q[0], s.q[1] = 3, 64    # invalid: 6 bytes
-    lib.attn_fwd_ex.argtypes = [ctypes.POINTER(attn.AttnStrides)] + lib.attn_fwd.argtypes
+    lib.attn_fwd_ex.argtypes = ([ctypes.POINTER(attn.AttnStrides), ctypes.POINTER(attn.AttnBiasTensor)]
+                                + lib.attn_fwd.argtypes)
     args = dict(q=1, k=1, v=1, o=1, lse=1, o_f32=None, cu_q=1, cu_k=1, batch=1, max_q=4,
                 max_k=4, total_q=4, total_k=4, hq=2, hkv=1, d=64, scale=0.125, mask=1, window=0,
                 slopes=None, dtype=0, ws=None, ws_bytes=0, stream=None)
-    assert lib.attn_fwd_ex(ctypes.byref(s), *args.values()) == 1
+    assert lib.attn_fwd_ex(ctypes.byref(s), None, *args.values()) == 1
     s.q[0] = 0  # only positive strides
-    assert lib.attn_fwd_ex(ctypes.byref(s), *args.values()) == 1
+    assert lib.attn_fwd_ex(ctypes.byref(s), None, *args.values()) == 1
+
+
+def test_bias_tensor_rejections(lib):
+    """A bias tensor without data, with a negative stride or misaligned data
+    is refused before any launch."""
+    ex = [ctypes.POINTER(attn.AttnStrides), ctypes.POINTER(attn.AttnBiasTensor)]
+    lib.attn_fwd_ex.argtypes = ex + lib.attn_fwd.argtypes
+    lib.attn_bwd_ex.argtypes = ex + lib.attn_bwd.argtypes
+    fargs = [1, 1, 1, 1, 1, None, 1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.125, 1, 0, None, 0, None, 0, None]
+    bargs = [1] * 10 + [1, 1, 1, 4, 4, 4, 4, 2, 1, 64, 0.125, 1, 0, None, 0, None, 0, None]
+    for data, strides in ((None, (0, 0, 4)), (256, (0, -1, 4)), (256, (-4, 0, 4)),
+                          (256, (0, 0, -4)), (258, (0, 0, 4))):
+        b = attn.AttnBiasTensor(data, *strides)
+        assert lib.attn_fwd_ex(None, ctypes.byref(b), *fargs) == 1
+        assert lib.attn_bwd_ex(None, ctypes.byref(b), *bargs) == 1

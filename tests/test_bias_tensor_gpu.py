@@ -1,0 +1,96 @@
+"""Explicit bias tensor on the GPU against the fp64 oracle, forward and
+backward: entries added to the scaled logits, -inf entries masking pairs,
+rows with no finite logit empty ("attention-algorithm-error-and-complexity-
+tests", third paragraph; "causal-mask-and-ragged-sequence-layouts", sixth
+paragraph: the backward rebuilds the same terms)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_online_gb300 import attn, inputs
+from tests import compare
+
+pytestmark = pytest.mark.gpu
+TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
+
+
+def run(x, bias, slopes=None):
+    w = x["workload"]
+    d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
+    b = bias.cuda()
+    sl = None if slopes is None else slopes.cuda()
+    o, lse, o32 = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
+                           w.max_k, w.mask, w.scale, want_o_f32=True, window=w.window,
+                           bias_slopes=sl, bias=b)
+    fplan = attn.last_plan()
+    dq, dk, dv = attn.bwd(d["q"], d["k"], d["v"], o, lse, d["dout"], d["cu_seqlens_q"],
+                          d["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, o_f32=o32,
+                          window=w.window, bias_slopes=sl, bias=b)
+    bplan = attn.last_plan()
+    torch.cuda.synchronize()
+    assert attn.get_device_error() == 0
+    return (o, lse, dq, dk, dv), (fplan, bplan)
+
+
+CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask, window, bias batch / heads broadcast, slopes)
+    ("bf16_tl_full", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, False, False),
+    ("bf16_br_head_bcast", (40, 9), (100, 30), 4, 1, 64, "bf16", BR, 0, True, False),
+    ("bf16_none_slopes", (50, 77), (70, 20), 4, 4, 128, "bf16", NONE, 0, False, True),
+    ("bf16_tl_window", (90, 33), None, 4, 2, 64, "bf16", TL, 9, False, False),
+    ("fp32_br", (37, 70), (50, 70), 4, 2, 64, "fp32", BR, 0, True, True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_bias_tensor_fwd_bwd(case):
+    name, lq, lk, hq, hkv, d, dt, mask, window, bcast, with_slopes = case
+    w = inputs.custom(name, lq, lk or lq, hq, hkv, d, dt, mask, seed=61, backward=True,
+                      v_shift_per_seq=2.0, window=window)
+    x = inputs.make_inputs(w)
+    bias = inputs.bias_tensor(1 if bcast else w.batch, 1 if bcast else hq, w.max_q, w.max_k,
+                              seed=62, dead_rows=3)
+    slopes = inputs.bias_slopes(hq) if with_slopes else None
+    (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias, slopes)
+    assert "_btab" in fplan and "_btab" in bplan, (fplan, bplan)
+    rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], w.scale, mask, window=window,
+                                         slopes=None if slopes is None else slopes.double().numpy(),
+                                         bias=bias)
+    tol = {} if dt == "bf16" else dict(atol=1e-4, rtol=1e-4)
+    compare.check_close("o", o, ro, **tol)
+    compare.check_lse("lse", lse, rlse)
+    compare.check_close("dq", dq, rdq, **tol)
+    compare.check_close("dk", dk, rdk, **tol)
+    compare.check_close("dv", dv, rdv, **tol)
+    # rows without a finite logit: O and dQ exactly zero
+    for h, t in np.argwhere(np.isneginf(rlse)):
+        assert np.all(compare.to_np(o)[t, h] == 0.0)
+        assert np.all(compare.to_np(dq)[t, h] == 0.0)
+
+
+def test_bias_tensor_broadcast_view_matches_materialised():
+    """A stride-0 view from ``expand`` gives bit for bit what the materialised
+    tensor gives."""
+    w = inputs.custom("bview", (30, 45), (30, 45), 4, 2, 64, "bf16", TL, seed=63, backward=True)
+    x = inputs.make_inputs(w)
+    small = inputs.bias_tensor(1, 1, w.max_q, w.max_k, seed=64)
+    view = small.expand(w.batch, 4, w.max_q, w.max_k)
+    got_v, _ = run(x, view)
+    got_m, _ = run(x, view.contiguous())
+    for a, b in zip(got_v, got_m):
+        assert torch.equal(a, b)
+
+
+def test_zero_bias_tensor_matches_no_bias_oracle():
+    """A zero tensor changes nothing: the result meets the oracle without bias."""
+    w = inputs.custom("bzero", (70, 3), (70, 20), 2, 1, 128, "bf16", BR, seed=65, backward=True)
+    x = inputs.make_inputs(w)
+    (o, lse, dq, dk, dv), _ = run(x, torch.zeros((1, 1, w.max_q, w.max_k)))
+    rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], w.scale, BR)
+    compare.check_close("o", o, ro)
+    compare.check_lse("lse", lse, rlse)
+    compare.check_close("dq", dq, rdq)
+    compare.check_close("dk", dk, rdk)
+    compare.check_close("dv", dv, rdv)

@@ -9,7 +9,10 @@ that are already resident in HBM:
   train_fwd_bwd   forward + backward, B=2, N=8192, 16/4 heads, d=128;
   varlen_causal   packed ragged forward, 12 sequences, 16 heads, d=128;
   window_prefill  the gqa_prefill shape under a bounded 1024-key causal window;
-  bias_prefill    the gqa_prefill shape with a linear positional bias.
+  bias_prefill    the gqa_prefill shape with a linear positional bias;
+  bias_tensor_prefill  causal forward, B=2, N=1024, 8/2 heads, with an
+                  explicit [B, Hq, N, N] bias tensor (CUDA-core kernel, so its
+                  roofline is the fp32 FMA rate: bound "alu").
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -94,6 +97,13 @@ def decode_bytes(w) -> float:
     kv = 2 * w.total_k * w.hkv * w.d * 2
     q_o = 2 * w.total_q * w.hq * w.d * 2
     return float(kv + q_o + w.total_q * w.hq * 4)
+
+
+def alu_peak_tflops(peaks) -> float:
+    """fp32 FMA peak of the whole GPU: SMs x 128 lanes x 2 flops x clock."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() \
+        else 152
+    return sms * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
 
 
 def load_peaks():
@@ -208,19 +218,22 @@ class Runner:
                                           w.hkv, w.d, attn.DTYPE_BF16)
             self.bws = torch.empty(max(bws, 1), dtype=torch.uint8, device=device)
         self.slopes = inputs.bias_slopes(w.hq).to(device) if w.bias else None
+        self.btab_cpu = inputs.bias_tensor(w.batch, w.hq, w.max_q, w.max_k, w.seed + 1) \
+            if w.bias_tensor else None
+        self.btab = None if self.btab_cpu is None else self.btab_cpu.to(device)
         self.plans = []
 
     def run(self):
         a, w, x = self.attn, self.w, self.x
         a.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q, w.max_k,
               w.mask, w.scale, out=self.o, lse=self.lse, workspace=self.ws, o_f32=self.o32,
-              window=w.window, bias_slopes=self.slopes)
+              window=w.window, bias_slopes=self.slopes, bias=self.btab)
         plans = [a.last_plan()]
         if w.backward:
             a.bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["dout"], x["cu_seqlens_q"],
                   x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, dq=self.dq, dk=self.dk,
                   dv=self.dv, workspace=self.bws, o_f32=self.o32, window=w.window,
-                  bias_slopes=self.slopes)
+                  bias_slopes=self.slopes, bias=self.btab)
             plans.append(a.last_plan())
         self.plans = plans
 
@@ -245,7 +258,8 @@ def validate(r: Runner, n_rows=24):
     host = {k: (t.cpu() if hasattr(t, "cpu") else t) for k, t in r.x.items()}
     o_ref, l_ref = oracle.fwd(host["q"], host["k"], host["v"], host["cu_seqlens_q"],
                               host["cu_seqlens_k"], w.scale, w.mask, rows=rows, window=w.window,
-                              slopes=inputs.bias_slopes(w.hq).double().numpy() if w.bias else None)
+                              slopes=inputs.bias_slopes(w.hq).double().numpy() if w.bias else None,
+                              bias=r.btab_cpu)
     on = r.o.double().cpu().numpy()[rows[:, 0], rows[:, 1]]
     ln = r.lse.double().cpu().numpy()[rows[:, 1], rows[:, 0]]
     err = np.abs(on - o_ref)
@@ -275,7 +289,7 @@ def time_gpu(args, rank, world, device):
         raise RuntimeError("device error flag set during the first run")
     validated = {}
     if rank == 0 and not args.skip_validate:
-        for n in ("gqa_prefill", "varlen_causal"):
+        for n in ("gqa_prefill", "varlen_causal", "bias_tensor_prefill"):
             if n in runners:
                 validated[n] = validate(runners[n])
 
@@ -464,7 +478,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads",
                     default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
-                            "window_prefill,bias_prefill")
+                            "window_prefill,bias_prefill,bias_tensor_prefill")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -513,6 +527,12 @@ def main():
             peak = peaks["hbm_gbs"]
             roof = {"bound": "hbm", "achieved": rate(d["work"], "GB/s", ms), "peak": peak,
                     "unit": "GB/s"}
+        elif "_simt" in " ".join(d["plan"]):
+            # CUDA-core kernels: the fp32 FMA rate, 128 lanes x 2 flops per SM
+            # and cycle at the maximum SM clock
+            peak = alu_peak_tflops(peaks)
+            roof = {"bound": "alu", "achieved": rate(d["work"], "TFLOP/s", ms), "peak": peak,
+                    "unit": "TFLOP/s"}
         else:
             peak = peaks["bf16_tflops"]
             roof = {"bound": "tensor", "achieved": rate(d["work"], "TFLOP/s", ms), "peak": peak,

@@ -15,6 +15,8 @@ Recipe (the pages fix no generator, so this is a stated choice):
     layouts", fifth paragraph);
   * every ragged batch is packed back to back and addressed by int32
     cumulative lengths ``cu_seqlens = [0, L0, L0 + L1, ...]``.
+  * an explicit bias tensor is drawn by its own generator (seed + 1) as
+    fp32 N(0, 1) entries with about a fifth of them set to -inf.
 """
 from __future__ import annotations
 
@@ -46,6 +48,7 @@ class Workload:
     v_shift_per_seq: float = 0.0
     window: int = 0  # > 0: bounded causal window of that many keys per row
     bias: bool = False  # linear positional bias with slopes bias_slopes(hq)
+    bias_tensor: bool = False  # explicit bias tensor bias_tensor(B, hq, max_q, max_k, seed + 1)
 
     @property
     def batch(self) -> int:
@@ -97,6 +100,9 @@ WORKLOADS = {
     # the prefill shape with a linear positional bias on every logit
     "bias_prefill": Workload("bias_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
                              128, "bf16", MASK_TOP_LEFT, 1002, bias=True),
+    # an explicit [B, Hq, N, N] bias tensor (a fifth of its entries -inf)
+    "bias_tensor_prefill": Workload("bias_tensor_prefill", (1024,) * 2, (1024,) * 2, 8, 2,
+                                    128, "bf16", MASK_TOP_LEFT, 1005, bias_tensor=True),
 }
 
 

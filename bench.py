@@ -10,9 +10,8 @@ that are already resident in HBM:
   varlen_causal   packed ragged forward, 12 sequences, 16 heads, d=128;
   window_prefill  the gqa_prefill shape under a bounded 1024-key causal window;
   bias_prefill    the gqa_prefill shape with a linear positional bias;
-  bias_tensor_prefill  causal forward, B=2, N=1024, 8/2 heads, with an
-                  explicit [B, Hq, N, N] bias tensor (CUDA-core kernel, so its
-                  roofline is the fp32 FMA rate: bound "alu").
+  bias_tensor_prefill  the gqa_prefill shape with an explicit [B, 1, N, N]
+                  bias tensor shared by the heads.
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -218,7 +217,7 @@ class Runner:
                                           w.hkv, w.d, attn.DTYPE_BF16)
             self.bws = torch.empty(max(bws, 1), dtype=torch.uint8, device=device)
         self.slopes = inputs.bias_slopes(w.hq).to(device) if w.bias else None
-        self.btab_cpu = inputs.bias_tensor(w.batch, w.hq, w.max_q, w.max_k, w.seed + 1) \
+        self.btab_cpu = inputs.bias_tensor(w.batch, 1, w.max_q, w.max_k, w.seed + 1) \
             if w.bias_tensor else None
         self.btab = None if self.btab_cpu is None else self.btab_cpu.to(device)
         self.plans = []

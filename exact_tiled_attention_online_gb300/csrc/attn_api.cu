@@ -219,7 +219,14 @@ attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
   }
   TcPlan plan =
       choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype, sm_count());
-  if (p.btab) plan.kind = PLAN_SIMT;  // the bias tensor is read by the CUDA-core kernel only
+  if (p.btab) {
+    // bf16 with a positive scale and no slopes: the prefill kernel's bias-tensor
+    // instance (the bias rides on the raw scores); otherwise the CUDA-core kernel
+    const bool tab_tc = plan.kind != PLAN_SIMT && scale > 0.f && !bias_slopes;
+    plan.kind = tab_tc ? PLAN_TC : PLAN_SIMT;
+    plan.pack = false;
+    plan.n_splits = 1;
+  }
   if (plan.kind != PLAN_SIMT) {
     // TMA needs 16-byte aligned tensors; with no keys at all every row is
     // empty and the CUDA-core kernel writes the zeros and -inf directly.

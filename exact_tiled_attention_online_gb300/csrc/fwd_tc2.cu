@@ -67,6 +67,7 @@ struct Tc2Args {
 struct Bars2 {
   uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];  // [tile A, tile B]
+  uint64_t b_full[2];  // kTab: the next tile's bias is in the tile's S columns
   uint32_t tmem_base;
   int abort;
 };
@@ -85,8 +86,11 @@ __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, 
 // output is an exact convex combination of V rows (wanted when the caller
 // keeps that output for the backward); without it O is normalised by the
 // fp32 sum.  kBias: add the linear positional bias (with kPosScale false:
-// the bias must be in the logits before the max).
-template <int D, bool kPosScale, bool kRoundedSum, bool kBias>
+// the bias must be in the logits before the max).  kTab: add an explicit
+// bias tensor, which the softmax warps write (divided by the positive scale)
+// into the tile's S columns before Q K^T accumulates onto it, so the scores
+// arrive biased and the softmax itself is unchanged.
+template <int D, bool kPosScale, bool kRoundedSum, bool kBias, bool kTab>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&b->v_empty[s], 1);
       mbar_init(&b->s_full[s], 1);
       mbar_init(&b->p_full[s], 128);
+      mbar_init(&b->b_full[s], 128);
       mbar_init(&b->pv_done[s], 1);
     }
     b->abort = 0;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint64_t off = (uint64_t)((((kk >> 2) * L::kChunk) + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, (kTab || kk > 0) ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
@@ -213,18 +218,27 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // s_full / p_full / pv_done barriers.
       auto in_a = [&](int n) { return n >= lo_a && n < hi_a; };
       auto in_b = [&](int n) { return n >= lo_b && n < hi_b; };
+      // kTab: Q K^T of tile X's c-th product accumulates onto the bias its
+      // softmax warps stored, announced by phase c of b_full[X]
       bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
       if (ok) {
-        tc_fence_after();
         if (in_a(0)) {
-          issue_qk(0, 0);
-          mma_commit(&b->s_full[0]);
+          if (kTab && !(ok = wait2(b, &b->b_full[0], 0, p.err))) {
+          } else {
+            tc_fence_after();
+            issue_qk(0, 0);
+            mma_commit(&b->s_full[0]);
+          }
         }
-        if (in_b(0)) {
-          issue_qk(1, 0);
-          mma_commit(&b->s_full[1]);
+        if (ok && in_b(0)) {
+          if (kTab && !(ok = wait2(b, &b->b_full[1], 0, p.err))) {
+          } else {
+            tc_fence_after();
+            issue_qk(1, 0);
+            mma_commit(&b->s_full[1]);
+          }
         }
-        mma_commit(&b->k_empty[0]);
+        if (ok) mma_commit(&b->k_empty[0]);
       }
       for (int n = 0; ok && n < N; n++) {
         const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
@@ -237,7 +251,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
           issue_pv(0, st, n > lo_a);
           mma_commit(&b->pv_done[0]);
         }
-        if (in_a(n1)) {
+        // kTab: tile A's next Q K^T waits for its bias, which waits for
+        // P_A V: tile B's P V goes first
+        if (!kTab && in_a(n1)) {
           if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           k1_ready = true;
           tc_fence_after();
@@ -252,8 +268,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
           mma_commit(&b->pv_done[1]);
         }
         mma_commit(&b->v_empty[st]);
+        if (kTab && in_a(n1)) {
+          if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
+          k1_ready = true;
+          if (!(ok = wait2(b, &b->b_full[0], (n1 - lo_a) & 1, p.err))) break;
+          tc_fence_after();
+          issue_qk(0, st1);
+          mma_commit(&b->s_full[0]);
+        }
         if (in_b(n1)) {
           if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
+          if (kTab && !(ok = wait2(b, &b->b_full[1], (n1 - lo_b) & 1, p.err))) break;
           tc_fence_after();
           issue_qk(1, st1);
           mma_commit(&b->s_full[1]);
@@ -281,12 +306,55 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const float c2 = p.scale_log2;
     const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
     static_assert(!(kBias && kPosScale), "the bias needs the logits before the max");
+    static_assert(!kTab || (kPosScale && !kBias), "the tensor bias rides on the raw scores");
     const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
     // causal mask and positive scale: the bias is linear over every allowed key
     const bool bias_linear = g.mask != ATTN_MASK_NONE && c2 > 0.f;
     const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
+    // kTab: this row's bias entries for key tile n, divided by the positive
+    // scale (so that c2 times the accumulated score is the biased logit in
+    // log2 units), into the tile's S columns; keys past the sequence and rows
+    // past it get 0 (their lanes are masked or never stored).
+    const float *brow = kTab && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, h, i) : nullptr;
+    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
+    // the loads are issued before the wait that gates the store, so their
+    // latency overlaps it
+    auto load_bias = [&](int n, uint32_t (&bv)[kTileKeys]) {
+      const int j0 = n * kTileKeys;
+      const bool vec = brow && j0 + kTileKeys <= g.nk &&
+                       ((reinterpret_cast<uintptr_t>(brow + j0) & 15) == 0);
+      if (vec) {
+#pragma unroll
+        for (int e = 0; e < kTileKeys; e += 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4 *>(brow + j0 + e));
+          bv[e] = __float_as_uint(f.x * inv_scale);
+          bv[e + 1] = __float_as_uint(f.y * inv_scale);
+          bv[e + 2] = __float_as_uint(f.z * inv_scale);
+          bv[e + 3] = __float_as_uint(f.w * inv_scale);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kTileKeys; e++) {
+          const int j = j0 + e;
+          bv[e] = __float_as_uint(brow && j < g.nk ? __ldg(brow + j) * inv_scale : 0.f);
+        }
+      }
+    };
+    auto store_bias = [&](const uint32_t (&bv)[kTileKeys]) {
+#pragma unroll
+      for (int c = 0; c < kTileKeys / 32; c++)
+        tmem_st32(s_col + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(bv + 32 * c));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&b->b_full[x]);
+    };
+    if (kTab && n_mine > 0) {
+      uint32_t bv[kTileKeys];
+      load_bias(kr.n_begin, bv);
+      store_bias(bv);
+    }
     for (int it = 0; it < n_mine; it++) {
       const int n = kr.n_begin + it;  // key tile in the sequence
       ok = wait2(b, &b->s_full[x], it & 1, p.err);
@@ -396,6 +464,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tmem_wait_st();  // P (S columns [64, 128)) and any rescaled O are in place
       tc_fence_before();
       mbar_arrive(&b->p_full[x]);
+      if (kTab && it + 1 < n_mine) {
+        // the next tile's bias may overwrite S once P V has read P
+        uint32_t bv[kTileKeys];
+        load_bias(n + 1, bv);
+        ok = wait2(b, &b->pv_done[x], it & 1, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        store_bias(bv);
+      }
     }
     if (ok && n_mine > 0) {
       ok = wait2(b, &b->pv_done[x], (n_mine - 1) & 1, p.err);
@@ -448,20 +528,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-template <int D, bool kPos, bool kRs, bool kBias>
+template <int D, bool kPos, bool kRs, bool kBias, bool kTab = false>
 cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                     const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs, kBias>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs, kBias, kTab>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Layout2<D>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc2_kernel<D, kPos, kRs, kBias><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -469,6 +549,9 @@ template <int D>
 cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
                       const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
   const bool pos = a.p.scale_log2 > 0.f, rs = a.p.o_f32 != nullptr;
+  if (a.p.btab)  // the caller routes a bias tensor here only with a positive scale, no slopes
+    return rs ? launch2<D, true, true, false, true>(a, mq, mk, mv, ctas, st)
+              : launch2<D, true, false, false, true>(a, mq, mk, mv, ctas, st);
   if (a.p.slopes) return rs ? launch2<D, false, true, true>(a, mq, mk, mv, ctas, st)
                             : launch2<D, false, false, true>(a, mq, mk, mv, ctas, st);
   if (pos) return rs ? launch2<D, true, true, false>(a, mq, mk, mv, ctas, st)
@@ -493,7 +576,8 @@ cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size
     return cudaErrorInvalidValue;
   const long long ctas = (long long)a.n_pairs * p.hq * p.batch;
   if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
-  snprintf(desc, desc_len, "fwd_tc2_d%d ctas=%lld rows_per_cta=256", p.d, ctas);
+  snprintf(desc, desc_len, "fwd_tc2_d%d%s ctas=%lld rows_per_cta=256", p.d, p.btab ? "_btab" : "",
+           ctas);
   if (ctas == 0) return cudaSuccess;
   if (p.d == 64) return launch2_d<64>(a, mq, mk, mv, (unsigned)ctas, st);
   return launch2_d<128>(a, mq, mk, mv, (unsigned)ctas, st);

@@ -48,7 +48,7 @@ class Workload:
     v_shift_per_seq: float = 0.0
     window: int = 0  # > 0: bounded causal window of that many keys per row
     bias: bool = False  # linear positional bias with slopes bias_slopes(hq)
-    bias_tensor: bool = False  # explicit bias tensor bias_tensor(B, hq, max_q, max_k, seed + 1)
+    bias_tensor: bool = False  # explicit bias tensor bias_tensor(B, 1, max_q, max_k, seed + 1)
 
     @property
     def batch(self) -> int:
@@ -100,9 +100,10 @@ WORKLOADS = {
     # the prefill shape with a linear positional bias on every logit
     "bias_prefill": Workload("bias_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
                              128, "bf16", MASK_TOP_LEFT, 1002, bias=True),
-    # an explicit [B, Hq, N, N] bias tensor (a fifth of its entries -inf)
-    "bias_tensor_prefill": Workload("bias_tensor_prefill", (1024,) * 2, (1024,) * 2, 8, 2,
-                                    128, "bf16", MASK_TOP_LEFT, 1005, bias_tensor=True),
+    # the prefill shape with an explicit [B, 1, N, N] bias tensor shared by the
+    # heads (a fifth of its entries -inf)
+    "bias_tensor_prefill": Workload("bias_tensor_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
+                                    128, "bf16", MASK_TOP_LEFT, 1002, bias_tensor=True),
 }
 
 

@@ -11,7 +11,9 @@ that are already resident in HBM:
   window_prefill  the gqa_prefill shape under a bounded 1024-key causal window;
   bias_prefill    the gqa_prefill shape with a linear positional bias;
   bias_tensor_prefill  the gqa_prefill shape with an explicit [B, 1, N, N]
-                  bias tensor shared by the heads.
+                  bias tensor shared by the heads;
+  bias_tensor_train    the train_fwd_bwd shape with such a tensor, forward +
+                  backward.
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -276,7 +278,7 @@ def time_gpu(args, rank, world, device):
     names = [n.strip() for n in args.workloads.split(",") if n.strip()]
     runners = {}
     for n in names:
-        big = n.startswith("decode") or n == "train_fwd_bwd"
+        big = n.startswith("decode") or n in ("train_fwd_bwd", "bias_tensor_train")
         runners[n] = Runner(n, device, device if big else "cpu", args.batch_div)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
@@ -477,7 +479,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads",
                     default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
-                            "window_prefill,bias_prefill,bias_tensor_prefill")
+                            "window_prefill,bias_prefill,bias_tensor_prefill,bias_tensor_train")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

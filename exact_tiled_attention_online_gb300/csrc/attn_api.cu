@@ -355,8 +355,10 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
   char desc[256];
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(dout);
+  // a bias tensor rides on the raw scores: tensor cores only with a positive
+  // scale and no slopes
   const bool tc = dtype == ATTN_DTYPE_BF16 && kTensorCorePath && total_k > 0 && total_q > 0 &&
-                  (mis & 15) == 0 && !p.btab;
+                  (mis & 15) == 0 && (!p.btab || (scale > 0.f && !bias_slopes));
   if (tc) {
     p.q16 = ws + wl.q16;
     p.do16 = ws + wl.do16;

@@ -70,6 +70,28 @@ __device__ __forceinline__ void math_group_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
+// N consecutive bias-tensor entries of one row from key j0 on, divided by the
+// positive scale (raw-score units: the score product accumulates onto them);
+// keys at or past nk, or no row, give 0.
+template <int N>
+__device__ __forceinline__ void load_bias_row(const float *brow, int j0, int nk, float inv_scale,
+                                              uint32_t (&bv)[N]) {
+  if (brow && j0 + N <= nk && (reinterpret_cast<uintptr_t>(brow + j0) & 15) == 0) {
+#pragma unroll
+    for (int e = 0; e < N; e += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4 *>(brow + j0 + e));
+      bv[e] = __float_as_uint(f.x * inv_scale);
+      bv[e + 1] = __float_as_uint(f.y * inv_scale);
+      bv[e + 2] = __float_as_uint(f.z * inv_scale);
+      bv[e + 3] = __float_as_uint(f.w * inv_scale);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; e++)
+      bv[e] = __float_as_uint(brow && j0 + e < nk ? __ldg(brow + j0 + e) * inv_scale : 0.f);
+  }
+}
+
 // ===========================================================================
 // dK, dV
 // ===========================================================================
@@ -101,12 +123,15 @@ struct BarsA {
   // gradient products done.  Few barriers keep the MMA thread's commits and
   // waits, which the tensor pipe's short issue queue does not hide, few.
   uint64_t kv_full, qdo_full[kStagesA], qdo_empty[kStagesA], st_full[2], ps_full[2], mm_done;
+  uint64_t b_full[2], s_free[2];  // kTab: bias stored in S^T buffer t / buffer t read by dV, dK
   uint32_t tmem_base;
   Sync sync;
 };
 
-// kBias: add the linear positional bias to the recomputed logits.
-template <int D, bool kBias>
+// kBias: add the linear positional bias to the recomputed logits.  kTab: an
+// explicit bias tensor; the math warps store a step's entries (over the
+// positive scale) into its S^T buffer and S^T = K Q^T accumulates onto them.
+template <int D, bool kBias, bool kTab>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -152,6 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b->ps_full[s], 256);
     }
     mbar_init(&b->mm_done, 1);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->b_full[s], 256);
+      mbar_init(&b->s_free[s], 1);
+    }
     b->sync.abort = 0;
     fence_mbar_init();
   }
@@ -206,12 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQm = smem_desc_sw128(sQ, kChunk64, 1024);
       const uint64_t dDOm = smem_desc_sw128(sDO, kChunk64, 1024);
       // S^T (or dP^T) = A_tile [128 keys x d] * B_tile [64 rows x d]^T
-      auto issue_st = [&](uint64_t da, uint64_t db, uint32_t col) {
+      // acc0: accumulate from the first K step on (onto a stored bias)
+      auto issue_st = [&](uint64_t da, uint64_t db, uint32_t col, bool acc0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint64_t oa = (uint64_t)((((kk >> 2) * kChunk128) + (kk & 3) * 32) >> 4);
           const uint64_t ob = (uint64_t)((((kk >> 2) * kChunk64) + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + col, da + oa, db + ob, idesc_s, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + col, da + oa, db + ob, idesc_s, (acc0 || kk > 0) ? 1u : 0u);
         }
       };
       // acc [128 keys x d] += A [128 keys x 64 rows] * B [64 rows x d], A in
@@ -224,11 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto qoff = [&](int s1) { return (uint64_t)((s1 * L::kQT) >> 4); };
       bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
-                wait_bar(&b->sync, &b->qdo_full[0], 0, p.err);
+                wait_bar(&b->sync, &b->qdo_full[0], 0, p.err) &&
+                (!kTab || wait_bar(&b->sync, &b->b_full[0], 0, p.err));
       if (ok) {
         tc_fence_after();
-        issue_st(dK0, dQk, kColS);
-        issue_st(dV0, dDOk, kColDP);
+        issue_st(dK0, dQk, kColS, kTab);
+        issue_st(dV0, dDOk, kColDP, false);
         mma_commit(&b->st_full[0]);
       }
       // tb: the step's TMEM buffer (two), qs: its Q / dO stage (kStagesA)
@@ -237,15 +268,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 < n_it) {
           const int t1 = (it + 1) & 1, q1 = (it + 1) % kStagesA, u1 = (it + 1) / kStagesA;
           if (!wait_bar(&b->sync, &b->qdo_full[q1], u1 & 1, p.err)) break;
+          if (kTab && !wait_bar(&b->sync, &b->b_full[t1], ((it + 1) >> 1) & 1, p.err)) break;
           tc_fence_after();
-          issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA);
-          issue_st(dV0, dDOk + qoff(q1), kColDP + t1 * kRowsA);
+          issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA, kTab);
+          issue_st(dV0, dDOk + qoff(q1), kColDP + t1 * kRowsA, false);
           mma_commit(&b->st_full[t1]);
         }
         if (!wait_bar(&b->sync, &b->ps_full[tb], (it >> 1) & 1, p.err)) break;
         tc_fence_after();
         issue_grad(kColS + tb * kRowsA, dDOm + qoff(qs), kColDV, it > 0);
         issue_grad(kColDP + tb * kRowsA, dQm + qoff(qs), kColDK, it > 0);
+        if (kTab && it + 2 < n_it) mma_commit(&b->s_free[tb]);  // step it + 2's bias may go in
         if (it + 1 == n_it) mma_commit(&b->mm_done);
         if (it + kStagesA < n_it) mma_commit(&b->qdo_empty[qs]);  // a later step refills it
       }
@@ -280,6 +313,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     const bool fetcher = tid < 2 * kRowsA;
     float next_val = (n_it > 0 && fetcher) ? row_value(0) : 0.f;
+    // kTab: bias entries of step u for this key and the warp's 32 rows, over
+    // the positive scale, into S^T buffer u & 1 (rows or keys out of range: 0)
+    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
+    auto load_bias = [&](int u, uint32_t (&bv)[32]) {
+      const int ib = it_row0(u) + half * 32;
+      const float *base = btab_row(p.btab, p.bss, p.bhs, p.brs, seq, it_head(u), 0) + j;
+#pragma unroll
+      for (int c = 0; c < 32; c++)
+        bv[c] = __float_as_uint(ib + c < g.nq && j < g.nk
+                                    ? __ldg(base + (long long)(ib + c) * p.brs) * inv_scale
+                                    : 0.f);
+    };
+    auto store_bias = [&](int u, const uint32_t (&bv)[32]) {
+      tmem_st32(t_lane + kColS + (u & 1) * kRowsA + half * 32, bv);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&b->b_full[u & 1]);
+    };
+    if (kTab)
+      for (int u = 0; u < 2 && u < n_it; u++) {
+        uint32_t bv[32];
+        load_bias(u, bv);
+        store_bias(u, bv);
+      }
     for (int it = 0; it < n_it; it++) {
       const int st = it & 1;
       const int i0 = it_row0(it);
@@ -345,6 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ps_full[st]);
+      if (kTab && it + 2 < n_it) {
+        // step it + 2 reuses this S^T buffer once dV and dK have read P^T, dS^T
+        uint32_t bv[32];
+        load_bias(it + 2, bv);
+        ok = __all_sync(0xffffffffu, wait_bar(&b->sync, &b->s_free[st], (it >> 1) & 1, p.err));
+        if (ok) {
+          tc_fence_after();
+          store_bias(it + 2, bv);
+        }
+      }
     }
     if (ok && n_it > 0) {
       if (wait_bar(&b->sync, &b->mm_done, 0, p.err))
@@ -416,11 +483,14 @@ struct LayoutB {
 struct BarsB {
   uint64_t qdo_full, k_full[kStagesK], v_full[2], k_empty[kStagesK], v_empty[2], s_full[2],
       dp_full, dp_free, ds_full, dq_done;
+  uint64_t b_full[2], s_free[2];  // kTab: bias stored in S buffer t / buffer t read by dQ
   uint32_t tmem_base;
   Sync sync;
 };
 
-template <int D, bool kBias>
+// kTab: an explicit bias tensor; the math warps store a tile's entries (over
+// the positive scale) into its S buffer and S = Q K^T accumulates onto them.
+template <int D, bool kBias, bool kTab>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -466,6 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&b->dp_full, 1);
     mbar_init(&b->dp_free, 256);
+    for (int s = 0; s < 2; s++) {
+      mbar_init(&b->b_full[s], 256);
+      mbar_init(&b->s_free[s], 1);
+    }
     mbar_init(&b->ds_full, 256);
     mbar_init(&b->dq_done, 1);
     b->sync.abort = 0;
@@ -518,11 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024), dV0 = smem_desc_sw128(sV, 16, 1024);
       const uint64_t dKm = smem_desc_sw128(sK, kChunk128, 1024);
       auto toff = [&](int s1) { return (uint64_t)((s1 * L::kTile) >> 4); };
-      auto issue_s = [&](uint64_t da, uint64_t db, uint32_t col) {
+      // acc0: accumulate from the first K step on (onto a stored bias)
+      auto issue_s = [&](uint64_t da, uint64_t db, uint32_t col, bool acc0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint64_t off = (uint64_t)((((kk >> 2) * kChunk128) + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(tmem + col, da + off, db + off, idesc_s, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + col, da + off, db + off, idesc_s, (acc0 || kk > 0) ? 1u : 0u);
         }
       };
       // dQ += dS K, dS in tensor memory: keys [64 h, 64 h + 64) as 32 packed
@@ -535,16 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = wait_bar(&b->sync, &b->qdo_full, 0, p.err) &&
-                wait_bar(&b->sync, &b->k_full[0], 0, p.err);
+                wait_bar(&b->sync, &b->k_full[0], 0, p.err) &&
+                (!kTab || wait_bar(&b->sync, &b->b_full[0], 0, p.err));
       if (ok) {
         tc_fence_after();
-        issue_s(dQ0, dK0, kColS);
+        issue_s(dQ0, dK0, kColS, kTab);
         mma_commit(&b->s_full[0]);
         ok = wait_bar(&b->sync, &b->v_full[0], 0, p.err);
       }
       if (ok) {
         tc_fence_after();
-        issue_s(dDO0, dV0, kColDP);
+        issue_s(dDO0, dV0, kColDP, false);
         mma_commit(&b->dp_full);
         if (2 < n_tiles) mma_commit(&b->v_empty[0]);
       }
@@ -555,8 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj + 1 < n_tiles) {
           const int k1 = (jj + 1) % kStagesK;
           if (!wait_bar(&b->sync, &b->k_full[k1], ((jj + 1) / kStagesK) & 1, p.err)) break;
+          if (kTab && !wait_bar(&b->sync, &b->b_full[s1], u1 & 1, p.err)) break;
           tc_fence_after();
-          issue_s(dQ0, dK0 + toff(k1), kColS + s1 * kTileKeys);
+          issue_s(dQ0, dK0 + toff(k1), kColS + s1 * kTileKeys, kTab);
           mma_commit(&b->s_full[s1]);
           // dP's single buffer is free as soon as the math warps have read
           // this tile's dP out, well before they finish dS: the next dP
@@ -565,13 +642,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               !wait_bar(&b->sync, &b->v_full[s1], u1 & 1, p.err))
             break;
           tc_fence_after();
-          issue_s(dDO0, dV0 + toff(s1), kColDP);
+          issue_s(dDO0, dV0 + toff(s1), kColDP, false);
           mma_commit(&b->dp_full);
           if (jj + 3 < n_tiles) mma_commit(&b->v_empty[s1]);  // tile jj + 3 refills it
         }
         if (!wait_bar(&b->sync, &b->ds_full, jj & 1, p.err)) break;
         tc_fence_after();
         issue_dq(st, ks, jj > 0);
+        if (kTab && jj + 2 < n_tiles) mma_commit(&b->s_free[st]);  // tile jj + 2's bias may go in
         if (jj + 1 == n_tiles) mma_commit(&b->dq_done);
         if (jj + kStagesK < n_tiles) mma_commit(&b->k_empty[ks]);  // a later tile refills it
       }
@@ -593,6 +671,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
     const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     bool ok = true;
+    // kTab: this warp's 64 keys of tile u's bias row into S buffer u & 1
+    const float *brow = kTab && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, h, i) : nullptr;
+    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
+    auto store_bias = [&](int u, const uint32_t (&bv)[64]) {
+      const uint32_t col = t_lane + kColS + (u & 1) * kTileKeys + half * 64;
+      tmem_st32(col, *reinterpret_cast<const uint32_t(*)[32]>(bv));
+      tmem_st32(col + 32, *reinterpret_cast<const uint32_t(*)[32]>(bv + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&b->b_full[u & 1]);
+    };
+    if (kTab)
+      for (int u = 0; u < 2 && u < n_tiles; u++) {
+        uint32_t bv[64];
+        load_bias_row<64>(brow, (n_first + u) * kTileKeys + half * 64, g.nk, inv_scale, bv);
+        store_bias(u, bv);
+      }
     for (int jj = 0; jj < n_tiles; jj++) {
       const int st = jj & 1;
       // S is issued before dP, so both are in once dP is
@@ -650,6 +745,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ds_full);
+      if (kTab && jj + 2 < n_tiles) {
+        // tile jj + 2 reuses this S buffer once dQ has read this tile's dS
+        uint32_t bv[64];
+        load_bias_row<64>(brow, (n_first + jj + 2) * kTileKeys + half * 64, g.nk, inv_scale, bv);
+        ok = wait_bar(&b->sync, &b->s_free[st], (jj >> 1) & 1, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        store_bias(jj + 2, bv);
+      }
     }
     if (ok && n_tiles > 0) {
       if (wait_bar(&b->sync, &b->dq_done, 0, p.err))
@@ -702,7 +809,7 @@ cudaError_t set_smem(K kernel, int bytes, bool *configured) {
   return cudaSuccess;
 }
 
-template <int D, bool kBias>
+template <int D, bool kBias, bool kTab>
 cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
   const BwdParams &p = a.p;
   // Every tensor-core product of the backward runs on the fp16 copies.
@@ -716,17 +823,17 @@ cudaError_t launch_d(const BwdTcArgs &a, cudaStream_t st) {
       !make_map(&mv, p.v16, D, p.hkv, p.total_k, 1, kTileKeys, f16))
     return cudaErrorInvalidValue;
   static bool conf_a[64] = {false}, conf_b[64] = {false};
-  cudaError_t e = set_smem(bwd_dkdv_tc_kernel<D, kBias>, LayoutA<D>::kAlloc, conf_a);
+  cudaError_t e = set_smem(bwd_dkdv_tc_kernel<D, kBias, kTab>, LayoutA<D>::kAlloc, conf_a);
   if (e != cudaSuccess) return e;
-  e = set_smem(bwd_dq_tc_kernel<D, kBias>, LayoutB<D>::kAlloc, conf_b);
+  e = set_smem(bwd_dq_tc_kernel<D, kBias, kTab>, LayoutB<D>::kAlloc, conf_b);
   if (e != cudaSuccess) return e;
   const long long ga = (long long)a.n_key_tiles * p.hkv * p.batch;
   const long long gb = (long long)a.n_row_tiles * p.hq * p.batch;
   if (ga >= (1LL << 31) || gb >= (1LL << 31)) return cudaErrorInvalidValue;
-  bwd_dkdv_tc_kernel<D, kBias><<<(unsigned)ga, kThreads, LayoutA<D>::kAlloc, st>>>(q64, do64, mk, mv, a);
+  bwd_dkdv_tc_kernel<D, kBias, kTab><<<(unsigned)ga, kThreads, LayoutA<D>::kAlloc, st>>>(q64, do64, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<D, kBias><<<(unsigned)gb, kThreads, LayoutB<D>::kAlloc, st>>>(q128, do128, mk, mv, a);
+  bwd_dq_tc_kernel<D, kBias, kTab><<<(unsigned)gb, kThreads, LayoutB<D>::kAlloc, st>>>(q128, do128, mk, mv, a);
   return cudaGetLastError();
 }
 
@@ -739,12 +846,14 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_
   a.group = p.hq / p.hkv;
   a.n_key_tiles = (p.max_k + kKeysA - 1) / kKeysA;
   a.n_row_tiles = (p.max_q + kTileRows - 1) / kTileRows;
-  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d ctas_dkdv=%lld ctas_dq=%lld",
-           p.d, p.d, (long long)a.n_key_tiles * p.hkv * p.batch,
+  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d%s ctas_dkdv=%lld ctas_dq=%lld",
+           p.d, p.d, p.btab ? "_btab" : "", (long long)a.n_key_tiles * p.hkv * p.batch,
            (long long)a.n_row_tiles * p.hq * p.batch);
   if (a.n_key_tiles == 0 || a.n_row_tiles == 0) return cudaSuccess;
-  if (p.slopes) return p.d == 64 ? launch_d<64, true>(a, st) : launch_d<128, true>(a, st);
-  return p.d == 64 ? launch_d<64, false>(a, st) : launch_d<128, false>(a, st);
+  // a bias tensor comes here only with a positive scale and no slopes
+  if (p.btab) return p.d == 64 ? launch_d<64, false, true>(a, st) : launch_d<128, false, true>(a, st);
+  if (p.slopes) return p.d == 64 ? launch_d<64, true, false>(a, st) : launch_d<128, true, false>(a, st);
+  return p.d == 64 ? launch_d<64, false, false>(a, st) : launch_d<128, false, false>(a, st);
 }
 
 }  // namespace attn

@@ -104,6 +104,10 @@ WORKLOADS = {
     # heads (a fifth of its entries -inf)
     "bias_tensor_prefill": Workload("bias_tensor_prefill", (4096,) * 4, (4096,) * 4, 32, 8,
                                     128, "bf16", MASK_TOP_LEFT, 1002, bias_tensor=True),
+    # the training shape with an explicit [B, 1, N, N] bias tensor, forward + backward
+    "bias_tensor_train": Workload("bias_tensor_train", (8192,) * 2, (8192,) * 2, 16, 4,
+                                  128, "bf16", MASK_TOP_LEFT, 1004, backward=True,
+                                  bias_tensor=True),
 }
 
 

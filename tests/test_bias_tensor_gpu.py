@@ -33,20 +33,21 @@ def run(x, bias, slopes=None):
     return (o, lse, dq, dk, dv), (fplan, bplan)
 
 
-CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask, window, bias broadcast, slopes, forward kernel)
-    ("bf16_tl_full", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2"),
-    ("bf16_tl_long", (700, 300), None, 4, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2"),
-    ("bf16_br_head_bcast", (40, 9), (100, 300), 4, 1, 64, "bf16", BR, 0, True, False, "fwd_tc2"),
-    ("bf16_none_d64", (200, 77), (150, 300), 4, 4, 64, "bf16", NONE, 0, False, False, "fwd_tc2"),
-    ("bf16_none_slopes", (50, 77), (70, 20), 4, 4, 128, "bf16", NONE, 0, False, True, "fwd_simt"),
-    ("bf16_tl_window", (90, 333), None, 4, 2, 64, "bf16", TL, 9, False, False, "fwd_tc2"),
-    ("fp32_br", (37, 70), (50, 70), 4, 2, 64, "fp32", BR, 0, True, True, "fwd_simt"),
+CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask, window, bias broadcast, slopes,
+    #          forward kernel, backward kernel)
+    ("bf16_tl_full", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "dq_tc"),
+    ("bf16_tl_long", (700, 300), None, 4, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "dq_tc"),
+    ("bf16_br_head_bcast", (40, 9), (100, 300), 4, 1, 64, "bf16", BR, 0, True, False, "fwd_tc2", "dq_tc"),
+    ("bf16_none_d64", (200, 77), (150, 300), 4, 4, 64, "bf16", NONE, 0, False, False, "fwd_tc2", "dq_tc"),
+    ("bf16_none_slopes", (50, 77), (70, 20), 4, 4, 128, "bf16", NONE, 0, False, True, "fwd_simt", "simt"),
+    ("bf16_tl_window", (90, 333), None, 4, 2, 64, "bf16", TL, 9, False, False, "fwd_tc2", "dq_tc"),
+    ("fp32_br", (37, 70), (50, 70), 4, 2, 64, "fp32", BR, 0, True, True, "fwd_simt", "simt"),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_bias_tensor_fwd_bwd(case):
-    name, lq, lk, hq, hkv, d, dt, mask, window, bcast, with_slopes, kernel = case
+    name, lq, lk, hq, hkv, d, dt, mask, window, bcast, with_slopes, kernel, bkernel = case
     w = inputs.custom(name, lq, lk or lq, hq, hkv, d, dt, mask, seed=61, backward=True,
                       v_shift_per_seq=2.0, window=window)
     x = inputs.make_inputs(w)
@@ -54,7 +55,7 @@ def test_bias_tensor_fwd_bwd(case):
                               seed=62, dead_rows=3)
     slopes = inputs.bias_slopes(hq) if with_slopes else None
     (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias, slopes)
-    assert "_btab" in fplan and "_btab" in bplan and kernel in fplan, (fplan, bplan)
+    assert "_btab" in fplan and "_btab" in bplan and kernel in fplan and bkernel in bplan, (fplan, bplan)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
                                          x["cu_seqlens_k"], w.scale, mask, window=window,
                                          slopes=None if slopes is None else slopes.double().numpy(),

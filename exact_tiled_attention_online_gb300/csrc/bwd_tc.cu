@@ -345,6 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (fetcher && it + 1 < n_it) next_val = row_value(it + 1);
       const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
       const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
+      // kTab: step it + 2's bias loads fly during this step's math
+      uint32_t bnext[32];
+      if (kTab && it + 2 < n_it) load_bias(it + 2, bnext);
       if (ok)
         ok = wait_bar(&b->sync, &b->st_full[st], (it >> 1) & 1, p.err);
       ok = __all_sync(0xffffffffu, ok);
@@ -404,12 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&b->ps_full[st]);
       if (kTab && it + 2 < n_it) {
         // step it + 2 reuses this S^T buffer once dV and dK have read P^T, dS^T
-        uint32_t bv[32];
-        load_bias(it + 2, bv);
         ok = __all_sync(0xffffffffu, wait_bar(&b->sync, &b->s_free[st], (it >> 1) & 1, p.err));
         if (ok) {
           tc_fence_after();
-          store_bias(it + 2, bv);
+          store_bias(it + 2, bnext);
         }
       }
     }

@@ -199,8 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO);
   float *sRow = reinterpret_cast<float *>(smem + L::kRow);
 
-  auto it_head = [&](int it) { return hk * a.group + it / n_m; };
-  auto it_row0 = [&](int it) { return (m_begin + it % n_m) * kRowsA; };
+  // Steps walk the group's heads one after another over the row tiles; with a
+  // bias tensor the heads of one row tile come back to back instead, so a
+  // tensor shared by the heads is read from cache after the first head.
+  auto it_head = [&](int it) { return hk * a.group + (kTab ? it % a.group : it / n_m); };
+  auto it_row0 = [&](int it) { return (m_begin + (kTab ? it / a.group : it % n_m)) * kRowsA; };
 
   if (warp == 0) {
     if (lane == 0 && n_it > 0) {

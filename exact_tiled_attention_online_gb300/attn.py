@@ -150,7 +150,7 @@ def _btab(bias: Optional[torch.Tensor], batch: int, hq: int, max_q: int, max_k: 
     from ``expand`` are fine), or None."""
     if bias is None:
         return None
-    if not isinstance(bias, torch.Tensor) or not bias.is_cuda or bias.dtype != torch.float32:
+    if not getattr(bias, "is_cuda", False) or bias.dtype != torch.float32:
         raise ValueError("bias must be an fp32 CUDA tensor")
     if bias.dim() != 4 or bias.shape[0] not in (1, batch) or bias.shape[1] not in (1, hq):
         raise ValueError("bias must be [1 or B, 1 or Hq, rows, keys]")

@@ -126,3 +126,43 @@ def test_bias_tensor_rejections(lib):
         b = attn.AttnBiasTensor(data, *strides)
         assert lib.attn_fwd_ex(None, ctypes.byref(b), *fargs) == 1
         assert lib.attn_bwd_ex(None, ctypes.byref(b), *bargs) == 1
+
+
+@pytest.mark.parametrize("shape,err", [((2, 4, 8, 8), "CUDA"), ((8, 8), "CUDA")])
+def test_binding_refuses_host_or_misshapen_bias(shape, err):
+    """The binding refuses a bias that is not a CUDA fp32 tensor before any
+    call into the library."""
+    import torch
+    with pytest.raises(ValueError, match=err):
+        attn._btab(torch.zeros(shape), 2, 4, 8, 8)
+
+
+def test_binding_bias_strides_broadcast():
+    """Broadcast dimensions (size 1) get stride 0; the key stride must be 1.
+    Checked on the stride arithmetic alone, with a stand-in for the tensor."""
+    class FakeTensor:  # quacks like a CUDA fp32 tensor for _btab's checks
+        import torch
+        is_cuda, dtype = True, torch.float32
+
+        def __init__(self, shape, strides):
+            self.shape, self._st = shape, strides
+
+        def dim(self):
+            return len(self.shape)
+
+        def stride(self, i):
+            return self._st[i]
+
+        def data_ptr(self):
+            return 4096
+
+    b = attn._btab(FakeTensor((1, 4, 8, 9), (288, 72, 9, 1)), 2, 4, 8, 9)
+    assert (b.seq_stride, b.head_stride, b.row_stride) == (0, 72, 9)
+    b = attn._btab(FakeTensor((2, 1, 8, 9), (72, 0, 9, 1)), 2, 4, 8, 9)
+    assert (b.seq_stride, b.head_stride, b.row_stride) == (72, 0, 9)
+    with pytest.raises(ValueError):
+        attn._btab(FakeTensor((2, 4, 8, 9), (288, 72, 1, 8)), 2, 4, 8, 9)  # keys not contiguous
+    with pytest.raises(ValueError):
+        attn._btab(FakeTensor((2, 4, 7, 9), (252, 63, 9, 1)), 2, 4, 8, 9)  # too few rows
+    with pytest.raises(ValueError):
+        attn._btab(FakeTensor((3, 4, 8, 9), (288, 72, 9, 1)), 2, 4, 8, 9)  # wrong batch

@@ -221,25 +221,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // kTab: Q K^T of tile X's c-th product accumulates onto the bias its
       // softmax warps stored, announced by phase c of b_full[X]
       bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
-      if (ok) {
-        if (in_a(0)) {
-          if (kTab && !(ok = wait2(b, &b->b_full[0], 0, p.err))) {
-          } else {
-            tc_fence_after();
-            issue_qk(0, 0);
-            mma_commit(&b->s_full[0]);
-          }
-        }
-        if (ok && in_b(0)) {
-          if (kTab && !(ok = wait2(b, &b->b_full[1], 0, p.err))) {
-          } else {
-            tc_fence_after();
-            issue_qk(1, 0);
-            mma_commit(&b->s_full[1]);
-          }
-        }
-        if (ok) mma_commit(&b->k_empty[0]);
+      if (ok && in_a(0) && (!kTab || (ok = wait2(b, &b->b_full[0], 0, p.err)))) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(&b->s_full[0]);
       }
+      if (ok && in_b(0) && (!kTab || (ok = wait2(b, &b->b_full[1], 0, p.err)))) {
+        tc_fence_after();
+        issue_qk(1, 0);
+        mma_commit(&b->s_full[1]);
+      }
+      if (ok) mma_commit(&b->k_empty[0]);
       for (int n = 0; ok && n < N; n++) {
         const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
         bool v_ready = false, k1_ready = false;

@@ -97,3 +97,24 @@ def test_zero_bias_tensor_matches_no_bias_oracle():
     compare.check_close("dq", dq, rdq)
     compare.check_close("dk", dk, rdk)
     compare.check_close("dv", dv, rdv)
+
+
+@pytest.mark.parametrize("shape", ["heads_only", "sequences_only"])
+def test_bias_tensor_mixed_broadcast(shape):
+    """A tensor with one entry per head shared by every sequence, or one per
+    sequence shared by every head, on the tensor-core path forward and
+    backward."""
+    w = inputs.custom("bmix", (130, 40, 200), (130, 90, 200), 4, 2, 128, "bf16", BR, seed=66,
+                      backward=True)
+    x = inputs.make_inputs(w)
+    b, hb = (1, 4) if shape == "heads_only" else (w.batch, 1)
+    bias = inputs.bias_tensor(b, hb, w.max_q, w.max_k, seed=67, dead_rows=2)
+    (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias)
+    assert "fwd_tc2" in fplan and "dq_tc" in bplan, (fplan, bplan)
+    rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], w.scale, BR, bias=bias)
+    compare.check_close("o", o, ro)
+    compare.check_lse("lse", lse, rlse)
+    compare.check_close("dq", dq, rdq)
+    compare.check_close("dk", dk, rdk)
+    compare.check_close("dv", dv, rdv)

@@ -25,6 +25,14 @@
 // out-of-range lanes get P = dS = 0.  D and lse2 (lse in log2 units, +inf for
 // empty rows) come from the preprocess kernel.  Waits are bounded like the
 // forward's.
+//
+// Scheduling: the streamed operand rings (Q / dO four stages deep in dkdv, K
+// three in dq) cover a stage's release, which waits for the products that
+// read it, plus the refill's TMA latency; dq releases its single dP buffer as
+// soon as the math warps have copied dP out, so the next dP product overlaps
+// the exponentials.  Biases rebuild the forward's: the linear positional bias
+// in the math (kBias), an explicit bias tensor stored into the score buffer
+// before the score product accumulates onto it (kTab).
 #include <stdio.h>
 
 #include <type_traits>

@@ -19,7 +19,10 @@
 //
 // With the extra registers a softmax thread loads its whole 128-score row
 // from TMEM with one wait, takes the max, and writes the 64 packed
-// probabilities back.
+// probabilities back.  Instances add the linear positional bias in the softmax (kBias)
+// or an explicit bias tensor that the softmax warps store into S before
+// Q K^T accumulates onto it (kTab; then tile A's next Q K^T follows tile B's
+// P V, since A's bias waits for A's P V to finish reading P).
 #include <stdio.h>
 
 #include <type_traits>

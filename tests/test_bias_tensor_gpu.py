@@ -10,6 +10,7 @@ import torch
 import oracle
 from exact_tiled_attention_online_gb300 import attn, inputs
 from tests import compare
+from tests.gpu_cases import sample_rows
 
 pytestmark = pytest.mark.gpu
 TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
@@ -118,3 +119,41 @@ def test_bias_tensor_mixed_broadcast(shape):
     compare.check_close("dq", dq, rdq)
     compare.check_close("dk", dk, rdk)
     compare.check_close("dv", dv, rdv)
+
+
+def test_bias_tensor_prefill_full_size_sampled():
+    """The bias-tensor prefill workload at full size: sampled rows against the
+    oracle with the same [B, 1, N, N] tensor."""
+    w = inputs.WORKLOADS["bias_tensor_prefill"]
+    x = inputs.make_inputs(w)
+    bias = inputs.bias_tensor(w.batch, 1, w.max_q, w.max_k, w.seed + 1)
+    d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
+    o, lse = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
+                      w.max_k, w.mask, w.scale, bias=bias.cuda())
+    assert "fwd_tc2" in attn.last_plan() and "_btab" in attn.last_plan()
+    torch.cuda.synchronize()
+    assert attn.get_device_error() == 0
+    rows = sample_rows(w, 24, seed=71)
+    ro, rl = oracle.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.scale,
+                        w.mask, rows=rows, bias=bias)
+    on, ln = compare.to_np(o), compare.to_np(lse)
+    compare.check_close("o", on[rows[:, 0], rows[:, 1]], ro)
+    compare.check_lse("lse", ln[rows[:, 1], rows[:, 0]], rl)
+
+
+def test_bias_tensor_train_full_size_sampled():
+    """The bias-tensor training workload at full size: sampled dQ rows and dK,
+    dV key rows against the oracle's sampled backward."""
+    w = inputs.WORKLOADS["bias_tensor_train"]
+    x = inputs.make_inputs(w)
+    bias = inputs.bias_tensor(w.batch, 1, w.max_q, w.max_k, w.seed + 1)
+    (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias)
+    assert "fwd_tc2" in fplan and "dq_tc" in bplan, (fplan, bplan)
+    qrows = sample_rows(w, 8, seed=72)
+    krows = np.array([(0, 0), (8191, 3), (8192, 1), (16383, 2)], np.int64)
+    rdq, rdk, rdv = oracle.bwd_sampled(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                       x["cu_seqlens_k"], w.scale, w.mask, qrows, krows,
+                                       bias=bias)
+    compare.check_close("dq", compare.to_np(dq)[qrows[:, 0], qrows[:, 1]], rdq)
+    compare.check_close("dk", compare.to_np(dk)[krows[:, 0], krows[:, 1]], rdk)
+    compare.check_close("dv", compare.to_np(dv)[krows[:, 0], krows[:, 1]], rdv)

@@ -358,11 +358,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
         break;
       }
       tc_fence_after();
-      // the whole row of 128 scores, one TMEM wait
+      // the whole row of 128 scores in one TMEM load instruction (measured 1%
+      // faster than four of 32 columns; one store of 64 columns for P was not)
       uint32_t v[kTileKeys];
-#pragma unroll
-      for (int c = 0; c < kTileKeys / 32; c++)
-        tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      static_assert(kTileKeys == 128, "one 128-column load");
+      tmem_ld128(s_col, v);
       tmem_wait_ld();
       if (!kr.full(n)) {
         // lanes outside [first, limit) of this row: first <= limit, so one

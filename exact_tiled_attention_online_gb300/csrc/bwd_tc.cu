@@ -713,8 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this warp's 64 dP columns and its first 32 S columns under one wait;
       // then the dP buffer is released
       uint32_t dv[64], sv[32];
-      tmem_ld32(t_lane + kColDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
-      tmem_ld32(t_lane + kColDP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_ld64(t_lane + kColDP + half * 64, dv);
       tmem_ld32(t_lane + kColS + st * kTileKeys + half * 64, sv);
       tmem_wait_ld();
       tc_fence_before();

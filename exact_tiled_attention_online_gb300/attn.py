@@ -25,7 +25,9 @@ DTYPE_BF16 = 0
 DTYPE_FP32 = 1
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
-          4: "CUDA error", 5: "device wait timed out", 6: "cu_seqlens out of bounds"}
+          4: "CUDA error", 5: "device wait timed out", 6: "cu_seqlens out of bounds",
+          7: "needs more than the static scratch holds",
+          8: "a backward input holds an infinity or NaN"}
 
 _SYMBOLS = ["attn_fwd", "attn_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_workspace_size", "attn_bwd_workspace_size",
             "attn_mask_probe", "attn_get_device_error", "attn_status_string",
@@ -241,7 +243,8 @@ def bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         bias_slopes: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None):
     """Attention backward; returns (dq, dk, dv) with dk/dv summed over each
     KV head's group of query heads.  Pass the forward's ``o_f32`` when it was
-    kept, so that D_i = dO_i . O_i does not carry O's bf16 rounding; pass the
+    kept: D_i = dO_i . O_i then comes from it; without it the library
+    recomputes the fp32 output for D (one extra forward pass).  Pass the
     forward's mask, ``window``, ``bias_slopes`` and ``bias``."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n, 3, True)

@@ -14,6 +14,8 @@ cudaError_t launch_fwd_simt(const FwdParams &p, attn_dtype dtype, cudaStream_t s
 cudaError_t launch_bwd_simt(const BwdParams &p, attn_dtype dtype, cudaStream_t st);
 cudaError_t launch_bwd_pre(const BwdParams &p, attn_dtype dtype, cudaStream_t st);
 cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_amax(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_fwd_tc2_delta(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
 cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st,
                           char *desc, size_t desc_len);
@@ -86,10 +88,11 @@ static int sm_count() {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Backward workspace: D and lse2 [hq, total_q] fp32; for bf16 also fp16
-// copies of q, dout ([total_q, hq, d]) and k, v ([total_k, hkv, d]).
+// Backward workspace: D and lse2 [hq, total_q] fp32; for bf16 also scaled
+// fp16 copies of q, dout ([total_q, hq, d]) and k, v ([total_k, hkv, d]) and
+// the four tensors' largest magnitudes (256 bytes).
 struct BwdLayout {
-  size_t delta, lse2, q16, do16, k16, v16, total;
+  size_t delta, lse2, q16, do16, k16, v16, amax, total;
 };
 static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, int dtype) {
   BwdLayout l{};
@@ -105,6 +108,8 @@ static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, in
     l.k16 = off + 2 * qb;
     l.v16 = off + 2 * qb + kb;
     off += 2 * qb + 2 * kb;
+    l.amax = off;
+    off += 256;
   }
   l.total = off;
   return l;
@@ -137,7 +142,7 @@ const char *attn_status_string(attn_status s) {
     case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device wait expired";
     case ATTN_ERR_DEVICE_BOUNDS: return "cu_seqlens inconsistent with the sizes passed";
     case ATTN_ERR_SCRATCH_LIMIT: return "problem needs more than the library's static scratch";
-    case ATTN_ERR_DEVICE_RANGE: return "a backward input lies outside the fp16 range";
+    case ATTN_ERR_DEVICE_RANGE: return "a backward input holds an infinity or NaN";
   }
   return "unknown status";
 }
@@ -238,6 +243,7 @@ attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
     if (gz > 65535) return ATTN_ERR_UNSUPPORTED;
   }
   char desc[384];
+  desc[0] = 0;  // a launcher that fails early may leave it unwritten
   cudaError_t ce;
   if (plan.kind == PLAN_SIMT) {
     ce = launch_fwd_simt(p, dtype, cs);
@@ -352,7 +358,8 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
     ce = launch_zero_rows(dk, total_k, hkv, d, p.sdk, elem, cs);
     if (ce == cudaSuccess) ce = launch_zero_rows(dv, total_k, hkv, d, p.sdv, elem, cs);
   }
-  char desc[256];
+  char desc[320];
+  desc[0] = 0;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(dout);
   // a bias tensor rides on the raw scores: tensor cores only with a positive
@@ -364,8 +371,30 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
     p.do16 = ws + wl.do16;
     p.k16 = ws + wl.k16;
     p.v16 = ws + wl.v16;
+    p.amax = reinterpret_cast<unsigned int *>(ws + wl.amax);
+    // Without the forward's fp32 output, D_i = dO_i . O_i comes from a
+    // forward pass that recomputes it (the rounded O would carry its bf16
+    // error into every gradient through D).
+    p.delta_ready = o_f32 ? 0 : 1;
+    if (ce == cudaSuccess) ce = launch_bwd_amax(p, cs);
     if (ce == cudaSuccess) ce = launch_bwd_pre(p, dtype, cs);
     if (ce == cudaSuccess) ce = launch_kv_to_f16(p, cs);
+    if (ce == cudaSuccess && !o_f32) {
+      FwdParams fp{};
+      fp.q = q; fp.k = k; fp.v = v;
+      fp.cu_q = cu_q; fp.cu_k = cu_k;
+      fp.batch = batch; fp.max_q = max_q; fp.max_k = max_k; fp.total_q = total_q;
+      fp.total_k = total_k;
+      fp.hq = hq; fp.hkv = hkv; fp.d = d; fp.scale = scale; fp.scale_log2 = p.scale_log2;
+      fp.mask = mask;
+      fp.window = window;
+      fp.slopes = bias_slopes;
+      fp.btab = p.btab; fp.bss = p.bss; fp.bhs = p.bhs; fp.brs = p.brs;
+      fp.sq = p.sq; fp.sk = p.sk; fp.sv = p.sv;
+      fp.err = p.err;
+      fp.dout = dout; fp.sdo = p.sdo; fp.delta = p.delta;
+      ce = launch_fwd_tc2_delta(fp, cs);
+    }
     if (ce == cudaSuccess) ce = launch_bwd_tc(p, cs, desc, sizeof(desc));
   } else {
     if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);

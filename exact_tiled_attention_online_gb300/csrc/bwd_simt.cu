@@ -28,7 +28,9 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
   const T *op = reinterpret_cast<const T *>(p.o) + toff(p.so, t, h) + lane * E;
   const T *dp = reinterpret_cast<const T *>(p.dout) + toff(p.sdo, t, h) + lane * E;
   float part = 0.f;
-  if (p.o_f32) {
+  if (p.delta_ready) {
+    // D comes from the recomputing forward
+  } else if (p.o_f32) {
     const float *of = p.o_f32 + (size_t)row * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; e++) part += of[e] * Elem<T>::to_f(dp[e]);
@@ -38,24 +40,21 @@ __global__ void __launch_bounds__(128) bwd_pre_kernel(BwdParams p) {
   }
   const float D_i = warp_sum(part);
   if (p.q16) {
-    // fp16 copies for the tensor-core backward; bf16 -> fp16 is exact inside
-    // the fp16 normal range, larger magnitudes are reported.
+    // scaled fp16 copies for the tensor-core backward (exact: a power of two)
+    const float fq = exp2_int(f16_copy_exponent(p.amax[kAmaxQ]));
+    const float fdo = exp2_int(f16_copy_exponent(p.amax[kAmaxDO]));
     const T *qp = reinterpret_cast<const T *>(p.q) + toff(p.sq, t, h) + lane * E;
     __half *q16 = reinterpret_cast<__half *>(p.q16) + (size_t)row * D + lane * E;
     __half *d16 = reinterpret_cast<__half *>(p.do16) + (size_t)row * D + lane * E;
-    bool bad = false;
 #pragma unroll
     for (int e = 0; e < E; e++) {
-      const float a = Elem<T>::to_f(qp[e]), c = Elem<T>::to_f(dp[e]);
-      bad |= fabsf(a) > 65504.f || fabsf(c) > 65504.f;
-      q16[e] = __float2half_rn(a);
-      d16[e] = __float2half_rn(c);
+      q16[e] = __float2half_rn(Elem<T>::to_f(qp[e]) * fq);
+      d16[e] = __float2half_rn(Elem<T>::to_f(dp[e]) * fdo);
     }
-    if (bad) raise_error(p.err, ATTN_ERR_DEVICE_RANGE);
   }
   if (lane == 0) {
     const float l = p.lse[(size_t)h * p.total_q + t];
-    p.delta[(size_t)h * p.total_q + t] = D_i;
+    if (!p.delta_ready) p.delta[(size_t)h * p.total_q + t] = D_i;
     // An empty row (lse = -inf) gets +inf so that 2^(s - lse2) = 0.
     p.lse2[(size_t)h * p.total_q + t] = l == -INFINITY ? INFINITY : l * kLog2e;
   }
@@ -92,7 +91,9 @@ __global__ void __launch_bounds__(128) bwd_pre_vec_kernel(BwdParams p) {
     dof[2 * k + 1] = __uint_as_float(dw[k] & 0xFFFF0000u);
   }
   float part = 0.f;
-  if (p.o_f32) {
+  if (p.delta_ready) {
+    // D comes from the recomputing forward
+  } else if (p.o_f32) {
     const float *of = p.o_f32 + (size_t)row * D + lane * E;
     float o[E];
     if constexpr (E == 4) {
@@ -113,17 +114,17 @@ __global__ void __launch_bounds__(128) bwd_pre_vec_kernel(BwdParams p) {
     }
   }
   const float D_i = warp_sum(part);
-  // fp16 copies of q and dout (exact inside the fp16 normal range; larger
-  // magnitudes are reported)
+  // scaled fp16 copies of q and dout (exact: a power of two, see
+  // f16_copy_exponent)
+  const float fq = exp2_int(f16_copy_exponent(p.amax[kAmaxQ]));
+  const float fdo = exp2_int(f16_copy_exponent(p.amax[kAmaxDO]));
   load_pairs(base_q + toff(p.sq, t, h) + lane * E, qw);
   uint32_t q16[E / 2], d16[E / 2];
-  bool bad = false;
 #pragma unroll
   for (int k = 0; k < E / 2; k++) {
-    const float a0 = __uint_as_float(qw[k] << 16), a1 = __uint_as_float(qw[k] & 0xFFFF0000u);
-    bad |= fabsf(a0) > 65504.f || fabsf(a1) > 65504.f || fabsf(dof[2 * k]) > 65504.f ||
-           fabsf(dof[2 * k + 1]) > 65504.f;
-    const __half2 qa = __floats2half2_rn(a0, a1), da = __floats2half2_rn(dof[2 * k], dof[2 * k + 1]);
+    const float a0 = __uint_as_float(qw[k] << 16) * fq, a1 = __uint_as_float(qw[k] & 0xFFFF0000u) * fq;
+    const __half2 qa = __floats2half2_rn(a0, a1),
+                  da = __floats2half2_rn(dof[2 * k] * fdo, dof[2 * k + 1] * fdo);
     q16[k] = *reinterpret_cast<const uint32_t *>(&qa);
     d16[k] = *reinterpret_cast<const uint32_t *>(&da);
   }
@@ -136,10 +137,9 @@ __global__ void __launch_bounds__(128) bwd_pre_vec_kernel(BwdParams p) {
     *reinterpret_cast<uint32_t *>(q16p) = q16[0];
     *reinterpret_cast<uint32_t *>(d16p) = d16[0];
   }
-  if (bad) raise_error(p.err, ATTN_ERR_DEVICE_RANGE);
   if (lane == 0) {
     const float l = p.lse[(size_t)h * p.total_q + t];
-    p.delta[(size_t)h * p.total_q + t] = D_i;
+    if (!p.delta_ready) p.delta[(size_t)h * p.total_q + t] = D_i;
     p.lse2[(size_t)h * p.total_q + t] = l == -INFINITY ? INFINITY : l * kLog2e;
   }
 }
@@ -274,15 +274,16 @@ static void launch_all(const BwdParams &p, cudaStream_t st) {
     bwd_dkdv_simt_kernel<T, D><<<dim3((p.max_k + 3) / 4, p.hkv, p.batch), 128, 0, st>>>(p);
 }
 
-// K and V (any token / head strides) -> contiguous fp16 copies for the
-// tensor-core backward, 8 elements a thread.
+// K and V (any token / head strides) -> contiguous scaled fp16 copies for the
+// tensor-core backward (see f16_copy_exponent), 8 elements a thread.
 __global__ void __launch_bounds__(256) kv_to_f16_kernel(const __nv_bfloat16 *__restrict__ k,
                                                         const __nv_bfloat16 *__restrict__ v,
                                                         __half *__restrict__ k16,
                                                         __half *__restrict__ v16, size_t n8,
                                                         int hkv, int d, Strides sk, Strides sv,
-                                                        int *err) {
-  bool bad = false;
+                                                        const unsigned int *__restrict__ amax) {
+  const float fk = exp2_int(f16_copy_exponent(amax[kAmaxK]));
+  const float fv = exp2_int(f16_copy_exponent(amax[kAmaxV]));
   const int per_row = d / 8;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * n8;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -295,15 +296,93 @@ __global__ void __launch_bounds__(256) kv_to_f16_kernel(const __nv_bfloat16 *__r
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(&in);
     uint4 out;
     __half *y = reinterpret_cast<__half *>(&out);
+    const float f = is_v ? fv : fk;
 #pragma unroll
-    for (int e = 0; e < 8; e++) {
-      const float f = __bfloat162float(x[e]);
-      bad |= fabsf(f) > 65504.f;
-      y[e] = __float2half_rn(f);
-    }
+    for (int e = 0; e < 8; e++) y[e] = __float2half_rn(__bfloat162float(x[e]) * f);
     reinterpret_cast<uint4 *>(is_v ? v16 : k16)[j] = out;
   }
-  if (bad) raise_error(err, ATTN_ERR_DEVICE_RANGE);
+}
+
+// Largest |x| of one [T, H, d] bf16 tensor as a bit pattern (sign cleared),
+// 8 elements (16 bytes) per step; contiguous tensors take a flat walk.
+struct AmaxJob {
+  const __nv_bfloat16 *base;
+  long long n8;  // 16-byte units
+  int heads, per_row;  // per_row = d / 8
+  Strides s;
+  bool flat;
+};
+struct AmaxArgs {
+  AmaxJob job[4];  // q, k, v, dout
+  unsigned int *amax;
+  int *err;
+};
+
+__device__ __forceinline__ unsigned int max_bits8(const uint4 w) {
+  const unsigned int a = max(w.x & 0x7fffu, (w.x >> 16) & 0x7fffu);
+  const unsigned int b = max(w.y & 0x7fffu, (w.y >> 16) & 0x7fffu);
+  const unsigned int c = max(w.z & 0x7fffu, (w.z >> 16) & 0x7fffu);
+  const unsigned int e = max(w.w & 0x7fffu, (w.w >> 16) & 0x7fffu);
+  return max(max(a, b), max(c, e));
+}
+
+// amax[t] = max over tensor t of |x| (bf16 bits, sign cleared; the caller
+// zeroes amax first); an infinity or NaN anywhere sets ATTN_ERR_DEVICE_RANGE.
+__global__ void __launch_bounds__(256) bwd_amax_kernel(const AmaxArgs a) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t first = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+#pragma unroll 1
+  for (int t = 0; t < 4; t++) {
+    const AmaxJob &j = a.job[t];
+    unsigned int m = 0;
+    if (j.flat) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(j.base);
+      for (size_t i = first; i < (size_t)j.n8; i += stride) m = max(m, max_bits8(__ldg(src + i)));
+    } else {
+      for (size_t i = first; i < (size_t)j.n8; i += stride) {
+        const size_t row = i / j.per_row, c8 = i % j.per_row;
+        const long long tok = (long long)(row / j.heads), h = (long long)(row % j.heads);
+        m = max(m, max_bits8(__ldg(reinterpret_cast<const uint4 *>(j.base + toff(j.s, tok, h)) + c8)));
+      }
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m != 0) {
+      if (bf16_bits_nonfinite(m)) raise_error(a.err, ATTN_ERR_DEVICE_RANGE);
+      atomicMax(a.amax + t, m);
+    }
+  }
+}
+
+cudaError_t launch_bwd_amax(const BwdParams &p, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(p.amax, 0, 4 * sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  AmaxArgs a;
+  const void *base[4] = {p.q, p.k, p.v, p.dout};
+  const Strides *str[4] = {&p.sq, &p.sk, &p.sv, &p.sdo};
+  const int heads[4] = {p.hq, p.hkv, p.hkv, p.hq};
+  const int tok[4] = {p.total_q, p.total_k, p.total_k, p.total_q};
+  long long most = 0;
+  for (int t = 0; t < 4; t++) {
+    AmaxJob &j = a.job[t];
+    j.base = static_cast<const __nv_bfloat16 *>(base[t]);
+    j.heads = heads[t];
+    j.per_row = p.d / 8;
+    j.s = *str[t];
+    j.n8 = (long long)tok[t] * heads[t] * p.d / 8;
+    j.flat = j.s.hs == p.d && j.s.ts == (long long)heads[t] * p.d;
+    if (j.n8 > most) most = j.n8;
+  }
+  a.amax = p.amax;
+  a.err = p.err;
+  if (most == 0) return cudaSuccess;
+  long long blocks = (most + 255) / 256;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long cap = 8LL * (sms > 0 ? sms : 152);  // 8 blocks of 256 per SM
+  if (blocks > cap) blocks = cap;
+  bwd_amax_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st) {
@@ -314,7 +393,7 @@ cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st) {
   kv_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16 *>(p.k), reinterpret_cast<const __nv_bfloat16 *>(p.v),
       reinterpret_cast<__half *>(p.k16), reinterpret_cast<__half *>(p.v16), n8, p.hkv, p.d, p.sk,
-      p.sv, p.err);
+      p.sv, p.amax);
   return cudaGetLastError();
 }
 

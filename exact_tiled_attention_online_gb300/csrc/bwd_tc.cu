@@ -15,10 +15,13 @@
 //         the row tile's key tiles and computes S = Q K^T, dP = dO V^T,
 //         dS = P (dP - D) (thread = row) and dQ += dS K in TMEM.
 //
-// The products run in fp16 on fp16 copies of q, k, v and dout (exact for bf16
-// values inside the fp16 range), so the P and dS operands keep 11 significant
-// bits: with bf16 P, dV of a key that thousands of rows attend misses the
-// 1e-2 contract.  Accumulation is fp32 in TMEM.
+// The products run in fp16 on fp16 copies of q, k, v and dout, each scaled by
+// a power of two that brings its largest magnitude into [4, 8) (exact for
+// every element within 2^19 of that largest one, whatever the tensor's
+// overall magnitude; the factors are undone exactly in the softmax constant,
+// D and the epilogues), so the P and dS operands keep 11 significant bits:
+// with bf16 P, dV of a key that thousands of rows attend misses the 1e-2
+// contract.  Accumulation is fp32 in TMEM.
 //
 // Both rebuild the forward's mask with the same planner and lane predicate
 // ("causal-mask-and-ragged-sequence-layouts", sixth paragraph); masked and
@@ -76,6 +79,34 @@ __device__ __forceinline__ bool wait_bar(Sync *sy, uint64_t *bar, uint32_t parit
 
 __device__ __forceinline__ void math_group_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// Factors that undo the power-of-two scaling of the fp16 copies (scale
+// exponents s_q, s_k, s_v, s_do from f16_copy_exponent): with Q' = 2^s_q Q
+// and so on, S' = 2^(s_q + s_k) S, dP' = 2^(s_v + s_do) dP, and the products
+// give dS' = 2^(s_v + s_do) dS, dV' = 2^s_do dV, dK' = 2^(s_v + s_do + s_q)
+// dK / scale, dQ' = 2^(s_v + s_do + s_k) dQ / scale.  Every factor is a
+// power of two (times the scale), so undoing them is exact.
+struct CopyScales {
+  float c2;    // S' -> log2 logit: scale log2(e) 2^-(s_q + s_k)
+  float dsc;   // D -> dP' units: 2^(s_v + s_do)
+  float bias;  // bias-tensor entry -> S' units: 2^(s_q + s_k) / scale
+  float g;     // 2^-(s_v + s_do), the first factor of dK and dQ
+  float gk, gq, gv;  // then dK: scale 2^-s_q, dQ: scale 2^-s_k; dV: 2^-s_do
+};
+
+__device__ __forceinline__ CopyScales copy_scales(const BwdParams &p) {
+  const int sq = f16_copy_exponent(p.amax[kAmaxQ]), sk = f16_copy_exponent(p.amax[kAmaxK]);
+  const int sv = f16_copy_exponent(p.amax[kAmaxV]), sd = f16_copy_exponent(p.amax[kAmaxDO]);
+  CopyScales c;
+  c.c2 = p.scale_log2 * exp2_int(-sq) * exp2_int(-sk);
+  c.dsc = exp2_int(sv + sd);
+  c.bias = (1.f / p.scale) * exp2_int(sq) * exp2_int(sk);
+  c.g = exp2_int(-(sv + sd));
+  c.gk = p.scale * exp2_int(-sq);
+  c.gq = p.scale * exp2_int(-sk);
+  c.gv = exp2_int(-sd);
+  return c;
 }
 
 // N consecutive bias-tensor entries of one row from key j0 on, divided by the
@@ -310,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb_last = key_row_begin(g.mask, j0 + kKeysA - 1, g.nq, g.nk);
     const int re_first = key_row_end(g.mask, g.window, j0, g.nq, g.nk);
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    const float c2 = p.scale_log2;
+    const CopyScales cs = copy_scales(p);
+    const float c2 = cs.c2;
     bool ok = true;
-    // lse2 (threads 0..63) or D (64..127) of one row of a step's query tile;
+    // lse2 (threads 0..63) or D (64..127, in dP' units) of one row of a step's query tile;
     // the next step's value is fetched while the current step computes.
     auto row_value = [&](int it) {
       const int c = tid & (kRowsA - 1);
@@ -320,13 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t at = (size_t)it_head(it) * p.total_q + g.q0 + i;
       // stored negated: the math below adds them
       if (tid < kRowsA) return i < g.nq ? -p.lse2[at] : -INFINITY;
-      return i < g.nq ? -p.delta[at] : 0.f;
+      return i < g.nq ? -p.delta[at] * cs.dsc : 0.f;
     };
     const bool fetcher = tid < 2 * kRowsA;
     float next_val = (n_it > 0 && fetcher) ? row_value(0) : 0.f;
-    // kTab: bias entries of step u for this key and the warp's 32 rows, over
-    // the positive scale, into S^T buffer u & 1 (rows or keys out of range: 0)
-    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
+    // kTab: bias entries of step u for this key and the warp's 32 rows, in
+    // S' units, into S^T buffer u & 1 (rows or keys out of range: 0)
+    const float inv_scale = kTab ? cs.bias : 0.f;
     auto load_bias = [&](int u, uint32_t (&bv)[32]) {
       const int ib = it_row0(u) + half * 32;
       const float *base = btab_row(p.btab, p.bss, p.bhs, p.brs, seq, it_head(u), 0) + j;
@@ -448,14 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 wk, wv;
-          wk.x = have ? pack_bf16x2(__uint_as_float(kv32[e]) * p.scale, __uint_as_float(kv32[e + 1]) * p.scale) : 0u;
-          wk.y = have ? pack_bf16x2(__uint_as_float(kv32[e + 2]) * p.scale, __uint_as_float(kv32[e + 3]) * p.scale) : 0u;
-          wk.z = have ? pack_bf16x2(__uint_as_float(kv32[e + 4]) * p.scale, __uint_as_float(kv32[e + 5]) * p.scale) : 0u;
-          wk.w = have ? pack_bf16x2(__uint_as_float(kv32[e + 6]) * p.scale, __uint_as_float(kv32[e + 7]) * p.scale) : 0u;
-          wv.x = have ? pack_bf16x2(__uint_as_float(vv32[e]), __uint_as_float(vv32[e + 1])) : 0u;
-          wv.y = have ? pack_bf16x2(__uint_as_float(vv32[e + 2]), __uint_as_float(vv32[e + 3])) : 0u;
-          wv.z = have ? pack_bf16x2(__uint_as_float(vv32[e + 4]), __uint_as_float(vv32[e + 5])) : 0u;
-          wv.w = have ? pack_bf16x2(__uint_as_float(vv32[e + 6]), __uint_as_float(vv32[e + 7])) : 0u;
+          // dK = (dK' 2^-(s_v + s_do)) scale 2^-s_q, dV = dV' 2^-s_do
+          auto kf = [&](int c1) { return __uint_as_float(kv32[c1]) * cs.g * cs.gk; };
+          auto vf = [&](int c1) { return __uint_as_float(vv32[c1]) * cs.gv; };
+          wk.x = have ? pack_bf16x2(kf(e), kf(e + 1)) : 0u;
+          wk.y = have ? pack_bf16x2(kf(e + 2), kf(e + 3)) : 0u;
+          wk.z = have ? pack_bf16x2(kf(e + 4), kf(e + 5)) : 0u;
+          wk.w = have ? pack_bf16x2(kf(e + 6), kf(e + 7)) : 0u;
+          wv.x = have ? pack_bf16x2(vf(e), vf(e + 1)) : 0u;
+          wv.y = have ? pack_bf16x2(vf(e + 2), vf(e + 3)) : 0u;
+          wv.z = have ? pack_bf16x2(vf(e + 4), vf(e + 5)) : 0u;
+          wv.w = have ? pack_bf16x2(vf(e + 6), vf(e + 7)) : 0u;
           *reinterpret_cast<uint4 *>(dkp + c * 32 + e) = wk;
           *reinterpret_cast<uint4 *>(dvp + c * 32 + e) = wv;
         }
@@ -674,18 +709,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_in = i < g.nq;
     const int t = g.q0 + i;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    const float c2 = p.scale_log2;
+    const CopyScales cs = copy_scales(p);
+    const float c2 = cs.c2;
     const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
     const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
     const float lse2 = row_in ? p.lse2[(size_t)h * p.total_q + t] : INFINITY;
-    const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] : 0.f;
+    const float D_i = row_in ? p.delta[(size_t)h * p.total_q + t] * cs.dsc : 0.f;  // dP' units
     const uint64_t c2x2 = f2(c2, c2), nl2 = f2(-lse2, -lse2), nd2 = f2(-D_i, -D_i);
     const float slope2 = kBias ? __ldg(p.slopes + h) * kLog2e : 0.f;
     const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     bool ok = true;
     // kTab: this warp's 64 keys of tile u's bias row into S buffer u & 1
     const float *brow = kTab && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, h, i) : nullptr;
-    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
+    const float inv_scale = kTab ? cs.bias : 0.f;  // entry -> S' units
     auto store_bias = [&](int u, const uint32_t (&bv)[64]) {
       const uint32_t col = t_lane + kColS + (u & 1) * kTileKeys + half * 64;
       tmem_st32(col, *reinterpret_cast<const uint32_t(*)[32]>(bv));
@@ -789,10 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 w;
-          w.x = have ? pack_bf16x2(__uint_as_float(q32[e]) * p.scale, __uint_as_float(q32[e + 1]) * p.scale) : 0u;
-          w.y = have ? pack_bf16x2(__uint_as_float(q32[e + 2]) * p.scale, __uint_as_float(q32[e + 3]) * p.scale) : 0u;
-          w.z = have ? pack_bf16x2(__uint_as_float(q32[e + 4]) * p.scale, __uint_as_float(q32[e + 5]) * p.scale) : 0u;
-          w.w = have ? pack_bf16x2(__uint_as_float(q32[e + 6]) * p.scale, __uint_as_float(q32[e + 7]) * p.scale) : 0u;
+          // dQ = (dQ' 2^-(s_v + s_do)) scale 2^-s_k
+          auto qf = [&](int c1) { return __uint_as_float(q32[c1]) * cs.g * cs.gq; };
+          w.x = have ? pack_bf16x2(qf(e), qf(e + 1)) : 0u;
+          w.y = have ? pack_bf16x2(qf(e + 2), qf(e + 3)) : 0u;
+          w.z = have ? pack_bf16x2(qf(e + 4), qf(e + 5)) : 0u;
+          w.w = have ? pack_bf16x2(qf(e + 6), qf(e + 7)) : 0u;
           *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
         }
       }
@@ -857,9 +895,11 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_
   a.group = p.hq / p.hkv;
   a.n_key_tiles = (p.max_k + kKeysA - 1) / kKeysA;
   a.n_row_tiles = (p.max_q + kTileRows - 1) / kTileRows;
-  snprintf(desc, desc_len, "bwd_pre+kv_to_f16+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d%s ctas_dkdv=%lld ctas_dq=%lld",
-           p.d, p.d, p.btab ? "_btab" : "", (long long)a.n_key_tiles * p.hkv * p.batch,
-           (long long)a.n_row_tiles * p.hq * p.batch);
+  snprintf(desc, desc_len,
+           "zero_rows+zero_rows+bwd_amax+bwd_pre+kv_to_f16%s+bwd_dkdv_tc_d%d+bwd_dq_tc_d%d%s "
+           "ctas_dkdv=%lld ctas_dq=%lld",
+           p.delta_ready ? "+fwd_tc2_delta" : "", p.d, p.d, p.btab ? "_btab" : "",
+           (long long)a.n_key_tiles * p.hkv * p.batch, (long long)a.n_row_tiles * p.hq * p.batch);
   if (a.n_key_tiles == 0 || a.n_row_tiles == 0) return cudaSuccess;
   // a bias tensor comes here only with a positive scale and no slopes
   if (p.btab) return p.d == 64 ? launch_d<64, false, true>(a, st) : launch_d<128, false, true>(a, st);

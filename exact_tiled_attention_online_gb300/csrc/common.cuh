@@ -236,6 +236,11 @@ struct FwdParams {
   // split-KV partial outputs (NULL when the plan writes o/lse directly)
   float *o_part, *lse_part;
   int n_splits;
+  // the backward's D term (fwd_tc2_delta.cu only): upstream gradient, its
+  // layout, and the [hq, total_q] output
+  const void *dout;
+  Strides sdo;
+  float *delta;
 };
 
 struct BwdParams {
@@ -255,8 +260,60 @@ struct BwdParams {
   int *err;
   float *delta;    // [hq, total_q]  D_i = dO_i . O_i
   float *lse2;     // [hq, total_q]  lse in log2 units (+inf for empty rows)
-  // fp16 copies of the inputs for the tensor-core backward (NULL otherwise)
+  int delta_ready; // D is written by the recomputing forward: the preprocess skips it
+  // fp16 copies of the inputs for the tensor-core backward (NULL otherwise),
+  // each scaled by a power of two (see f16_copy_exponent)
   void *q16, *do16, *k16, *v16;
+  // [4] largest bf16 magnitude (bit pattern) of q, k, v, dout: the copies'
+  // scale exponents follow from it
+  unsigned int *amax;
 };
+
+// ---------------------------------------------------------------------------
+// Scaled fp16 copies for the tensor-core backward.  Each of q, k, v and dout
+// is copied to fp16 multiplied by 2^s, with s chosen from the tensor's
+// largest magnitude so that it lands in [2^(kF16Top - 1), 2^kF16Top) = [4, 8).
+// A power of two changes no significand, so every bf16 element within 2^19
+// of the largest keeps its exact value (bf16 has 8 significant bits, fp16
+// 11 down to 2^-14 and subnormals to 2^-24), whatever the tensor's overall
+// magnitude.  The kernels undo the factors exactly: scores by 2^-(s_q + s_k),
+// dP by 2^-(s_v + s_do), and so on.  With every copy below 8 in magnitude,
+// |dS| = P |dP - D| <= 2 d 8 8 = 16384 (d = 128), inside fp16's 65504.
+// ---------------------------------------------------------------------------
+constexpr int kF16Top = 3;
+constexpr int kF16ExpLimit = 60;  // |s| bound: factors and their products stay normal fp32
+enum { kAmaxQ = 0, kAmaxK = 1, kAmaxV = 2, kAmaxDO = 3 };
+
+// s for a tensor whose largest |x| has the bf16 bit pattern `bits` (sign
+// cleared); 0 for an all-zero tensor.  amax lies in [2^(e-1), 2^e).
+__host__ __device__ __forceinline__ int f16_copy_exponent(unsigned int bits) {
+  if (bits == 0) return 0;
+  const int biased = (int)((bits >> 7) & 0xffu);
+  int e;
+  if (biased != 0) {
+    e = biased - 126;  // 1.m 2^(biased - 127)
+  } else {             // subnormal: m 2^-133, m in [2^(k-1), 2^k)
+    int m = (int)(bits & 0x7fu), k = 0;
+    while (m >> k) k++;
+    e = k - 133;
+  }
+  int s = kF16Top - e;
+  return s < -kF16ExpLimit ? -kF16ExpLimit : (s > kF16ExpLimit ? kF16ExpLimit : s);
+}
+
+// 2^s as an fp32 for |s| <= 126.
+__host__ __device__ __forceinline__ float exp2_int(int s) {
+  union {
+    unsigned int u;
+    float f;
+  } c;
+  c.u = (unsigned int)(127 + s) << 23;
+  return c.f;
+}
+
+// true when `bits` (bf16 pattern, sign cleared) is an infinity or NaN
+__host__ __device__ __forceinline__ bool bf16_bits_nonfinite(unsigned int bits) {
+  return (bits & 0x7f80u) == 0x7f80u;
+}
 
 }  // namespace attn

@@ -5,6 +5,7 @@
 // decode's partial outputs live in one file-scope device array instead of a
 // caller-provided workspace; the kernels are the ones attn_fwd launches.
 #include <stdio.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "plan.h"
@@ -53,9 +54,15 @@ extern "C" attn_status attn_fwd_static_scratch(
   attn_status st = internal_check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask,
                                         window, dtype);
   if (st != ATTN_OK) return st;
+  if (batch == 0 || total_q == 0 || max_q == 0 || total_k == 0) {
+    // No query rows (a no-op), or no keys (every row empty; no split plan):
+    // attn_fwd handles both without any scratch.
+    return attn_fwd(q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q, total_k,
+                    hq, hkv, d, scale, mask, window, bias_slopes, dtype, nullptr, 0, stream);
+  }
   TcPlan plan = choose_fwd_plan(batch, max_q, max_k, total_q, hq, hkv, d, window, dtype,
                                 internal_sm_count());
-  if (plan.kind != PLAN_TC_SPLIT || total_k == 0) {
+  if (plan.kind != PLAN_TC_SPLIT) {
     // Nothing to keep in scratch: the workspace-free attn_fwd path.
     return attn_fwd(q, k, v, o, lse, o_f32, cu_q, cu_k, batch, max_q, max_k, total_q, total_k,
                     hq, hkv, d, scale, mask, window, bias_slopes, dtype, nullptr, 0, stream);
@@ -93,10 +100,17 @@ extern "C" attn_status attn_fwd_static_scratch(
   p.n_splits = plan.n_splits;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   char desc[384];
+  desc[0] = 0;
   cudaError_t ce = launch_fwd_tc(p, plan, cs, desc, sizeof(desc));
   if (ce == cudaSuccess) ce = launch_combine(p, plan, cs);
-  char full[448];
-  snprintf(full, sizeof(full), "%s [static scratch]", desc);
+  char full[512];
+  snprintf(full, sizeof(full), "%s [static scratch]%s%s", desc,
+           ce == cudaSuccess ? "" : " [launch failed: ",
+           ce == cudaSuccess ? "" : cudaGetErrorString(ce));
+  if (ce != cudaSuccess) {
+    const size_t n = strlen(full);
+    snprintf(full + n, sizeof(full) - n, "]");
+  }
   internal_set_plan(full);
   return ce == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

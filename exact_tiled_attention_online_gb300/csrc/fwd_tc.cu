@@ -466,6 +466,7 @@ cudaError_t launch_d(const TcArgs &a, const CUtensorMap &mq, const CUtensorMap &
 
 cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st, char *desc,
                           size_t desc_len) {
+  snprintf(desc, desc_len, "fwd_tc_d%d (tensor map or grid size rejected)", p.d);
   TcArgs a;
   a.p = p;
   a.pack = plan.pack;

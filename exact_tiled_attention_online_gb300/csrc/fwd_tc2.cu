@@ -1,551 +1,10 @@
-// fwd_tc2.cu -- tensor-core prefill forward with two query tiles per CTA.
-//
-// Same arithmetic as fwd_tc.cu (the online-softmax recurrence of the
-// "formal-correctness" page, "The FlashAttention Proof"; masks from the tile
-// planner of common.cuh), scheduled so the tensor core never waits on one
-// softmax: a CTA owns 256 query rows of one head as two 128-row tiles A and B
-// that share every K/V tile, and the MMA thread interleaves their products
-//
-//   QK_A(n), QK_B(n), PV_A(n), QK_A(n+1), PV_B(n), QK_B(n+1), PV_A(n+1), ...
-//
-// so that while one softmax warpgroup turns its S into P, the tensor core is
-// busy with the other tile.  Warpgroups: the first holds warp 0 (TMA
-// producer) and warp 1 (TMEM allocation and MMA issue) and gives most of its
-// registers to the other two, which run the softmax of tile A (warps 4..7)
-// and tile B (warps 8..11), thread = row = TMEM lane.  TMEM: S_A, S_B, O_A,
-// O_B; each tile's bf16 P overwrites the second half of its S and feeds P V
-// from tensor memory, so P never passes through shared memory.  Shared
-// memory: Q_A, Q_B and a 2-stage K/V ring.
-//
-// With the extra registers a softmax thread loads its whole 128-score row
-// from TMEM with one wait, takes the max, and writes the 64 packed
-// probabilities back.  Instances add the linear positional bias in the softmax (kBias)
-// or an explicit bias tensor that the softmax warps store into S before
-// Q K^T accumulates onto it (kTab; then tile A's next Q K^T follows tile B's
-// P V, since A's bias waits for A's P V to finish reading P).
-#include <stdio.h>
-
-#include <type_traits>
-
-#include "common.cuh"
-#include "plan.h"
-#include "sm100.cuh"
-#include "tma_map.h"
+// fwd_tc2.cu -- launcher of the tensor-core prefill forward (the kernel
+// template is in fwd_tc2.cuh): the instances that write O, lse and, when
+// asked, the fp32 output.
+#include "fwd_tc2.cuh"
 
 namespace attn {
-using namespace sm100;
-
 namespace {
-
-constexpr int kThreads2 = 384;
-// Registers per thread: the launch gives every thread kRegsLaunch (the most
-// 384 threads can have); the control warpgroup drops to kRegsCtl and the two
-// softmax warpgroups rise to kRegsSoftmax.
-constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 80, kRegsSoftmax = 208;
-static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads2 * kRegsLaunch,
-              "the increases must not exceed what the decreases free");
-static_assert(kThreads2 * kRegsLaunch <= 65536, "register file");
-constexpr float kRescale2 = 8.0f;
-constexpr uint32_t kCols2 = 512;
-
-template <int D>
-struct Layout2 {
-  static constexpr int kChunk = 128 * 128;
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTile = kChunks * kChunk;
-  static constexpr int kQA = 0;
-  static constexpr int kK = 2 * kTile;      // [2] stages
-  static constexpr int kV = kK + 2 * kTile;  // [2] stages
-  static constexpr int kBar = kV + 2 * kTile;
-  static constexpr int kUsed = kBar + 256;
-  static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
-};
-
-struct Tc2Args {
-  FwdParams p;
-  int group;
-  int n_pairs;    // CTAs per (sequence, head), or per (sequence, head pair) with heads2
-  int heads2;     // 1: tiles A and B are the same 128 rows of two heads of one KV head
-};
-
-struct Bars2 {
-  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done[2];  // [tile A, tile B]
-  uint64_t b_full[2];  // kTab: the next tile's bias is in the tile's S columns
-  uint32_t tmem_base;
-  int abort;
-};
-
-__device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, int *err) {
-  if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
-  if (*reinterpret_cast<volatile int *>(&b->abort)) return false;
-  if (mbar_wait(bar, parity)) return true;
-  *reinterpret_cast<volatile int *>(&b->abort) = 1;
-  raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
-  return false;
-}
-
-// kPosScale: scale > 0 (the row max of the raw scores gives the max of the
-// logits).  kRoundedSum: also sum the bf16-rounded probabilities so the fp32
-// output is an exact convex combination of V rows (wanted when the caller
-// keeps that output for the backward); without it O is normalised by the
-// fp32 sum.  kBias: add the linear positional bias (with kPosScale false:
-// the bias must be in the logits before the max).  kTab: add an explicit
-// bias tensor, which the softmax warps write (divided by the positive scale)
-// into the tile's S columns before Q K^T accumulates onto it, so the scores
-// arrive biased and the softmax itself is unchanged.
-template <int D, bool kPosScale, bool kRoundedSum, bool kBias, bool kTab>
-__global__ void __launch_bounds__(kThreads2, 1)
-    fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
-  using L = Layout2<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_base = smem_u32(smem_raw);
-  uint8_t *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
-  Bars2 *b = reinterpret_cast<Bars2 *>(smem + L::kBar);
-  const FwdParams &p = a.p;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // One-dimensional grid, the tile rank slowest (longest causal rows of every
-  // (head, sequence) first).  Tiles A and B are rows [i0, i0 + 256) of head h,
-  // or with heads2 rows [i0, i0 + 128) of heads h and h + 1 (same KV head),
-  // which gives both tiles the same key range.
-  const int units = a.heads2 ? p.hq / 2 : p.hq;  // CTAs per (sequence, rank)
-  const int per_rank = units * p.batch;
-  const int rank = (int)blockIdx.x / per_rank;
-  const int h = ((int)blockIdx.x % units) * (a.heads2 ? 2 : 1);  // tile A's head
-  const int seq = ((int)blockIdx.x % per_rank) / units;
-  const int h_b = a.heads2 ? h + 1 : h;                            // tile B's head
-  const int rows_b = a.heads2 ? 0 : kTileRows;                     // tile B's row offset
-  const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
-  if (!g.ok) {
-    if (threadIdx.x == 0 && rank == 0 && h == 0) raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int i0 = (a.n_pairs - 1 - rank) * (kTileRows + rows_b);  // first row of tile A
-  if (i0 >= g.nq) return;
-  const KvRange kra = plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0, kTileRows, kTileKeys);
-  const KvRange krb =
-      plan_kv_tiles(g.mask, g.window, g.nq, g.nk, i0 + rows_b, kTileRows, kTileKeys);
-  // Key tiles run n = n0 + u for u in [0, N).  Tile X is active on the u in
-  // [lo_X, hi_X) (an empty range when none of its rows sees a key); the two
-  // ranges overlap or touch, because tile B's first row starts its keys no
-  // later than tile A's last row ends them, so [0, N) has no unused tile.
-  const bool act_a = kra.n_end > kra.n_begin, act_b = krb.n_end > krb.n_begin;
-  const int n0 = act_a ? kra.n_begin : krb.n_begin;
-  const int lo_a = act_a ? kra.n_begin - n0 : 0, hi_a = act_a ? kra.n_end - n0 : 0;
-  const int lo_b = act_b ? krb.n_begin - n0 : 0, hi_b = act_b ? krb.n_end - n0 : 0;
-  const int N = hi_a > hi_b ? hi_a : hi_b;
-  const int hk = h / a.group;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&b->q_full, 1);
-    for (int s = 0; s < 2; s++) {
-      mbar_init(&b->k_full[s], 1);
-      mbar_init(&b->v_full[s], 1);
-      mbar_init(&b->k_empty[s], 1);
-      mbar_init(&b->v_empty[s], 1);
-      mbar_init(&b->s_full[s], 1);
-      mbar_init(&b->p_full[s], 128);
-      mbar_init(&b->b_full[s], 128);
-      mbar_init(&b->pv_done[s], 1);
-    }
-    b->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&b->tmem_base, kCols2);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = b->tmem_base;
-  // TMEM columns: S_A 0, S_B 128, O_A 256, O_B 256 + D.
-  const uint32_t sQ = smem_u32(smem + L::kQA);
-  const uint32_t sK = smem_u32(smem + L::kK);
-  const uint32_t sV = smem_u32(smem + L::kV);
-
-  if (warp < 4) {
-    reg_dealloc<kRegsCtl>();
-    if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && N > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
-      for (int t2 = 0; t2 < 2; t2++)
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full, c * 64,
-                      t2 ? h_b : h, g.q0 + i0 + t2 * rows_b);
-      for (int n = 0; n < N; n++) {
-        const int st = n & 1, u = n >> 1;
-        const int key_row = g.k0 + (n0 + n) * kTileKeys;
-        if (n >= 2 && !wait2(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
-                      hk, key_row);
-        if (n >= 2 && !wait2(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st], c * 64,
-                      hk, key_row);
-      }
-    }
-    } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue
-    if (lane == 0 && N > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-      // Descriptors are built once; a byte offset below 256 KB adds to the
-      // start-address field (16-byte units) without carrying out of it.
-      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
-      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dV0 = smem_desc_sw128(sV, L::kChunk, 1024);
-      auto issue_qk = [&](int x, int st) {  // S_x = Q_x K^T
-        const uint64_t dq = dQ0 + (uint64_t)((x * L::kTile) >> 4);
-        const uint64_t dk = dK0 + (uint64_t)((st * L::kTile) >> 4);
-        const uint32_t d_tmem = tmem + (uint32_t)(x * kTileKeys);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk++) {
-          const uint64_t off = (uint64_t)((((kk >> 2) * L::kChunk) + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, (kTab || kk > 0) ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
-        const uint64_t dv = dV0 + (uint64_t)((st * L::kTile) >> 4);
-        const uint32_t d_tmem = tmem + 256u + (uint32_t)(x * D);
-        const uint32_t a_tmem = tmem + (uint32_t)(x * kTileKeys + 64);  // P: S columns [64, 128)
-#pragma unroll
-        for (int kk = 0; kk < kTileKeys / 16; kk++)
-          mma_bf16_ts(d_tmem, a_tmem + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv,
-                      (acc || kk > 0) ? 1u : 0u);
-      };
-      // Tile X's c-th product (c = n - lo_X) completes phase c of its
-      // s_full / p_full / pv_done barriers.
-      auto in_a = [&](int n) { return n >= lo_a && n < hi_a; };
-      auto in_b = [&](int n) { return n >= lo_b && n < hi_b; };
-      // kTab: Q K^T of tile X's c-th product accumulates onto the bias its
-      // softmax warps stored, announced by phase c of b_full[X]
-      bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
-      if (ok && in_a(0) && (!kTab || (ok = wait2(b, &b->b_full[0], 0, p.err)))) {
-        tc_fence_after();
-        issue_qk(0, 0);
-        mma_commit(&b->s_full[0]);
-      }
-      if (ok && in_b(0) && (!kTab || (ok = wait2(b, &b->b_full[1], 0, p.err)))) {
-        tc_fence_after();
-        issue_qk(1, 0);
-        mma_commit(&b->s_full[1]);
-      }
-      if (ok) mma_commit(&b->k_empty[0]);
-      for (int n = 0; ok && n < N; n++) {
-        const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
-        bool v_ready = false, k1_ready = false;
-        if (in_a(n)) {
-          if (!(ok = wait2(b, &b->p_full[0], (n - lo_a) & 1, p.err))) break;
-          if (!(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
-          v_ready = true;
-          tc_fence_after();
-          issue_pv(0, st, n > lo_a);
-          mma_commit(&b->pv_done[0]);
-        }
-        // kTab: tile A's next Q K^T waits for its bias, which waits for
-        // P_A V: tile B's P V goes first
-        if (!kTab && in_a(n1)) {
-          if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
-          k1_ready = true;
-          tc_fence_after();
-          issue_qk(0, st1);
-          mma_commit(&b->s_full[0]);
-        }
-        if (in_b(n)) {
-          if (!(ok = wait2(b, &b->p_full[1], (n - lo_b) & 1, p.err))) break;
-          if (!v_ready && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
-          tc_fence_after();
-          issue_pv(1, st, n > lo_b);
-          mma_commit(&b->pv_done[1]);
-        }
-        mma_commit(&b->v_empty[st]);
-        if (kTab && in_a(n1)) {
-          if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
-          k1_ready = true;
-          if (!(ok = wait2(b, &b->b_full[0], (n1 - lo_a) & 1, p.err))) break;
-          tc_fence_after();
-          issue_qk(0, st1);
-          mma_commit(&b->s_full[0]);
-        }
-        if (in_b(n1)) {
-          if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
-          if (kTab && !(ok = wait2(b, &b->b_full[1], (n1 - lo_b) & 1, p.err))) break;
-          tc_fence_after();
-          issue_qk(1, st1);
-          mma_commit(&b->s_full[1]);
-        }
-        if (n1 < N) mma_commit(&b->k_empty[st1]);
-      }
-    }
-    }
-  } else {
-    reg_alloc<kRegsSoftmax>();
-    // ------------------------------------------------------------ softmax
-    const int x = warp >= 8 ? 1 : 0;  // tile A (0) or B (1)
-    const int wq = warp & 3;          // TMEM lane quarter this warp may access
-    const int r = wq * 32 + lane;
-    const int hx = x ? h_b : h;         // this tile's head
-    const int i = i0 + x * rows_b + r;  // this thread's row
-    const bool row_in = i < g.nq;
-    const int t = g.q0 + i;
-    const int row_limit = row_key_limit(g.mask, i, g.nq, g.nk);
-    const int row_first = row_key_first(g.mask, g.window, i, g.nq, g.nk);
-    const KvRange &kr = x ? krb : kra;
-    const int n_mine = kr.n_end - kr.n_begin;  // products of this tile
-    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t s_col = t_lane + (uint32_t)(x * kTileKeys);
-    const uint32_t o_col = t_lane + 256u + (uint32_t)(x * D);
-    const float c2 = p.scale_log2;
-    const float cm = kPosScale ? c2 : 1.f;  // multiplier still to apply to raw scores
-    static_assert(!(kBias && kPosScale), "the bias needs the logits before the max");
-    static_assert(!kTab || (kPosScale && !kBias), "the tensor bias rides on the raw scores");
-    const float slope2 = kBias ? __ldg(p.slopes + hx) * kLog2e : 0.f;
-    // causal mask and positive scale: the bias is linear over every allowed key
-    const bool bias_linear = g.mask != ATTN_MASK_NONE && c2 > 0.f;
-    const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
-    float m_ref = -INFINITY, l = 0.f, lr = 0.f;
-    bool ok = true;
-    // kTab: this row's bias entries for key tile n, divided by the positive
-    // scale (so that c2 times the accumulated score is the biased logit in
-    // log2 units), into the tile's S columns; keys past the sequence and rows
-    // past it get 0 (their lanes are masked or never stored).
-    const float *brow = kTab && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, hx, i) : nullptr;
-    const float inv_scale = kTab ? 1.f / p.scale : 0.f;
-    // the loads are issued before the wait that gates the store, so their
-    // latency overlaps it
-    auto load_bias = [&](int n, uint32_t (&bv)[kTileKeys]) {
-      const int j0 = n * kTileKeys;
-      const bool vec = brow && j0 + kTileKeys <= g.nk &&
-                       ((reinterpret_cast<uintptr_t>(brow + j0) & 15) == 0);
-      if (vec) {
-#pragma unroll
-        for (int e = 0; e < kTileKeys; e += 4) {
-          const float4 f = __ldg(reinterpret_cast<const float4 *>(brow + j0 + e));
-          bv[e] = __float_as_uint(f.x * inv_scale);
-          bv[e + 1] = __float_as_uint(f.y * inv_scale);
-          bv[e + 2] = __float_as_uint(f.z * inv_scale);
-          bv[e + 3] = __float_as_uint(f.w * inv_scale);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kTileKeys; e++) {
-          const int j = j0 + e;
-          bv[e] = __float_as_uint(brow && j < g.nk ? __ldg(brow + j) * inv_scale : 0.f);
-        }
-      }
-    };
-    auto store_bias = [&](const uint32_t (&bv)[kTileKeys]) {
-#pragma unroll
-      for (int c = 0; c < kTileKeys / 32; c++)
-        tmem_st32(s_col + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(bv + 32 * c));
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&b->b_full[x]);
-    };
-    if (kTab && n_mine > 0) {
-      uint32_t bv[kTileKeys];
-      load_bias(kr.n_begin, bv);
-      store_bias(bv);
-    }
-    for (int it = 0; it < n_mine; it++) {
-      const int n = kr.n_begin + it;  // key tile in the sequence
-      ok = wait2(b, &b->s_full[x], it & 1, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // the whole row of 128 scores in one TMEM load instruction (measured 1%
-      // faster than four of 32 columns; one store of 64 columns for P was not)
-      uint32_t v[kTileKeys];
-      static_assert(kTileKeys == 128, "one 128-column load");
-      tmem_ld128(s_col, v);
-      tmem_wait_ld();
-      if (!kr.full(n)) {
-        // lanes outside [first, limit) of this row: first <= limit, so one
-        // unsigned compare tests both ends
-        const int first = row_first - n * kTileKeys;
-        const unsigned span = (unsigned)(row_limit - row_first);
-#pragma unroll
-        for (int e = 0; e < kTileKeys; e++)
-          if ((unsigned)(e - first) >= span) v[e] = 0xff800000u;
-      }
-      if constexpr (!kPosScale) {
-        const float dist0 = bound - (float)(n * kTileKeys);
-        if (kBias && bias_linear) {
-          // Every allowed key sits at or before the causal bound, so the bias
-          // is -slope2 (dist0 - e) with dist0 - e >= 0 exact in fp32, and a
-          // masked lane's -inf stays -inf (c2 > 0): z = y c2 - slope2 (dist0 - e),
-          // two lanes per instruction.
-          const uint64_t c2x2 = f2(c2, c2), ns2 = f2(-slope2, -slope2), d2 = f2(dist0, dist0);
-#pragma unroll
-          for (int e = 0; e < kTileKeys; e += 2) {
-            const uint64_t t2 = fadd2(d2, f2(-(float)e, -(float)(e + 1)));
-            const uint64_t z2 = ffma2(ns2, t2, fmul2(f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), c2x2));
-            float z0, z1;
-            f2_split(z2, z0, z1);
-            v[e] = __float_as_uint(z0);
-            v[e + 1] = __float_as_uint(z1);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < kTileKeys; e++) {
-            const float y = __uint_as_float(v[e]);
-            float z = y * c2;
-            if constexpr (kBias) z += pos_bias2(slope2, dist0, e);
-            v[e] = __float_as_uint(y == -INFINITY ? -INFINITY : z);
-          }
-        }
-      }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int e = 0; e < kTileKeys; e += 2)
-        m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      if (kPosScale) mt *= c2;
-      const float m_new = mt > m_ref + kRescale2 ? mt : m_ref;
-      const float alpha = m_new == m_ref ? 1.f : fast_exp2(m_ref - m_new);
-      const float base = m_new == -INFINITY ? 0.f : m_new;
-      // P = 2^(raw * c - base), two lanes per instruction; l sums fp32 P (for
-      // lse), lr the bf16-rounded P that P V uses (so O / lr is an exact
-      // convex combination of V rows).  Each half of 64 scores becomes 32
-      // packed bf16 pairs over S columns [64, 128): keys [0, 64) at 64, keys
-      // [64, 128) at 96.
-      const uint64_t cx2 = f2(cm, cm), nb2 = f2(-base, -base);
-      uint64_t s2[2] = {0, 0}, r2[2] = {0, 0};
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float x0, x1;
-          f2_split(ffma2(f2(__uint_as_float(v[64 * hh + e]), __uint_as_float(v[64 * hh + e + 1])),
-                         cx2, nb2),
-                   x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          const int k = e / 2;
-          s2[k & 1] = fadd2(s2[k & 1], f2(p0, p1));
-          pk[k] = pack_bf16x2(p0, p1);
-          if constexpr (kRoundedSum)
-            r2[k & 1] = fadd2(r2[k & 1], f2(__uint_as_float(pk[k] << 16),
-                                            __uint_as_float(pk[k] & 0xffff0000u)));
-        }
-        tmem_st32(s_col + 64 + 32 * hh, pk);
-      }
-      {
-        float a0, a1, b0, b1;
-        f2_split(fadd2(s2[0], s2[1]), a0, a1);
-        f2_split(fadd2(r2[0], r2[1]), b0, b1);
-        l = l * alpha + (a0 + a1);
-        lr = kRoundedSum ? lr * alpha + (b0 + b1) : l;
-      }
-      m_ref = m_new;
-      // S_x(n) landed after every earlier product of this thread, so the
-      // previous P V into O_x is complete: O_x may be rescaled now.
-      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; c++) {
-          uint32_t o32[32];
-          tmem_ld32(o_col + c * 32, o32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e++) o32[e] = __float_as_uint(__uint_as_float(o32[e]) * alpha);
-          tmem_st32(o_col + c * 32, o32);
-        }
-      }
-      tmem_wait_st();  // P (S columns [64, 128)) and any rescaled O are in place
-      tc_fence_before();
-      mbar_arrive(&b->p_full[x]);
-      if (kTab && it + 1 < n_mine) {
-        // the next tile's bias may overwrite S once P V has read P
-        uint32_t bv[kTileKeys];
-        load_bias(n + 1, bv);
-        ok = wait2(b, &b->pv_done[x], it & 1, p.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        store_bias(bv);
-      }
-    }
-    if (ok && n_mine > 0) {
-      ok = wait2(b, &b->pv_done[x], (n_mine - 1) & 1, p.err);
-      if (ok) tc_fence_after();
-    }
-    // ------------------------------------------------------------ epilogue
-    const bool have = __all_sync(0xffffffffu, ok) && n_mine > 0;
-    const float inv = lr > 0.f ? 1.f / lr : 0.f;
-    const float lse2 = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + toff(p.so, t, hx);
-#pragma unroll
-    for (int c = 0; c < D / 32; c++) {
-      uint32_t o32[32];
-      if (have) {
-        tmem_ld32(o_col + c * 32, o32);
-        tmem_wait_ld();
-      }
-      if (row_in) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w;
-          w.x = have ? pack_bf16x2(__uint_as_float(o32[e]) * inv, __uint_as_float(o32[e + 1]) * inv) : 0u;
-          w.y = have ? pack_bf16x2(__uint_as_float(o32[e + 2]) * inv, __uint_as_float(o32[e + 3]) * inv) : 0u;
-          w.z = have ? pack_bf16x2(__uint_as_float(o32[e + 4]) * inv, __uint_as_float(o32[e + 5]) * inv) : 0u;
-          w.w = have ? pack_bf16x2(__uint_as_float(o32[e + 6]) * inv, __uint_as_float(o32[e + 7]) * inv) : 0u;
-          *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
-        }
-        if (p.o_f32) {
-          float *df = p.o_f32 + ((size_t)t * p.hq + hx) * D + c * 32;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            float4 f;
-            f.x = have ? __uint_as_float(o32[e]) * inv : 0.f;
-            f.y = have ? __uint_as_float(o32[e + 1]) * inv : 0.f;
-            f.z = have ? __uint_as_float(o32[e + 2]) * inv : 0.f;
-            f.w = have ? __uint_as_float(o32[e + 3]) * inv : 0.f;
-            *reinterpret_cast<float4 *>(df + e) = f;
-          }
-        }
-      }
-    }
-    if (row_in && p.lse) p.lse[(size_t)hx * p.total_q + t] = have ? lse2 * kLn2 : -INFINITY;
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kCols2);
-  }
-}
-
-template <int D, bool kPos, bool kRs, bool kBias, bool kTab = false>
-cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                    const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs, kBias, kTab>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Layout2<D>::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
-  return cudaGetLastError();
-}
 
 template <int D>
 cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
@@ -566,24 +25,12 @@ cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap
 
 // Prefill plan (one head per tile, no key splits) with two query tiles per CTA.
 cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len) {
+  snprintf(desc, desc_len, "fwd_tc2_d%d (tensor map or grid size rejected)", p.d);
   Tc2Args a;
-  a.p = p;
-  a.group = p.hq / p.hkv;
-  // two heads of one KV head per CTA when the group pairs up: both tiles then
-  // have the same key range, no idle diagonal tile (windowed prefill 2%,
-  // linear bias 1.5% faster, causal unchanged); with a bias tensor it measured
-  // 7% slower, so those keep two row blocks of one head
-  a.heads2 = a.group % 2 == 0 && !p.btab ? 1 : 0;
-  const int rows_per_cta = a.heads2 ? kTileRows : 2 * kTileRows;
-  a.n_pairs = (p.max_q + rows_per_cta - 1) / rows_per_cta;
   CUtensorMap mq, mk, mv;
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_map(&mq, p.q, p.d, p.hq, p.total_q, 1, kTileRows, bf, p.sq.hs, p.sq.ts) ||
-      !make_map(&mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sk.hs, p.sk.ts) ||
-      !make_map(&mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sv.hs, p.sv.ts))
-    return cudaErrorInvalidValue;
-  const long long ctas = (long long)a.n_pairs * (a.heads2 ? p.hq / 2 : p.hq) * p.batch;
-  if (ctas >= (1LL << 31)) return cudaErrorInvalidValue;
+  long long ctas = 0;
+  int rows_per_cta = 0;
+  if (!setup_tc2(p, &a, &mq, &mk, &mv, &ctas, &rows_per_cta)) return cudaErrorInvalidValue;
   snprintf(desc, desc_len, "fwd_tc2_d%d%s ctas=%lld rows_per_cta=%d heads_per_cta=%d", p.d,
            p.btab ? "_btab" : "", ctas, rows_per_cta, a.heads2 ? 2 : 1);
   if (ctas == 0) return cudaSuccess;

@@ -55,6 +55,7 @@ inline TcPlan choose_fwd_plan(int batch, int max_q, int max_k, int total_q, int 
   }
   p.n_m_tiles = (max_q + p.tile_tokens - 1) / p.tile_tokens;
   const long long ctas = (long long)batch * (p.pack ? hkv : hq) * p.n_m_tiles;
+  if (ctas <= 0) return p;  // no query rows (an empty batch is a no-op): nothing to split
   int kv_tiles = (max_k + kTileKeys - 1) / kTileKeys;
   if (window > 0) {  // a bounded window: a tile's keys span window + tile_tokens - 1
     const long long span = (long long)window + p.tile_tokens - 1;

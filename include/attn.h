@@ -82,7 +82,7 @@ typedef enum {
   ATTN_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait expired              */
   ATTN_ERR_DEVICE_BOUNDS = 6,  /* cu_seqlens disagree with the sizes passed  */
   ATTN_ERR_SCRATCH_LIMIT = 7,  /* needs more than the static scratch holds   */
-  ATTN_ERR_DEVICE_RANGE = 8    /* a bf16 backward input is outside fp16 range */
+  ATTN_ERR_DEVICE_RANGE = 8    /* a bf16 backward input is infinite or NaN */
 } attn_status;
 
 typedef enum {
@@ -135,9 +135,8 @@ size_t attn_fwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
  *                May be NULL when not wanted.
  *   o_f32        optional output [total_q, n_heads_q, head_dim] fp32: the
  *                normalised output before its rounding to `dtype`.  Pass it
- *                on to attn_bwd, which then forms D_i = dO_i . O_i from it;
- *                with a bf16 O alone, the rounding error of O enters every
- *                gradient through D.  NULL skips it.
+ *                on to attn_bwd, which then forms D_i = dO_i . O_i from it
+ *                instead of recomputing that output.  NULL skips it.
  *   scale        finite softmax scale (usually 1/sqrt(head_dim)).
  *   workspace    device scratch of at least attn_fwd_workspace_size() bytes,
  *                256-byte aligned (may be NULL when that size is 0).
@@ -179,8 +178,11 @@ typedef struct {
  * contiguous layouts) and an optional explicit bias tensor `bias` (NULL:
  * none; both NULL is exactly attn_fwd).  Same results; ATTN_ERR_INVALID_ARG
  * for a stride that breaks the rules above, a negative bias stride or a bias
- * without data.  Calls with a bias tensor run on the CUDA-core kernels (one
- * warp per query row and head).
+ * without data.  bf16 calls with a bias tensor, a positive scale and no
+ * bias_slopes run on the tensor-core prefill kernel (the entries are stored
+ * into the score buffer before Q K^T accumulates onto them); other calls
+ * with a bias tensor (fp32, a non-positive scale, or slopes as well) run on
+ * the CUDA-core kernels (one warp per query row and head).
  */
 attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q,
                         const void *k, const void *v, void *o, float *lse,
@@ -195,10 +197,14 @@ attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
 /*
  * Workspace bytes attn_bwd needs: the per-row terms D_i = dO_i . O_i and the
  * base-2 logsumexp ([n_heads_q, total_q] fp32 each) and, for bf16, fp16
- * copies of q, dout, k and v: the tensor-core backward multiplies in fp16 so
- * that the probabilities P and the score gradients dS it feeds to the tensor
- * cores keep 11 significant bits (bf16 keeps 8, which is not enough for a
- * key seen by thousands of rows).  (size_t)-1 for bad arguments.
+ * copies of q, dout, k and v (plus 256 bytes for their largest magnitudes):
+ * the tensor-core backward multiplies in fp16 so that the probabilities P
+ * and the score gradients dS it feeds to the tensor cores keep 11
+ * significant bits (bf16 keeps 8, which is not enough for a key seen by
+ * thousands of rows).  Each copy is scaled by a power of two that brings the
+ * tensor's largest magnitude into [4, 8), so every element within 2^19 of
+ * it is copied exactly, at any overall magnitude of the inputs; the kernels
+ * undo the factors exactly.  (size_t)-1 for bad arguments.
  */
 size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
                                int total_q, int total_k, int n_heads_q,
@@ -213,14 +219,18 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
  * with dK and dV summed over the query heads that share each KV head
  * ("attention-algorithm-error-and-complexity-tests", third paragraph).
  *   o, lse   the forward's outputs for the same inputs.
- *   o_f32    the forward's optional fp32 output, or NULL: D_i is then formed
- *            from the rounded o.
+ *   o_f32    the forward's optional fp32 output, or NULL.  D_i must not
+ *            carry the rounding of O (with value rows that share a large
+ *            offset it would exceed the gradient tolerance), so for bf16
+ *            without o_f32 the backward first recomputes the fp32 output
+ *            with the prefill forward kernel, whose epilogue writes D_i
+ *            instead of O (one extra forward pass of work; pass o_f32 to
+ *            skip it).  fp32 calls form D_i from o itself.
  *   dq       [total_q, n_heads_q, head_dim]; dk, dv [total_k, n_heads_kv,
  *            head_dim]; type `dtype`.  Fully overwritten (rows no query
  *            reaches get zeros).
- * For bf16, q, k, v and dout must lie inside the fp16 range (|x| < 65504);
- * a larger value sets ATTN_ERR_DEVICE_RANGE on the device flag.  dq, dk and dv
- * must be 16-byte aligned.
+ * For bf16, an infinity or NaN in q, k, v or dout sets ATTN_ERR_DEVICE_RANGE
+ * on the device flag.  dq, dk and dv must be 16-byte aligned.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v,
                      const void *o, const float *lse, const float *o_f32,
@@ -238,7 +248,8 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
  * `strides` (NULL: contiguous) and the forward's explicit bias tensor `bias`
  * (NULL: none; both NULL is exactly attn_bwd), rebuilt in the recomputed
  * logits.  The workspace size does not depend on either.  With a bias tensor
- * the CUDA-core backward runs.
+ * the tensor-core backward runs under the same conditions as the forward's
+ * (bf16, positive scale, no bias_slopes); otherwise the CUDA-core backward.
  */
 attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bias, const void *q,
                         const void *k, const void *v, const void *o,

@@ -125,6 +125,32 @@ def test_forward_deterministic():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("lk", [(2048, 2048), (16384, 16384), (0, 0)])
+def test_empty_query_batch_is_a_no_op(lk):
+    """cu_seqlens_q = [0, 0, 0] against long key ranges: a legal call with no
+    query row ("causal-mask-and-ragged-sequence-layouts", fifth paragraph).
+    The forward, the backward and the workspace queries return OK and write
+    nothing (sentinel buffers stay as they were)."""
+    w = inputs.custom("noq", (0, 0), lk, 32, 8, 128, "bf16", BR, seed=2, backward=True)
+    x = inputs.make_inputs(w, device="cuda")
+    assert attn.fwd_workspace_size(w.batch, 0, w.max_k, 0, w.hq, w.hkv, w.d,
+                                   attn.DTYPE_BF16) >= 0
+    o = torch.empty((0, w.hq, w.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.hq, 0), dtype=torch.float32, device="cuda")
+    o2, lse2 = attn.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], 0,
+                        w.max_k, BR, w.scale, out=o, lse=lse)
+    assert o2.numel() == 0 and lse2.numel() == 0
+    dk = torch.full_like(x["k"], 7.0)
+    dv = torch.full_like(x["v"], 7.0)
+    dq, dk, dv = attn.bwd(x["q"], x["k"], x["v"], o, lse, x["dout"], x["cu_seqlens_q"],
+                          x["cu_seqlens_k"], 0, w.max_k, BR, w.scale, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert attn.get_device_error() == 0
+    # no query row reaches any key: every key's gradient is zero
+    assert dq.numel() == 0
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
 def test_bad_cu_seqlens_sets_device_flag():
     """cu_seqlens that run past total_q are caught on the device (no access
     beyond the buffers) and reported through the error flag."""

@@ -67,6 +67,18 @@ def test_short_window_decode_does_not_split(plan_bin):
     assert (kind, pack) == (2, 1) and splits >= 2
 
 
+def test_empty_query_batch_plans_without_split(plan_bin):
+    """No query rows (max_seqlen_q = 0, or batch = 0) is a legal no-op: the
+    planner returns a plan without a key split instead of dividing by its
+    zero CTA count ("causal-mask-and-ragged-sequence-layouts", fifth
+    paragraph: empty batches where the API permits them)."""
+    for shape in ((2, 0, 4096, 32, 8), (2, 0, 32768, 32, 8), (1, 0, 100000, 32, 32),
+                  (0, 0, 32768, 32, 8), (0, 16, 32768, 32, 8)):
+        kind, pack, tokens, splits = plan(plan_bin, *shape, 152)
+        assert kind == 1 and splits == 1, shape
+    assert plan(plan_bin, 2, 0, 32768, 32, 8, 152, window=4096)[3] == 1
+
+
 def test_fp32_takes_cuda_cores(plan_bin, tmp_path):
     src = SRC.replace("ATTN_DTYPE_BF16", "ATTN_DTYPE_FP32")
     (tmp_path / "p.cpp").write_text(src)

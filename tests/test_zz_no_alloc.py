@@ -71,6 +71,44 @@ def test_static_scratch_matches_workspace_forward(name, lq, lk):
         compare.check_lse(f"lse call {call}", lse, ref_lse)
 
 
+FALLTHROUGH = [  # shapes whose plan keeps nothing in the array: (name, lq, lk, mask)
+    ("no_query_rows", (0, 0), (2048, 4096), inputs.MASK_BOTTOM_RIGHT),
+    ("no_keys", (5, 3), (0, 0), inputs.MASK_BOTTOM_RIGHT),
+    ("q_longer_than_k", (64, 64), (32, 32), inputs.MASK_BOTTOM_RIGHT),
+    ("prefill", (300, 129), (300, 129), inputs.MASK_TOP_LEFT),
+]
+
+
+@pytest.mark.parametrize("name,lq,lk,mask", FALLTHROUGH, ids=[c[0] for c in FALLTHROUGH])
+def test_static_scratch_without_split(name, lq, lk, mask):
+    """Calls that do not take the split plan (no query rows, no keys, a
+    non-split prefill, Nq > Nk bottom-right) give attn_fwd's results; rows
+    with no allowed key get exact zeros and lse = -inf."""
+    w = inputs.custom(name, lq, lk, 32, 8, 128, "bf16", mask, seed=23)
+    x = inputs.make_inputs(w, device="cuda")
+    ref_o, ref_lse, ref_o32 = attn.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"],
+                                       x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale,
+                                       want_o_f32=True)
+    assert "splits=" not in attn.last_plan() or "splits=1" in attn.last_plan()
+    for call in range(2):
+        o = torch.full_like(ref_o, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        o32 = torch.full_like(ref_o32, float("nan"))
+        assert _call_static(x, w, o, lse, o32) == 0, f"call {call}"
+        torch.cuda.synchronize()
+        assert attn.get_device_error() == 0
+        compare.check_close(f"o call {call}", o, ref_o)
+        compare.check_close(f"o_f32 call {call}", o32, ref_o32)
+        compare.check_lse(f"lse call {call}", lse, ref_lse)
+        empty = torch.isneginf(lse)
+        if name in ("no_keys", "q_longer_than_k"):
+            assert empty.any()
+        if empty.any():
+            rows = empty.t().nonzero()  # (token, head) of every empty row
+            assert torch.count_nonzero(o[rows[:, 0], rows[:, 1]]) == 0
+            assert torch.count_nonzero(o32[rows[:, 0], rows[:, 1]]) == 0
+
+
 def test_static_scratch_refuses_oversize_problem():
     # 64 sequences x 8 queries x 128 query heads against 64k keys: the split
     # plan's partial outputs would need about 100 MB, over the 64 MiB array.

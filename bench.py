@@ -13,7 +13,9 @@ that are already resident in HBM:
   bias_tensor_prefill  the gqa_prefill shape with an explicit [B, 1, N, N]
                   bias tensor shared by the heads;
   bias_tensor_train    the train_fwd_bwd shape with such a tensor, forward +
-                  backward.
+                  backward;
+  train_fwd_bwd_plain  train_fwd_bwd without keeping the forward's fp32
+                  output, so the backward recomputes it for its D term.
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -21,6 +23,11 @@ tails reported ("attention-kernel-portability-and-benchmarking", fourth
 paragraph).  Work counts only allowed (query, key) pairs: 4 d flops per pair
 forward, 10 d backward; decode bytes are one read of the K/V cache plus Q, O
 and lse.
+
+Output: one JSON line on stdout (the summary: headline, roofline, e2e,
+clocks, CPU baselines, then every workload's value, unit, median time and
+roofline fraction at the end of the line) and one JSON line on stderr with
+the details (kernel plans, p90 and max times, memory).
 
 ``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of
 the same workload, on the host cores.
@@ -196,7 +203,7 @@ class Runner:
         from exact_tiled_attention_online_gb300 import attn
         self.attn = attn
         self.name = name
-        self.w = inputs.WORKLOADS[name]
+        self.w = inputs.WORKLOADS[name[:-len("_plain")] if name.endswith("_plain") else name]
         if batch_div > 1:  # a smaller case of the same kernels, for profiler captures
             w = self.w
             b = max(1, w.batch // batch_div)
@@ -206,8 +213,9 @@ class Runner:
         w = self.w
         self.o = torch.empty_like(x["q"])
         self.lse = torch.empty((w.hq, w.total_q), dtype=torch.float32, device=device)
+        self.keep_o32 = w.backward and not name.endswith("_plain")
         self.o32 = torch.empty(x["q"].shape, dtype=torch.float32, device=device) \
-            if w.backward else None
+            if self.keep_o32 else None
         ws = attn.fwd_workspace_size(w.batch, w.max_q, w.max_k, w.total_q, w.hq, w.hkv, w.d,
                                      attn.DTYPE_BF16, w.window)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
@@ -223,6 +231,7 @@ class Runner:
             if w.bias_tensor else None
         self.btab = None if self.btab_cpu is None else self.btab_cpu.to(device)
         self.plans = []
+        self.ws_bytes = self.ws.numel() + (self.bws.numel() if w.backward else 0)
 
     def run(self):
         a, w, x = self.attn, self.w, self.x
@@ -277,14 +286,21 @@ def time_gpu(args, rank, world, device):
     torch.cuda.set_device(device)
     names = [n.strip() for n in args.workloads.split(",") if n.strip()]
     runners = {}
-    for n in names:
-        big = n.startswith("decode") or n in ("train_fwd_bwd", "bias_tensor_train")
+    memory = {}
+    for n in names:  # each workload's buffers, then its first run, with its memory figures
+        big = n.startswith("decode") or n.startswith("train_fwd_bwd") or n == "bias_tensor_train"
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated(device)
+        torch.cuda.reset_peak_memory_stats(device)
         runners[n] = Runner(n, device, device if big else "cpu", args.batch_div)
+        runners[n].run()
+        torch.cuda.synchronize()
+        memory[n] = {"workspace_bytes": int(runners[n].ws_bytes),
+                     "buffers_bytes": int(torch.cuda.memory_allocated(device) - before),
+                     "peak_allocated_bytes": int(torch.cuda.max_memory_allocated(device) - before),
+                     "reserved_bytes": int(torch.cuda.memory_reserved(device))}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
-
-    for r in runners.values():  # first run, then validate
-        r.run()
     torch.cuda.synchronize()
     if attn.get_device_error() != 0:
         raise RuntimeError("device error flag set during the first run")
@@ -322,14 +338,33 @@ def time_gpu(args, rank, world, device):
     if attn.get_device_error() != 0:
         raise RuntimeError("device error flag set during the timed steps")
 
+    # the headline again with L2 warm: back-to-back launches, no flush
+    warm = {}
+    if HEADLINE in runners:
+        r = runners[HEADLINE]
+        ev = []
+        for _ in range(args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            r.run()
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        warm[HEADLINE] = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+
     per = {}
     for n, r in runners.items():
         ms = sorted(e0.elapsed_time(e1) for e0, e1 in events[n])
         work, unit = r.work()
         per[n] = {"ms_median": statistics.median(ms), "ms_p90": ms[int(0.9 * (len(ms) - 1))],
                   "ms_max": ms[-1], "work": work, "unit": unit, "plan": r.plans,
-                  "kernels": r.kernels_per_run()}
-    return runners, per, wall, clocks.summary(), validated
+                  "kernels": r.kernels_per_run(), "memory": memory[n]}
+        if n in warm:
+            per[n]["ms_median_l2_warm"] = warm[n]
+    per_total = {"max_memory_allocated": int(torch.cuda.max_memory_allocated(device)),
+                 "max_memory_reserved": int(torch.cuda.max_memory_reserved(device))}
+    return runners, per, wall, clocks.summary(), validated, per_total
 
 
 def reduce_max(x: float, world: int, device) -> float:
@@ -414,9 +449,24 @@ def e2e_headline(args, r: Runner, device):
     return ms, h2d, d2h
 
 
-def cpu_baseline(workload: str, budget_s: float = 12.0):
+def set_oracle_threads(n):
+    """OpenMP thread count for the oracle's next parallel regions (those
+    started from this thread); None leaves the default (all cores)."""
+    import ctypes
+    try:
+        gomp = ctypes.CDLL("libgomp.so.1")
+    except OSError:
+        return False
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    gomp.omp_set_num_threads(int(n) if n else int(os.environ.get("OMP_NUM_THREADS", cores)))
+    return True
+
+
+def cpu_baseline(workload: str, budget_s: float = 12.0, threads=None, repeats: int = 1):
     """The oracle, as it stands, on a bounded sample of the workload: random
-    (token, head) rows of the forward, timed on the host cores."""
+    (token, head) rows of the forward (every row when the sample would cover
+    the workload), timed on the host cores; the median of ``repeats`` runs.
+    ``threads``: OpenMP threads (None: all cores)."""
     import oracle
     w = inputs.WORKLOADS[workload]
     x = inputs.make_inputs(w)
@@ -426,9 +476,15 @@ def cpu_baseline(workload: str, budget_s: float = 12.0):
     v = x["v"].double().numpy()
     cq, ck = x["cu_seqlens_q"].numpy(), x["cu_seqlens_k"].numpy()
     orc = oracle.default()
+    set_oracle_threads(threads)
+    all_rows = w.total_q * w.hq
 
     def sample(n):
-        rows = np.stack([rng.integers(w.total_q, size=n), rng.integers(w.hq, size=n)], 1)
+        if n >= all_rows:  # the whole workload
+            rows = np.stack(np.meshgrid(np.arange(w.total_q), np.arange(w.hq), indexing="ij"),
+                            -1).reshape(-1, 2)
+        else:
+            rows = np.stack([rng.integers(w.total_q, size=n), rng.integers(w.hq, size=n)], 1)
         t0 = time.perf_counter()
         orc.fwd(q, k, v, cq, ck, w.scale, w.mask, rows=rows, window=w.window)
         dt = time.perf_counter() - t0
@@ -440,14 +496,32 @@ def cpu_baseline(workload: str, budget_s: float = 12.0):
             pairs += row_keys(w.mask, int(t - cq[s]), int(nq), int(nk), w.window)
         return dt, 4.0 * w.d * pairs
 
-    dt, fl = sample(64)
-    n = int(min(200000, max(64, 64 * budget_s / max(dt, 1e-3))))
-    dt, fl = sample(n)
+    dt, fl = sample(min(64, all_rows))
+    n = int(min(200000, all_rows, max(64, 64 * budget_s / max(dt, 1e-3))))
+    runs = [sample(n) for _ in range(max(1, repeats))]
+    rates = sorted(f / d / 1e12 for d, f in runs)
+    secs = sorted(d for d, _ in runs)
+    set_oracle_threads(None)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    threads = int(os.environ.get("OMP_NUM_THREADS", cores))
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, threads),
-            "kind": "oracle", "seconds": dt,
-            "sample": f"{n} random (token, head) rows of {workload}, forward, fp64"}
+    used = int(threads) if threads else min(cores, int(os.environ.get("OMP_NUM_THREADS", cores)))
+    what = "every (token, head) row" if n >= all_rows else f"{n} random (token, head) rows"
+    return {"value": statistics.median(rates), "unit": "TFLOP/s", "cores": used,
+            "kind": "oracle", "seconds": statistics.median(secs), "repeats": len(runs),
+            "sample": f"{what} of {workload}, forward, fp64"}
+
+
+def cpu_baseline_legs(budget_s: float = 1.5):
+    """The oracle on the three forward workloads the CPU can take in part
+    (tiny fp32, packed ragged, GQA prefill), single-core and on all cores,
+    median of 3 runs each ("attention-kernel-portability-and-benchmarking",
+    fourth and fifth paragraphs: medians, the inputs and the conditions)."""
+    legs = {}
+    for name in ("tiny_fp32", "varlen_causal", "gqa_prefill"):
+        for threads in (1, None):
+            r = cpu_baseline(name, budget_s=budget_s, threads=threads, repeats=3)
+            legs[f"{name}@{r['cores']}c"] = {"tflops": r["value"], "s": r["seconds"],
+                                             "sample": r["sample"]}
+    return legs
 
 
 def run_sweep(args):
@@ -512,7 +586,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads",
                     default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
-                            "window_prefill,bias_prefill,bias_tensor_prefill,bias_tensor_train")
+                            "window_prefill,bias_prefill,bias_tensor_prefill,bias_tensor_train,"
+                            "train_fwd_bwd_plain")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -545,7 +620,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local)
-    runners, per, wall, clocks, validated = time_gpu(args, rank, world, device)
+    runners, per, wall, clocks, validated, mem_total = time_gpu(args, rank, world, device)
 
     head = per[HEADLINE] if HEADLINE in per else next(iter(per.values()))
     head_name = HEADLINE if HEADLINE in per else next(iter(per))
@@ -573,7 +648,10 @@ def main():
                     "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
         workloads[n] = {"value": v, "unit": d["unit"], "ms_median": ms, "ms_p90": d["ms_p90"],
-                        "ms_max": d["ms_max"], "roofline": roof, "plan": d["plan"]}
+                        "ms_max": d["ms_max"], "roofline": roof, "plan": d["plan"],
+                        "memory": d["memory"]}
+        if "ms_median_l2_warm" in d:
+            workloads[n]["ms_median_l2_warm"] = d["ms_median_l2_warm"]
 
     out = {"metric": METRIC, "value": value, "unit": head["unit"], "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -587,7 +665,8 @@ def main():
                       "l2": "flushed before every timed workload (256 MiB write)",
                       "parallelism": f"replicas x{world}, no collective"},
            "gpu_launches": sum(d["kernels"] for d in per.values()) * args.steps,
-           "clocks": clocks, "workloads": workloads, "validated": validated}
+           "clocks": clocks,
+           "validated": {n: v["ok"] for n, v in validated.items()}}
 
     hw = workloads[head_name]
     roof = dict(hw["roofline"])
@@ -605,8 +684,27 @@ def main():
                       "schedule": "pipelined: copies in, kernel, copies out on three streams, "
                                   "two buffer sets"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(head_name)
+        out["cpu_baseline"] = cpu_baseline(head_name, repeats=3)
+        out["cpu_baseline_legs"] = {k: round(v["tflops"], 6)
+                                    for k, v in cpu_baseline_legs().items()}
+    out["memory"] = {"max_allocated_mb": round(mem_total["max_memory_allocated"] / 2**20, 1),
+                     "max_reserved_mb": round(mem_total["max_memory_reserved"] / 2**20, 1)}
+    if HEADLINE in workloads and "ms_median_l2_warm" in workloads[HEADLINE]:
+        out["l2_warm"] = {"workload": HEADLINE,
+                          "ms_median": workloads[HEADLINE]["ms_median_l2_warm"],
+                          "value": rate(per[HEADLINE]["work"] * world, per[HEADLINE]["unit"],
+                                        workloads[HEADLINE]["ms_median_l2_warm"])}
+    # every workload, compact, at the end of the line: value, unit, median ms,
+    # roofline fraction, workspace MiB (the details go to stderr)
+    out["workloads"] = {n: [round(wv["value"], 1), "GB/s" if wv["unit"] == "GB/s" else "TF",
+                            round(wv["ms_median"], 4), round(wv["roofline"]["frac"], 3),
+                            round(wv["memory"]["workspace_bytes"] / 2**20, 1)]
+                        for n, wv in workloads.items()}
+    out["workloads_fields"] = "value, unit, ms_median, roofline frac, workspace MiB"
     if rank == 0:
+        detail = {"detail": True, "workloads": workloads, "validated": validated,
+                  "memory_total": mem_total}
+        print(json.dumps(detail), file=sys.stderr)
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()

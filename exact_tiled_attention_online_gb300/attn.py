@@ -29,10 +29,6 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too sm
           7: "needs more than the static scratch holds",
           8: "a backward input holds an infinity or NaN"}
 
-_SYMBOLS = ["attn_fwd", "attn_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_fwd_workspace_size", "attn_bwd_workspace_size",
-            "attn_mask_probe", "attn_get_device_error", "attn_status_string",
-            "attn_last_plan", "attn_version"]
-
 
 class AttnStrides(ctypes.Structure):
     """``attn_strides``: {token stride, head stride} in elements per tensor."""
@@ -92,6 +88,8 @@ def library() -> ctypes.CDLL:
     L.attn_last_plan.restype = ctypes.c_char_p
     L.attn_version.argtypes = []
     L.attn_version.restype = I
+    L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.attn_set_wait_limit_ns.restype = None
     _lib = L
     return L
 
@@ -293,6 +291,12 @@ def mask_probe(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, 
 
 def get_device_error(stream=None) -> int:
     return library().attn_get_device_error(_stream(stream))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound of every wait inside the kernels for the following calls (0:
+    the 2 s default); see ``attn_set_wait_limit_ns`` in include/attn.h."""
+    library().attn_set_wait_limit_ns(int(ns))
 
 
 def last_plan() -> str:

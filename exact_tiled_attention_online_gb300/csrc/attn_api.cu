@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "plan.h"
 
@@ -44,6 +46,10 @@ static int *device_error_ptr() {
 }
 
 static thread_local char t_plan[512] = "none";
+
+// Bound of every device wait, in ns (0: the kernels' 2 s default); set by
+// attn_set_wait_limit_ns, read by every call.
+static std::atomic<unsigned long long> g_wait_ns{0};
 
 static void set_plan(const char *s) {
   snprintf(t_plan, sizeof(t_plan), "%s", s);
@@ -122,6 +128,7 @@ attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, i
   return check_sizes(batch, max_q, max_k, total_q, total_k, hq, hkv, d, mask, window, dtype);
 }
 int internal_sm_count() { return sm_count(); }
+unsigned long long internal_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 void internal_set_plan(const char *s) { set_plan(s); }
 
 }  // namespace attn
@@ -148,6 +155,8 @@ const char *attn_status_string(attn_status s) {
 }
 
 const char *attn_last_plan(void) { return t_plan; }
+
+void attn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
 
 size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int hq, int hkv,
                                int d, int window, attn_dtype dtype) {
@@ -218,6 +227,7 @@ attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
     return ATTN_ERR_INVALID_ARG;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   if (batch == 0 || total_q == 0 || max_q == 0) {
     set_plan("empty");
     return ATTN_OK;
@@ -342,6 +352,7 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
     return ATTN_ERR_INVALID_ARG;
   p.err = device_error_ptr();
   if (!p.err) return ATTN_ERR_CUDA;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   char *ws = static_cast<char *>(workspace);
   const BwdLayout wl = bwd_layout(total_q, total_k, hq, hkv, d, dtype);
   p.delta = reinterpret_cast<float *>(ws + wl.delta);
@@ -393,6 +404,7 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
       fp.sq = p.sq; fp.sk = p.sk; fp.sv = p.sv;
       fp.err = p.err;
       fp.dout = dout; fp.sdo = p.sdo; fp.delta = p.delta;
+      fp.wait_ns = p.wait_ns;
       ce = launch_fwd_tc2_delta(fp, cs);
     }
     if (ce == cudaSuccess) ce = launch_bwd_tc(p, cs, desc, sizeof(desc));

@@ -328,25 +328,44 @@ __device__ __forceinline__ unsigned int max_bits8(const uint4 w) {
 
 // amax[t] = max over tensor t of |x| (bf16 bits, sign cleared; the caller
 // zeroes amax first); an infinity or NaN anywhere sets ATTN_ERR_DEVICE_RANGE.
+// Four independent 16-byte loads per thread and step keep enough bytes in
+// flight; one atomic per block and tensor (a per-warp atomic on one address
+// serialised tens of thousands of them).
 __global__ void __launch_bounds__(256) bwd_amax_kernel(const AmaxArgs a) {
+  __shared__ unsigned int part[4][8];
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t first = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int t = 0; t < 4; t++) {
     const AmaxJob &j = a.job[t];
+    const size_t n = (size_t)j.n8;
     unsigned int m = 0;
     if (j.flat) {
       const uint4 *src = reinterpret_cast<const uint4 *>(j.base);
-      for (size_t i = first; i < (size_t)j.n8; i += stride) m = max(m, max_bits8(__ldg(src + i)));
+      size_t i = first;
+      for (; i + 3 * stride < n; i += 4 * stride) {
+        const uint4 w0 = __ldg(src + i), w1 = __ldg(src + i + stride);
+        const uint4 w2 = __ldg(src + i + 2 * stride), w3 = __ldg(src + i + 3 * stride);
+        m = max(m, max(max(max_bits8(w0), max_bits8(w1)), max(max_bits8(w2), max_bits8(w3))));
+      }
+      for (; i < n; i += stride) m = max(m, max_bits8(__ldg(src + i)));
     } else {
-      for (size_t i = first; i < (size_t)j.n8; i += stride) {
+      for (size_t i = first; i < n; i += stride) {
         const size_t row = i / j.per_row, c8 = i % j.per_row;
         const long long tok = (long long)(row / j.heads), h = (long long)(row % j.heads);
         m = max(m, max_bits8(__ldg(reinterpret_cast<const uint4 *>(j.base + toff(j.s, tok, h)) + c8)));
       }
     }
     m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0 && m != 0) {
+    if (lane == 0) part[t][warp] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    const int t = threadIdx.x;
+    unsigned int m = 0;
+    for (int w = 0; w < 8; w++) m = max(m, part[t][w]);
+    if (m != 0) {
       if (bf16_bits_nonfinite(m)) raise_error(a.err, ATTN_ERR_DEVICE_RANGE);
       atomicMax(a.amax + t, m);
     }
@@ -375,11 +394,11 @@ cudaError_t launch_bwd_amax(const BwdParams &p, cudaStream_t st) {
   a.amax = p.amax;
   a.err = p.err;
   if (most == 0) return cudaSuccess;
-  long long blocks = (most + 255) / 256;
+  long long blocks = (most + 4 * 256 - 1) / (4 * 256);  // four 16-byte loads per thread
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long cap = 8LL * (sms > 0 ? sms : 152);  // 8 blocks of 256 per SM
+  const long long cap = 8LL * (sms > 0 ? sms : 152);  // 8 blocks of 256 per SM: one full wave
   if (blocks > cap) blocks = cap;
   bwd_amax_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();

@@ -65,13 +65,17 @@ struct BwdTcArgs {
 };
 
 struct Sync {
+  uint64_t limit_ns;  // bound of every wait of this call
   int abort;
+  // for a drain after an early exit: single-tile fills (0 / 1), ring fills
+  // the producer issued, and whether the MMA thread issued any product
+  int filled_one, filled_a, filled_b, mma_issued;
 };
 
 __device__ __forceinline__ bool wait_bar(Sync *sy, uint64_t *bar, uint32_t parity, int *err) {
   if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (*reinterpret_cast<volatile int *>(&sy->abort)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, sy->limit_ns)) return true;
   *reinterpret_cast<volatile int *>(&sy->abort) = 1;
   raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
   return false;
@@ -163,9 +167,12 @@ struct BarsA {
   // waits, which the tensor pipe's short issue queue does not hide, few.
   uint64_t kv_full, qdo_full[kStagesA], qdo_empty[kStagesA], st_full[2], ps_full[2], mm_done;
   uint64_t b_full[2], s_free[2];  // kTab: bias stored in S^T buffer t / buffer t read by dV, dK
+  uint64_t drain;  // the MMA thread's products have all completed
   uint32_t tmem_base;
   Sync sync;
 };
+
+static_assert(sizeof(BarsA) <= 512, "barrier block fits its shared-memory slot");
 
 // kBias: add the linear positional bias to the recomputed logits.  kTab: an
 // explicit bias tensor; the math warps store a step's entries (over the
@@ -220,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b->b_full[s], 256);
       mbar_init(&b->s_free[s], 1);
     }
+    mbar_init(&b->drain, 1);
+    b->sync.limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->sync.abort = 0;
+    b->sync.filled_one = b->sync.filled_a = b->sync.filled_b = b->sync.mma_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -248,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
+      int filled = 0;  // Q / dO ring fills (stage = fill % kStagesA)
       mbar_arrive_expect_tx(&b->kv_full, 2 * L::kKV);
       for (int c = 0; c < L::kChunks; c++) {
         tma_load_3d(smem + L::kK + c * kChunk128, &tm_k, &b->kv_full, c * 64, hk, g.k0 + j0);
@@ -258,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = it_head(it), tok = g.q0 + it_row0(it);
         if (it >= kStagesA && !wait_bar(&b->sync, &b->qdo_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->qdo_full[st], 2 * L::kQT);
+        filled++;
         for (int c = 0; c < L::kChunks; c++) {
           tma_load_3d(smem + L::kQ + st * L::kQT + c * kChunk64, &tm_q, &b->qdo_full[st], c * 64, h,
                       tok);
@@ -265,9 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       h, tok);
         }
       }
+      b->sync.filled_one = 1;
+      b->sync.filled_a = filled;
     }
   } else if (warp == 1) {
     if (lane == 0 && n_it > 0) {
+      b->sync.mma_issued = 1;
       constexpr uint32_t idesc_s = idesc_f16_f32(128, kRowsA, 0, 0);
       constexpr uint32_t idesc_g = idesc_f16_f32(128, D, 0, 1);
       // Descriptors built once; byte offsets below 256 KB add to the
@@ -500,6 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A block in which a wait gave up may still have copies and products in
+  // flight: drain them before the tensor memory is freed (the flag is only
+  // set before the barrier above).
+  if (*reinterpret_cast<volatile int *>(&b->sync.abort)) {
+    if (threadIdx.x == 0) {
+      bool drained = drain_phase(&b->kv_full, b->sync.filled_one);
+      for (int st = 0; st < kStagesA; st++)
+        drained = drain_phase(&b->qdo_full[st], ring_armed(b->sync.filled_a, st, kStagesA)) && drained;
+      if (!drained) raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    }
+    if (threadIdx.x == 32 && b->sync.mma_issued && !drain_mma(&b->drain))
+      raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -531,9 +561,12 @@ struct BarsB {
   uint64_t qdo_full, k_full[kStagesK], v_full[2], k_empty[kStagesK], v_empty[2], s_full[2],
       dp_full, dp_free, ds_full, dq_done;
   uint64_t b_full[2], s_free[2];  // kTab: bias stored in S buffer t / buffer t read by dQ
+  uint64_t drain;  // the MMA thread's products have all completed
   uint32_t tmem_base;
   Sync sync;
 };
+
+static_assert(sizeof(BarsB) <= 256, "barrier block fits its shared-memory slot");
 
 // kTab: an explicit bias tensor; the math warps store a tile's entries (over
 // the positive scale) into its S buffer and S = Q K^T accumulates onto them.
@@ -589,7 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&b->ds_full, 256);
     mbar_init(&b->dq_done, 1);
+    mbar_init(&b->drain, 1);
+    b->sync.limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->sync.abort = 0;
+    b->sync.filled_one = b->sync.filled_a = b->sync.filled_b = b->sync.mma_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -610,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      int filled_k = 0, filled_v = 0;  // K ring fills (fill % kStagesK), V ring fills (fill % 2)
       mbar_arrive_expect_tx(&b->qdo_full, 2 * L::kTile);
       for (int c = 0; c < L::kChunks; c++) {
         tma_load_3d(smem + L::kQ + c * kChunk128, &tm_q, &b->qdo_full, c * 64, h, g.q0 + i0);
@@ -621,18 +658,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key_row = g.k0 + (n_first + jj) * kTileKeys;
         if (jj >= kStagesK && !wait_bar(&b->sync, &b->k_empty[ks], (ku - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->k_full[ks], L::kTile);
+        filled_k++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk128, &tm_k, &b->k_full[ks], c * 64,
                       hk, key_row);
         if (jj >= 2 && !wait_bar(&b->sync, &b->v_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+        filled_v++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kV + st * L::kTile + c * kChunk128, &tm_v, &b->v_full[st], c * 64,
                       hk, key_row);
       }
+      b->sync.filled_one = 1;
+      b->sync.filled_a = filled_k;
+      b->sync.filled_b = filled_v;
     }
   } else if (warp == 1) {
     if (lane == 0 && n_tiles > 0) {
+      b->sync.mma_issued = 1;
       constexpr uint32_t idesc_s = idesc_f16_f32(128, kTileKeys, 0, 0);
       constexpr uint32_t idesc_q = idesc_f16_f32(128, D, 0, 1);
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024), dDO0 = smem_desc_sw128(sDO, 16, 1024);
@@ -839,6 +882,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A block in which a wait gave up may still have copies and products in
+  // flight: drain them before the tensor memory is freed (the flag is only
+  // set before the barrier above).
+  if (*reinterpret_cast<volatile int *>(&b->sync.abort)) {
+    if (threadIdx.x == 0) {
+      bool drained = drain_phase(&b->qdo_full, b->sync.filled_one);
+      for (int ks = 0; ks < kStagesK; ks++)
+        drained = drain_phase(&b->k_full[ks], ring_armed(b->sync.filled_a, ks, kStagesK)) && drained;
+      for (int st = 0; st < 2; st++)
+        drained = drain_phase(&b->v_full[st], ring_armed(b->sync.filled_b, st, 2)) && drained;
+      if (!drained) raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    }
+    if (threadIdx.x == 32 && b->sync.mma_issued && !drain_mma(&b->drain))
+      raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

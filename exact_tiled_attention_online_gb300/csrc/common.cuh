@@ -241,6 +241,7 @@ struct FwdParams {
   const void *dout;
   Strides sdo;
   float *delta;
+  unsigned long long wait_ns;  // bound of every device wait (0: the 2 s default)
 };
 
 struct BwdParams {
@@ -267,6 +268,7 @@ struct BwdParams {
   // [4] largest bf16 magnitude (bit pattern) of q, k, v, dout: the copies'
   // scale exponents follow from it
   unsigned int *amax;
+  unsigned long long wait_ns;  // bound of every device wait (0: the 2 s default)
 };
 
 // ---------------------------------------------------------------------------

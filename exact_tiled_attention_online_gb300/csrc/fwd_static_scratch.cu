@@ -19,6 +19,7 @@ int *internal_error_flag();
 attn_status internal_check_sizes(int batch, int max_q, int max_k, int total_q, int total_k,
                                  int hq, int hkv, int d, int mask, int window, int dtype);
 int internal_sm_count();
+unsigned long long internal_wait_ns();
 void internal_set_plan(const char *s);
 
 // The scratch array: ATTN_STATIC_SCRATCH_BYTES on every device that loads the
@@ -92,6 +93,7 @@ extern "C" attn_status attn_fwd_static_scratch(
   p.sv = {(long long)hkv * d, d};
   p.so = {(long long)hq * d, d};
   p.err = err;
+  p.wait_ns = internal_wait_ns();
   // Same carving as the caller-provided workspace of attn_fwd: partial
   // outputs first, partial logsumexps after them.
   p.o_part = reinterpret_cast<float *>(scratch);

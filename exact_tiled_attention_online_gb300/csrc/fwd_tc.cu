@@ -69,9 +69,16 @@ struct TcArgs {
 
 struct Bars {
   uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2], s_full[2], p_full, o_done;
+  uint64_t drain;     // the MMA thread's products have all completed
+  uint64_t limit_ns;  // bound of every wait of this call
   uint32_t tmem_base;
   int abort;
+  // for a drain after an early exit: Q fills, K / V ring fills (stage =
+  // fill % 2) the producer issued, and whether the MMA thread issued any
+  int filled_q, filled_k, filled_v, mma_issued;
 };
+
+static_assert(sizeof(Bars) <= 256, "barrier block fits its shared-memory slot");
 
 __device__ __forceinline__ bool aborted(Bars *b) {
   return *reinterpret_cast<volatile int *>(&b->abort) != 0;
@@ -80,7 +87,7 @@ __device__ __forceinline__ bool aborted(Bars *b) {
 __device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err) {
   if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (aborted(b)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, b->limit_ns)) return true;
   *reinterpret_cast<volatile int *>(&b->abort) = 1;
   raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
   return false;
@@ -149,7 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&b->p_full, 128);
     mbar_init(&b->o_done, 1);
+    mbar_init(&b->drain, 1);
+    b->limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->abort = 0;
+    b->filled_q = b->filled_k = b->filled_v = b->mma_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -173,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       const int qh = a.pack ? kvh * a.group : head_idx;
+      int filled_k = 0, filled_v = 0;
       mbar_arrive_expect_tx(&b->q_full, L::kTile);
       for (int c = 0; c < L::kChunks; c++)
         tma_load_3d(smem + L::kQ + c * L::kChunk, &tm_q, &b->q_full, c * 64, qh, g.q0 + i0);
@@ -181,19 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key_row = g.k0 + (n_begin + jj) * kTileKeys;
         if (jj >= 2 && !wait_or_abort(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+        filled_k++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
                       kvh, key_row);
         if (jj >= 2 && !wait_or_abort(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+        filled_v++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st], c * 64,
                       kvh, key_row);
       }
+      b->filled_q = 1;  // for a drain after an early exit
+      b->filled_k = filled_k;
+      b->filled_v = filled_v;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && n_tiles > 0) {
+      b->mma_issued = 1;
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
       auto issue_qk = [&](int st) {
@@ -439,6 +456,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A block in which a wait gave up may still have copies and products in
+  // flight: drain them before the tensor memory is freed (the flag is only
+  // set before the barrier above).
+  if (aborted(b)) {
+    if (threadIdx.x == 0) {
+      bool drained = drain_phase(&b->q_full, b->filled_q);
+      for (int st = 0; st < 2; st++)
+        drained = drain_phase(&b->k_full[st], ring_armed(b->filled_k, st, 2)) &&
+                  drain_phase(&b->v_full[st], ring_armed(b->filled_v, st, 2)) && drained;
+      if (!drained) raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    }
+    if (threadIdx.x == 32 && b->mma_issued && !drain_mma(&b->drain))
+      raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -76,14 +76,21 @@ struct Bars2 {
   uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];  // [tile A, tile B]
   uint64_t b_full[2];  // kTab: the next tile's bias is in the tile's S columns
+  uint64_t drain;      // the MMA thread's products have all completed
+  uint64_t limit_ns;   // bound of every wait of this call
   uint32_t tmem_base;
   int abort;
+  // for a drain after an early exit: Q fills, K / V ring fills (stage =
+  // fill % 2) the producer issued, and whether the MMA thread issued any
+  int filled_q, filled_k, filled_v, mma_issued;
 };
+
+static_assert(sizeof(Bars2) <= 256, "barrier block fits its shared-memory slot");
 
 __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, int *err) {
   if (mbar_test_wait(bar, parity)) return true;  // already complete: the cheap path
   if (*reinterpret_cast<volatile int *>(&b->abort)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, b->limit_ns)) return true;
   *reinterpret_cast<volatile int *>(&b->abort) = 1;
   raise_error(err, ATTN_ERR_DEVICE_TIMEOUT);
   return false;
@@ -158,7 +165,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&b->b_full[s], 128);
       mbar_init(&b->pv_done[s], 1);
     }
+    mbar_init(&b->drain, 1);
+    b->limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->abort = 0;
+    b->filled_q = b->filled_k = b->filled_v = b->mma_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -182,6 +192,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      int filled_k = 0, filled_v = 0;
       mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
       for (int t2 = 0; t2 < 2; t2++)
         for (int c = 0; c < L::kChunks; c++)
@@ -192,19 +203,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int key_row = g.k0 + (n0 + n) * kTileKeys;
         if (n >= 2 && !wait2(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+        filled_k++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
                       hk, key_row);
         if (n >= 2 && !wait2(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+        filled_v++;
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st], c * 64,
                       hk, key_row);
       }
+      b->filled_q = 1;  // for a drain after an early exit
+      b->filled_k = filled_k;
+      b->filled_v = filled_v;
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && N > 0) {
+      b->mma_issued = 1;
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kTileKeys, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
       // Descriptors are built once; a byte offset below 256 KB adds to the
@@ -561,6 +578,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
 
   tc_fence_before();
   __syncthreads();
+  // A block in which a wait gave up may still have copies and products in
+  // flight; they must land before its tensor memory is freed and it exits
+  // (the flag is only set before the barrier above, so every thread reads
+  // the same value).  On the normal path every copy and product has been
+  // waited for already.
+  if (*reinterpret_cast<volatile int *>(&b->abort)) {
+    if (threadIdx.x == 0) {
+      bool drained = drain_phase(&b->q_full, b->filled_q);
+      for (int st = 0; st < 2; st++)
+        drained = drain_phase(&b->k_full[st], ring_armed(b->filled_k, st, 2)) &&
+                  drain_phase(&b->v_full[st], ring_armed(b->filled_v, st, 2)) && drained;
+      if (!drained) raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    }
+    if (threadIdx.x == 32 && b->mma_issued && !drain_mma(&b->drain))
+      raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kCols2);

@@ -69,12 +69,23 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Default bound of every wait (2 s) and the bound of the waits that drain a
+// CTA's own asynchronous copies and products before it frees its tensor
+// memory and exits.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+// A limit below this gives up at the first wait whose phase is not already
+// complete (it skips even the hardware-suspended try_wait): a deterministic
+// way for a test to make a wait expire with nothing broken.
+constexpr uint64_t kMinSpinNs = 1000ull;
+
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` nanoseconds.  Returns false on timeout; the caller records the
 // error and unwinds instead of spinning forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns < kMinSpinNs) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
@@ -82,6 +93,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
       if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Producer side of a CTA's drain: wait (bounded) for the last phase armed on
+// `bar`, `armed` phases having been armed in all, so that no copy into this
+// CTA's shared memory is still in flight when it exits.
+__device__ __forceinline__ bool drain_phase(uint64_t *bar, int armed) {
+  return armed <= 0 || mbar_wait(bar, (uint32_t)((armed - 1) & 1), kDrainLimitNs);
+}
+
+// Phases armed on stage `st` of a ring of `stages` after `n` fills in ring
+// order (fill i goes to stage i % stages).
+__device__ __forceinline__ int ring_armed(int n, int st, int stages) {
+  return n > st ? (n - st + stages - 1) / stages : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -197,6 +221,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// MMA side of a CTA's drain: every tcgen05 operation this thread issued has
+// completed once `bar` (count 1, used for nothing else) completes phase 0;
+// bounded.  Called before the CTA frees its tensor memory.
+__device__ __forceinline__ bool drain_mma(uint64_t *bar) {
+  mma_commit(bar);
+  return mbar_wait(bar, 0, kDrainLimitNs);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

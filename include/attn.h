@@ -324,6 +324,21 @@ attn_status attn_fwd_static_scratch(const void *q, const void *k, const void *v,
                                     const float *bias_slopes, attn_dtype dtype,
                                     void *stream);
 
+/*
+ * Bound, in nanoseconds, of every wait inside the library's kernels (one
+ * thread waiting for another role of its block: a copy, a product, a
+ * softmax step), for the calls made after it; 0 restores the default of
+ * 2 s.  A wait that reaches the bound gives up: the block stops issuing
+ * work, waits (bounded, 2 s) for its copies and products already in
+ * flight, frees its tensor memory and exits, and the call's outputs are
+ * undefined; attn_get_device_error() then returns ATTN_ERR_DEVICE_TIMEOUT.
+ * A bound below 1000 ns gives up at the first wait whose condition is not
+ * already met, which makes a timeout reproducible for tests of that path.
+ * The setting is process-wide (all host threads, all devices).  The pages
+ * have no counterpart: this is failure handling of the library itself.
+ */
+void attn_set_wait_limit_ns(uint64_t ns);
+
 /* Static description of a status code. */
 const char *attn_status_string(attn_status status);
 

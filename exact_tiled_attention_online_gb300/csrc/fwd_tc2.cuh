@@ -70,7 +70,39 @@ struct Tc2Args {
   int group;
   int n_pairs;    // CTAs per (sequence, head), or per (sequence, head pair) with heads2
   int heads2;     // 1: tiles A and B are the same 128 rows of two heads of one KV head
+  int compact;    // 1: the grid is the compact work list of compact_item()
 };
+
+// Compact work list for packed batches of at most 32 sequences.  Work item c
+// enumerates row blocks b = n_blocks - 1 .. 0 of `rows` rows (the heaviest
+// causal rows first, as in the rank-major grid), within a block the
+// sequences that have it, within a sequence its `units` head units, so no
+// CTA is launched for a block past a sequence's end.  Every warp computes
+// the same answer from one coalesced read of cu_seqlens.  false when c lies
+// past the last item.
+__device__ __forceinline__ bool compact_item(const int32_t *cu_q, int batch, int max_q, int rows,
+                                             int n_blocks, int units, int c, int *seq, int *blk,
+                                             int *unit) {
+  const int lane = threadIdx.x & 31;
+  int nq = 0;
+  if (lane < batch) {
+    nq = __ldg(cu_q + lane + 1) - __ldg(cu_q + lane);
+    nq = nq < 0 ? 0 : (nq > max_q ? max_q : nq);  // inconsistent lengths are caught later
+  }
+  const int tiles = (nq + rows - 1) / rows;
+  for (int b = n_blocks - 1; b >= 0; b--) {
+    const unsigned m = __ballot_sync(0xffffffffu, tiles > b);
+    const int cnt = __popc(m) * units;
+    if (c < cnt) {
+      *seq = (int)__fns(m, 0, c / units + 1);  // the (c / units)-th sequence with block b
+      *unit = c % units;
+      *blk = b;
+      return true;
+    }
+    c -= cnt;
+  }
+  return false;
+}
 
 struct Bars2 {
   uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
@@ -126,15 +158,26 @@ __global__ void __launch_bounds__(kThreads2, 1)
   // or with heads2 rows [i0, i0 + 128) of heads h and h + 1 (same KV head),
   // which gives both tiles the same key range.
   const int units = a.heads2 ? p.hq / 2 : p.hq;  // CTAs per (sequence, rank)
-  const int per_rank = units * p.batch;
-  const int rank = (int)blockIdx.x / per_rank;
-  const int h = ((int)blockIdx.x % units) * (a.heads2 ? 2 : 1);  // tile A's head
-  const int seq = ((int)blockIdx.x % per_rank) / units;
-  const int h_b = a.heads2 ? h + 1 : h;                            // tile B's head
-  const int rows_b = a.heads2 ? 0 : kTileRows;                     // tile B's row offset
+  const int rows_b = a.heads2 ? 0 : kTileRows;   // tile B's row offset
+  int rank, unit, seq;
+  if (a.compact) {
+    int blk;
+    if (!compact_item(p.cu_q, p.batch, p.max_q, kTileRows + rows_b, a.n_pairs, units,
+                      (int)blockIdx.x, &seq, &blk, &unit))
+      return;
+    rank = a.n_pairs - 1 - blk;
+  } else {
+    const int per_rank = units * p.batch;
+    rank = (int)blockIdx.x / per_rank;
+    unit = (int)blockIdx.x % units;
+    seq = ((int)blockIdx.x % per_rank) / units;
+  }
+  const int h = unit * (a.heads2 ? 2 : 1);  // tile A's head
+  const int h_b = a.heads2 ? h + 1 : h;     // tile B's head
   const SeqGeom g = load_seq(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q, p.max_k, p.mask, p.window);
   if (!g.ok) {
-    if (threadIdx.x == 0 && rank == 0 && h == 0) raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
+    if (threadIdx.x == 0 && (a.compact || (rank == 0 && h == 0)))
+      raise_error(p.err, ATTN_ERR_DEVICE_BOUNDS);
     return;
   }
   const int i0 = (a.n_pairs - 1 - rank) * (kTileRows + rows_b);  // first row of tile A
@@ -638,7 +681,20 @@ inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorM
       !make_map(mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sk.hs, p.sk.ts) ||
       !make_map(mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sv.hs, p.sv.ts))
     return false;
-  *ctas = (long long)a->n_pairs * (a->heads2 ? p.hq / 2 : p.hq) * p.batch;
+  const int units = a->heads2 ? p.hq / 2 : p.hq;
+  *ctas = (long long)a->n_pairs * units * p.batch;
+  // A packed batch of at most 32 sequences takes the compact work list when
+  // it is shorter: sum_s ceil(nq_s / R) <= (total_q + batch (R - 1)) / R
+  // items per head unit, against n_pairs per sequence and unit otherwise.
+  a->compact = 0;
+  if (p.batch <= 32) {
+    const long long R = *rows_per_cta;
+    const long long items = ((long long)p.total_q + p.batch * (R - 1)) / R * units;
+    if (items < *ctas) {
+      a->compact = 1;
+      *ctas = items;
+    }
+  }
   return *ctas < (1LL << 31);
 }
 

@@ -34,8 +34,10 @@
 // read it, plus the refill's TMA latency; dq releases its single dP buffer as
 // soon as the math warps have copied dP out, so the next dP product overlaps
 // the exponentials.  Biases rebuild the forward's: the linear positional bias
-// in the math (kBias), an explicit bias tensor stored into the score buffer
-// before the score product accumulates onto it (kTab).
+// in the math (kBias); an explicit bias tensor (kTab) added in registers by
+// the dK/dV math, stored into the score buffer before the score product
+// accumulates onto it by the dQ math (its threads hold a 64-key row segment,
+// too many registers to keep a prefetched copy).
 #include <stdio.h>
 
 #include <type_traits>
@@ -166,7 +168,6 @@ struct BarsA {
   // gradient products done.  Few barriers keep the MMA thread's commits and
   // waits, which the tensor pipe's short issue queue does not hide, few.
   uint64_t kv_full, qdo_full[kStagesA], qdo_empty[kStagesA], st_full[2], ps_full[2], mm_done;
-  uint64_t b_full[2], s_free[2];  // kTab: bias stored in S^T buffer t / buffer t read by dV, dK
   uint64_t drain;  // the MMA thread's products have all completed
   uint32_t tmem_base;
   Sync sync;
@@ -175,8 +176,9 @@ struct BarsA {
 static_assert(sizeof(BarsA) <= 512, "barrier block fits its shared-memory slot");
 
 // kBias: add the linear positional bias to the recomputed logits.  kTab: an
-// explicit bias tensor; the math warps store a step's entries (over the
-// positive scale) into its S^T buffer and S^T = K Q^T accumulates onto them.
+// explicit bias tensor; the math warps add each step's entries (log2 units,
+// loaded a step ahead) to the exponent argument in registers, so the score
+// products and their buffers are those of the plain kernel.
 template <int D, bool kBias, bool kTab>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -223,10 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&b->ps_full[s], 256);
     }
     mbar_init(&b->mm_done, 1);
-    for (int s = 0; s < 2; s++) {
-      mbar_init(&b->b_full[s], 256);
-      mbar_init(&b->s_free[s], 1);
-    }
     mbar_init(&b->drain, 1);
     b->sync.limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->sync.abort = 0;
@@ -311,11 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto qoff = [&](int s1) { return (uint64_t)((s1 * L::kQT) >> 4); };
       bool ok = wait_bar(&b->sync, &b->kv_full, 0, p.err) &&
-                wait_bar(&b->sync, &b->qdo_full[0], 0, p.err) &&
-                (!kTab || wait_bar(&b->sync, &b->b_full[0], 0, p.err));
+                wait_bar(&b->sync, &b->qdo_full[0], 0, p.err);
       if (ok) {
         tc_fence_after();
-        issue_st(dK0, dQk, kColS, kTab);
+        issue_st(dK0, dQk, kColS, false);
         issue_st(dV0, dDOk, kColDP, false);
         mma_commit(&b->st_full[0]);
       }
@@ -325,9 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 < n_it) {
           const int t1 = (it + 1) & 1, q1 = (it + 1) % kStagesA, u1 = (it + 1) / kStagesA;
           if (!wait_bar(&b->sync, &b->qdo_full[q1], u1 & 1, p.err)) break;
-          if (kTab && !wait_bar(&b->sync, &b->b_full[t1], ((it + 1) >> 1) & 1, p.err)) break;
           tc_fence_after();
-          issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA, kTab);
+          issue_st(dK0, dQk + qoff(q1), kColS + t1 * kRowsA, false);
           issue_st(dV0, dDOk + qoff(q1), kColDP + t1 * kRowsA, false);
           mma_commit(&b->st_full[t1]);
         }
@@ -335,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_grad(kColS + tb * kRowsA, dDOm + qoff(qs), kColDV, it > 0);
         issue_grad(kColDP + tb * kRowsA, dQm + qoff(qs), kColDK, it > 0);
-        if (kTab && it + 2 < n_it) mma_commit(&b->s_free[tb]);  // step it + 2's bias may go in
         if (it + 1 == n_it) mma_commit(&b->mm_done);
         if (it + kStagesA < n_it) mma_commit(&b->qdo_empty[qs]);  // a later step refills it
       }
@@ -372,29 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool fetcher = tid < 2 * kRowsA;
     float next_val = (n_it > 0 && fetcher) ? row_value(0) : 0.f;
     // kTab: bias entries of step u for this key and the warp's 32 rows, in
-    // S' units, into S^T buffer u & 1 (rows or keys out of range: 0)
-    const float inv_scale = kTab ? cs.bias : 0.f;
-    auto load_bias = [&](int u, uint32_t (&bv)[32]) {
+    // log2 units (rows or keys out of range: 0), added to the exponent
+    // argument in registers; step u + 1's loads fly during step u
+    auto load_bias = [&](int u, float (&bv)[32]) {
       const int ib = it_row0(u) + half * 32;
       const float *base = btab_row(p.btab, p.bss, p.bhs, p.brs, seq, it_head(u), 0) + j;
 #pragma unroll
       for (int c = 0; c < 32; c++)
-        bv[c] = __float_as_uint(ib + c < g.nq && j < g.nk
-                                    ? __ldg(base + (long long)(ib + c) * p.brs) * inv_scale
-                                    : 0.f);
+        bv[c] = ib + c < g.nq && j < g.nk ? __ldg(base + (long long)(ib + c) * p.brs) * kLog2e
+                                          : 0.f;
     };
-    auto store_bias = [&](int u, const uint32_t (&bv)[32]) {
-      tmem_st32(t_lane + kColS + (u & 1) * kRowsA + half * 32, bv);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&b->b_full[u & 1]);
-    };
-    if (kTab)
-      for (int u = 0; u < 2 && u < n_it; u++) {
-        uint32_t bv[32];
-        load_bias(u, bv);
-        store_bias(u, bv);
-      }
+    float bcur[kTab ? 32 : 1], bnext[kTab ? 32 : 1];
+    if constexpr (kTab) {
+      if (n_it > 0) load_bias(0, bcur);
+    }
     for (int it = 0; it < n_it; it++) {
       const int st = it & 1;
       const int i0 = it_row0(it);
@@ -403,9 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (fetcher && it + 1 < n_it) next_val = row_value(it + 1);
       const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
       const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
-      // kTab: step it + 2's bias loads fly during this step's math
-      uint32_t bnext[32];
-      if (kTab && it + 2 < n_it) load_bias(it + 2, bnext);
+      if constexpr (kTab) {
+        if (it > 0) {
+#pragma unroll
+          for (int c = 0; c < 32; c++) bcur[c] = bnext[c];
+        }
+        if (it + 1 < n_it) load_bias(it + 1, bnext);
+      }
       if (ok)
         ok = wait_bar(&b->sync, &b->st_full[st], (it >> 1) & 1, p.err);
       ok = __all_sync(0xffffffffu, ok);
@@ -433,6 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kBias) {
             nl.x += pos_bias2(slope2, bdist0, c0);
             nl.y += pos_bias2(slope2, bdist0, c0 + 1);
+          }
+          if constexpr (kTab) {  // a -inf entry gives P = 0
+            nl.x += bcur[e];
+            nl.y += bcur[e + 1];
           }
           float x0, x1;
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, f2(nl.x, nl.y)),
@@ -463,14 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ps_full[st]);
-      if (kTab && it + 2 < n_it) {
-        // step it + 2 reuses this S^T buffer once dV and dK have read P^T, dS^T
-        ok = __all_sync(0xffffffffu, wait_bar(&b->sync, &b->s_free[st], (it >> 1) & 1, p.err));
-        if (ok) {
-          tc_fence_after();
-          store_bias(it + 2, bnext);
-        }
-      }
     }
     if (ok && n_it > 0) {
       if (wait_bar(&b->sync, &b->mm_done, 0, p.err))

@@ -369,19 +369,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kTab: bias entries of step u for this key and the warp's 32 rows, in
     // log2 units (rows or keys out of range: 0), added to the exponent
     // argument in registers; step u + 1's loads fly during step u
+    // Raw entries (natural-log units; the use folds in log2(e)); a step wholly
+    // inside the sequence loads without per-entry bounds tests.
     auto load_bias = [&](int u, float (&bv)[32]) {
       const int ib = it_row0(u) + half * 32;
-      const float *base = btab_row(p.btab, p.bss, p.bhs, p.brs, seq, it_head(u), 0) + j;
+      const long long rs = p.brs;
+      const float *ptr = btab_row(p.btab, p.bss, p.bhs, p.brs, seq, it_head(u), ib) + j;
+      if (ib + 32 <= g.nq && j < g.nk) {
 #pragma unroll
-      for (int c = 0; c < 32; c++)
-        bv[c] = ib + c < g.nq && j < g.nk ? __ldg(base + (long long)(ib + c) * p.brs) * kLog2e
-                                          : 0.f;
+        for (int c = 0; c < 32; c++, ptr += rs) bv[c] = __ldg(ptr);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; c++, ptr += rs) bv[c] = ib + c < g.nq && j < g.nk ? __ldg(ptr) : 0.f;
+      }
     };
-    float bcur[kTab ? 32 : 1], bnext[kTab ? 32 : 1];
-    if constexpr (kTab) {
-      if (n_it > 0) load_bias(0, bcur);
-    }
-    for (int it = 0; it < n_it; it++) {
+    // One step; kTab: the step's entries in bcur, the next step's loads issued
+    // into bnext (the caller alternates the two buffers).
+    auto step = [&](int it, float (&bcur)[kTab ? 32 : 1], float (&bnext)[kTab ? 32 : 1]) {
       const int st = it & 1;
       const int i0 = it_row0(it);
       if (fetcher) sRow[st * 2 * kRowsA + tid] = next_val;
@@ -390,16 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *nlse2 = sRow + st * 2 * kRowsA;  // -lse2 of the 64 rows
       const float *nd = nlse2 + kRowsA;              // -D of the 64 rows
       if constexpr (kTab) {
-        if (it > 0) {
-#pragma unroll
-          for (int c = 0; c < 32; c++) bcur[c] = bnext[c];
-        }
         if (it + 1 < n_it) load_bias(it + 1, bnext);
       }
       if (ok)
         ok = wait_bar(&b->sync, &b->st_full[st], (it >> 1) & 1, p.err);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) continue;
+      if (!ok) return;
       tc_fence_after();
       const bool step_full = tile_in && rb_last <= i0 && re_first >= i0 + kRowsA;
       // rows i0 + c with c_lo <= c < c_lo + span see key j
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             nl.y += pos_bias2(slope2, bdist0, c0 + 1);
           }
           if constexpr (kTab) {  // a -inf entry gives P = 0
-            nl.x += bcur[e];
-            nl.y += bcur[e + 1];
+            nl.x = fmaf(bcur[e], kLog2e, nl.x);
+            nl.y = fmaf(bcur[e + 1], kLog2e, nl.y);
           }
           float x0, x1;
           f2_split(ffma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2x2, f2(nl.x, nl.y)),
@@ -457,6 +457,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&b->ps_full[st]);
+    };
+    float b0[kTab ? 32 : 1], b1[kTab ? 32 : 1];
+    if constexpr (kTab) {
+      if (n_it > 0) load_bias(0, b0);
+      for (int it = 0; it < n_it; it += 2) {  // the two buffers alternate without copies
+        step(it, b0, b1);
+        if (it + 1 < n_it) step(it + 1, b1, b0);
+      }
+    } else {
+      for (int it = 0; it < n_it; it++) step(it, b0, b1);
     }
     if (ok && n_it > 0) {
       if (wait_bar(&b->sync, &b->mm_done, 0, p.err))

@@ -90,6 +90,10 @@ def library() -> ctypes.CDLL:
     L.attn_version.restype = I
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.attn_set_wait_limit_ns.restype = None
+    L.attn_set_deterministic.argtypes = [ctypes.c_int]
+    L.attn_set_deterministic.restype = None
+    L.attn_get_deterministic.argtypes = []
+    L.attn_get_deterministic.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -297,6 +301,18 @@ def set_wait_limit_ns(ns: int) -> None:
     """Bound of every wait inside the kernels for the following calls (0:
     the 2 s default); see ``attn_set_wait_limit_ns`` in include/attn.h."""
     library().attn_set_wait_limit_ns(int(ns))
+
+
+def set_deterministic(on: bool) -> None:
+    """Backward form for the following bf16 calls: True keeps the
+    two-kernel backward (every gradient reproducible bit for bit), False
+    (the default) the fused one (dQ summed with reductions); see
+    ``attn_set_deterministic`` in include/attn.h."""
+    library().attn_set_deterministic(1 if on else 0)
+
+
+def get_deterministic() -> bool:
+    return bool(library().attn_get_deterministic())
 
 
 def last_plan() -> str:

@@ -19,6 +19,7 @@ cudaError_t launch_kv_to_f16(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_amax(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_fwd_tc2_delta(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
+cudaError_t launch_bwd_fused(const BwdParams &p, cudaStream_t st, char *desc, size_t desc_len);
 cudaError_t launch_fwd_tc(const FwdParams &p, const TcPlan &plan, cudaStream_t st,
                           char *desc, size_t desc_len);
 cudaError_t launch_combine(const FwdParams &p, const TcPlan &plan, cudaStream_t st);
@@ -50,6 +51,10 @@ static thread_local char t_plan[512] = "none";
 // Bound of every device wait, in ns (0: the kernels' 2 s default); set by
 // attn_set_wait_limit_ns, read by every call.
 static std::atomic<unsigned long long> g_wait_ns{0};
+
+// Nonzero: the bf16 backward keeps to the two-kernel form, whose dQ is
+// reproducible bit for bit (set by attn_set_deterministic).
+static std::atomic<int> g_deterministic{0};
 
 static void set_plan(const char *s) {
   snprintf(t_plan, sizeof(t_plan), "%s", s);
@@ -98,7 +103,7 @@ static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // fp16 copies of q, dout ([total_q, hq, d]) and k, v ([total_k, hkv, d]) and
 // the four tensors' largest magnitudes (256 bytes).
 struct BwdLayout {
-  size_t delta, lse2, q16, do16, k16, v16, amax, total;
+  size_t delta, lse2, q16, do16, k16, v16, amax, dqacc, total;
 };
 static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, int dtype) {
   BwdLayout l{};
@@ -116,6 +121,10 @@ static BwdLayout bwd_layout(int total_q, int total_k, int hq, int hkv, int d, in
     off += 2 * qb + 2 * kb;
     l.amax = off;
     off += 256;
+    if (d == 128) {  // the fused backward's fp32 dQ accumulator
+      l.dqacc = off;
+      off += align256((size_t)total_q * hq * d * 4);
+    }
   }
   l.total = off;
   return l;
@@ -157,6 +166,10 @@ const char *attn_status_string(attn_status s) {
 const char *attn_last_plan(void) { return t_plan; }
 
 void attn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+
+void attn_set_deterministic(int on) { g_deterministic.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+int attn_get_deterministic(void) { return g_deterministic.load(std::memory_order_relaxed); }
 
 size_t attn_fwd_workspace_size(int batch, int max_q, int max_k, int total_q, int hq, int hkv,
                                int d, int window, attn_dtype dtype) {
@@ -407,7 +420,14 @@ attn_status attn_bwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
       fp.wait_ns = p.wait_ns;
       ce = launch_fwd_tc2_delta(fp, cs);
     }
-    if (ce == cudaSuccess) ce = launch_bwd_tc(p, cs, desc, sizeof(desc));
+    if (ce == cudaSuccess) {
+      if (d == 128 && !g_deterministic.load(std::memory_order_relaxed)) {
+        p.dqacc = reinterpret_cast<float *>(ws + wl.dqacc);
+        ce = launch_bwd_fused(p, cs, desc, sizeof(desc));
+      } else {
+        ce = launch_bwd_tc(p, cs, desc, sizeof(desc));
+      }
+    }
   } else {
     if (ce == cudaSuccess) ce = launch_bwd_simt(p, dtype, cs);
     snprintf(desc, sizeof(desc), "bwd_pre+bwd_dq_simt+bwd_dkdv_simt_%s_d%d%s",

@@ -269,6 +269,9 @@ struct BwdParams {
   // scale exponents follow from it
   unsigned int *amax;
   unsigned long long wait_ns;  // bound of every device wait (0: the 2 s default)
+  // [total_q, hq, d] fp32 dQ accumulator of the fused backward (NULL: the
+  // two-kernel backward)
+  float *dqacc;
 };
 
 // ---------------------------------------------------------------------------

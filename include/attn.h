@@ -204,7 +204,9 @@ attn_status attn_fwd_ex(const attn_strides *strides, const attn_bias_tensor *bia
  * thousands of rows).  Each copy is scaled by a power of two that brings the
  * tensor's largest magnitude into [4, 8), so every element within 2^19 of
  * it is copied exactly, at any overall magnitude of the inputs; the kernels
- * undo the factors exactly.  (size_t)-1 for bad arguments.
+ * undo the factors exactly.  For bf16 with head_dim 128 it also holds the
+ * fused backward's fp32 dQ accumulator ([total_q, n_heads_q, 128]).
+ * (size_t)-1 for bad arguments.
  */
 size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
                                int total_q, int total_k, int n_heads_q,
@@ -338,6 +340,21 @@ attn_status attn_fwd_static_scratch(const void *q, const void *k, const void *v,
  * have no counterpart: this is failure handling of the library itself.
  */
 void attn_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Backward form for the bf16 calls that follow (process-wide, all host
+ * threads and devices).  0, the default: with head_dim 128 the tensor-core
+ * backward runs as one kernel per 128-key tile that computes S and dP once
+ * per (row, key) pair and produces dK, dV and the tile's dQ contributions;
+ * dQ is summed over key tiles in an fp32 accumulator with global reductions,
+ * so its rounding depends on the order in which CTAs finish and can differ
+ * in the last bits from run to run.  Nonzero: two kernels, one owning dK and
+ * dV and one owning dQ (S and dP computed in both), no reductions, every
+ * gradient reproducible bit for bit.  head_dim 64 and fp32 calls always take
+ * the reproducible form.  attn_get_deterministic returns the setting.
+ */
+void attn_set_deterministic(int on);
+int attn_get_deterministic(void);
 
 /* Static description of a status code. */
 const char *attn_status_string(attn_status status);

@@ -1,5 +1,7 @@
 """Shared helpers for the GPU parity tests: run the CUDA path through the
 binding and the oracle on the same seeded inputs."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -22,6 +24,23 @@ def oracle_fwd(x, rows=None):
     w = x["workload"]
     return oracle.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.scale,
                       w.mask, rows=rows, window=w.window)
+
+
+@contextlib.contextmanager
+def backward_form(deterministic):
+    """Run the enclosed calls with the two-kernel (True) or the fused (False)
+    bf16 backward, then restore the previous setting."""
+    prev = attn.get_deterministic()
+    attn.set_deterministic(deterministic)
+    try:
+        yield
+    finally:
+        attn.set_deterministic(prev)
+
+
+def tc_backward(plan):
+    """The plan ran a tensor-core backward (fused or two-kernel)."""
+    return "bwd_dq_tc" in plan or "bwd_fused_tc" in plan
 
 
 def sample_rows(w, n, seed):

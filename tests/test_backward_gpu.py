@@ -8,7 +8,7 @@ import torch
 import oracle
 from exact_tiled_attention_online_gb300 import attn, inputs
 from tests import compare
-from tests.gpu_cases import sample_rows
+from tests.gpu_cases import backward_form, sample_rows
 
 pytestmark = pytest.mark.gpu
 TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
@@ -36,14 +36,20 @@ CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask)
 ]
 
 
+FORMS = [False, True]  # fused (the default), two-kernel
+FORM_IDS = ["fused", "two_kernel"]
+
+
+@pytest.mark.parametrize("two_kernel", FORMS, ids=FORM_IDS)
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_backward_full(case):
+def test_backward_full(case, two_kernel):
     name, lq, lk, hq, hkv, d, dt, mask = case
     # value ranges differ per sequence so that leakage shows
     w = inputs.custom(name, lq, lk, hq, hkv, d, dt, mask, seed=17, backward=True,
                       v_shift_per_seq=2.0)
     x = inputs.make_inputs(w)
-    o, lse, dq, dk, dv = run_fwd_bwd(x)
+    with backward_form(two_kernel):
+        o, lse, dq, dk, dv = run_fwd_bwd(x)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
                                          x["cu_seqlens_k"], w.scale, mask)
     compare.check_close("o", o, ro)
@@ -56,10 +62,13 @@ def test_backward_full(case):
         assert np.all(compare.to_np(dq)[t, h] == 0.0)
 
 
-def test_train_full_size_sampled():
+@pytest.mark.parametrize("two_kernel", FORMS, ids=FORM_IDS)
+def test_train_full_size_sampled(two_kernel):
     w = inputs.WORKLOADS["train_fwd_bwd"]
     x = inputs.make_inputs(w)
-    o, lse, dq, dk, dv = run_fwd_bwd(x)
+    with backward_form(two_kernel):
+        o, lse, dq, dk, dv = run_fwd_bwd(x)
+        assert ("bwd_dq_tc" if two_kernel else "bwd_fused_tc") in attn.last_plan()
     qrows = sample_rows(w, 24, seed=8)
     rng = np.random.default_rng(9)
     # keys near the start of a sequence are reached by every later query row;
@@ -78,15 +87,68 @@ def test_train_full_size_sampled():
 
 
 def test_backward_deterministic():
-    """Every gradient row has one owner CTA and no atomics: repeated calls give
-    bit-identical dq, dk, dv."""
+    """Two-kernel form: every gradient row has one owner CTA and no atomics,
+    so repeated calls give bit-identical dq, dk, dv."""
     w = inputs.custom("det", (300, 129), (300, 129), 8, 2, 128, "bf16", TL, seed=4, backward=True)
     x = inputs.make_inputs(w)
-    first = run_fwd_bwd(x)
-    for _ in range(3):
-        again = run_fwd_bwd(x)
-        for a, b in zip(first, again):
-            assert torch.equal(a, b)
+    with backward_form(True):
+        first = run_fwd_bwd(x)
+        assert "bwd_dq_tc" in attn.last_plan()
+        for _ in range(3):
+            again = run_fwd_bwd(x)
+            for a, b in zip(first, again):
+                assert torch.equal(a, b)
+
+
+AGREE = [  # (name, lq, lk, hq, hkv, mask, window, bias kind)
+    ("ragged_gqa4", (63, 129, 1, 200), None, 8, 2, TL, 0, None),
+    ("long_gqa8", (1100, 517), None, 16, 2, TL, 0, None),
+    ("br_empty_rows", (64, 10), (32, 300), 4, 1, BR, 0, None),
+    ("noncausal", (100, 37), (50, 260), 4, 4, NONE, 0, None),
+    ("window", (700, 129), None, 8, 2, TL, 100, None),
+    ("slopes", (300, 50), (700, 40), 4, 2, BR, 0, "slopes"),
+    ("bias_tensor", (63, 129, 1, 200), None, 8, 2, TL, 0, "tensor"),
+]
+
+
+@pytest.mark.parametrize("case", AGREE, ids=[c[0] for c in AGREE])
+def test_fused_matches_two_kernel(case):
+    """The fused backward computes dK and dV with the same products in the
+    same order as the two-kernel one (bit-identical, and identical from call
+    to call); only dQ is summed differently (fp32 reductions across key
+    tiles), so it agrees to about one bf16 rounding."""
+    name, lq, lk, hq, hkv, mask, window, kind = case
+    w = inputs.custom(name, lq, lk or lq, hq, hkv, 128, "bf16", mask, seed=19, backward=True,
+                      v_shift_per_seq=2.0, window=window)
+    x = inputs.make_inputs(w)
+    d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
+    sl = inputs.bias_slopes(hq).cuda() if kind == "slopes" else None
+    bt = inputs.bias_tensor(w.batch, hq, w.max_q, w.max_k, seed=20, dead_rows=2).cuda() \
+        if kind == "tensor" else None
+    o, lse, o32 = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
+                           w.max_k, mask, w.scale, want_o_f32=True, window=window,
+                           bias_slopes=sl, bias=bt)
+
+    def grads(two_kernel):
+        with backward_form(two_kernel):
+            g = attn.bwd(d["q"], d["k"], d["v"], o, lse, d["dout"], d["cu_seqlens_q"],
+                         d["cu_seqlens_k"], w.max_q, w.max_k, mask, w.scale, o_f32=o32,
+                         window=window, bias_slopes=sl, bias=bt)
+            plan = attn.last_plan()
+        torch.cuda.synchronize()
+        assert attn.get_device_error() == 0
+        assert ("bwd_dq_tc" if two_kernel else "bwd_fused_tc") in plan, plan
+        return g
+
+    dq2, dk2, dv2 = grads(True)
+    dqf, dkf, dvf = grads(False)
+    assert torch.equal(dkf, dk2) and torch.equal(dvf, dv2)
+    compare.check_close("dq fused vs two-kernel", dqf, compare.to_np(dq2).astype(np.float64),
+                        atol=1e-3, rtol=2.0 ** -7)
+    dqf2, dkf2, dvf2 = grads(False)
+    assert torch.equal(dkf2, dkf) and torch.equal(dvf2, dvf)
+    compare.check_close("dq fused repeat", dqf2, compare.to_np(dqf).astype(np.float64),
+                        atol=1e-3, rtol=2.0 ** -7)
 
 
 @pytest.mark.parametrize("mask", [TL, BR, NONE])

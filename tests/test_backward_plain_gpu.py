@@ -20,7 +20,7 @@ import torch
 import oracle
 from exact_tiled_attention_online_gb300 import attn, inputs
 from tests import compare
-from tests.gpu_cases import sample_rows
+from tests.gpu_cases import sample_rows, tc_backward
 
 pytestmark = pytest.mark.gpu
 TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
@@ -70,7 +70,7 @@ def test_backward_without_o_f32(case):
     bias = inputs.bias_tensor(w.batch, hq, w.max_q, w.max_k, seed=72, dead_rows=2) \
         if kind == "tensor" else None
     (o, lse, dq, dk, dv), plan = run(x, False, slopes, bias)
-    assert "fwd_tc2_delta" in plan and "bwd_dq_tc" in plan, plan
+    assert "fwd_tc2_delta" in plan and tc_backward(plan), plan
     rdq, rdk, rdv, ro, rlse = oracle.bwd(
         x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.scale, mask,
         window=window, slopes=None if slopes is None else slopes.double().numpy(), bias=bias)
@@ -135,7 +135,7 @@ def test_backward_input_magnitude(e, keep_o32):
     for name in ("q", "k", "v", "dout"):
         x[name] = (x[name].double() * f).to(torch.bfloat16)
     (o, lse, dq, dk, dv), plan = run(x, keep_o32)
-    assert "bwd_dq_tc" in plan
+    assert tc_backward(plan), plan
     rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
                                          x["cu_seqlens_k"], w.scale, w.mask)
     u1, u3 = 2.0 ** -e, 2.0 ** (-3 * e)

@@ -10,7 +10,7 @@ import torch
 import oracle
 from exact_tiled_attention_online_gb300 import attn, inputs
 from tests import compare
-from tests.gpu_cases import sample_rows
+from tests.gpu_cases import sample_rows, tc_backward
 
 pytestmark = pytest.mark.gpu
 TL, BR, NONE = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT, inputs.MASK_NONE
@@ -36,12 +36,12 @@ def run(x, bias, slopes=None):
 
 CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask, window, bias broadcast, slopes,
     #          forward kernel, backward kernel)
-    ("bf16_tl_full", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "dq_tc"),
-    ("bf16_tl_long", (700, 300), None, 4, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "dq_tc"),
-    ("bf16_br_head_bcast", (40, 9), (100, 300), 4, 1, 64, "bf16", BR, 0, True, False, "fwd_tc2", "dq_tc"),
-    ("bf16_none_d64", (200, 77), (150, 300), 4, 4, 64, "bf16", NONE, 0, False, False, "fwd_tc2", "dq_tc"),
+    ("bf16_tl_full", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "tc"),
+    ("bf16_tl_long", (700, 300), None, 4, 2, 128, "bf16", TL, 0, False, False, "fwd_tc2", "tc"),
+    ("bf16_br_head_bcast", (40, 9), (100, 300), 4, 1, 64, "bf16", BR, 0, True, False, "fwd_tc2", "tc"),
+    ("bf16_none_d64", (200, 77), (150, 300), 4, 4, 64, "bf16", NONE, 0, False, False, "fwd_tc2", "tc"),
     ("bf16_none_slopes", (50, 77), (70, 20), 4, 4, 128, "bf16", NONE, 0, False, True, "fwd_simt", "simt"),
-    ("bf16_tl_window", (90, 333), None, 4, 2, 64, "bf16", TL, 9, False, False, "fwd_tc2", "dq_tc"),
+    ("bf16_tl_window", (90, 333), None, 4, 2, 64, "bf16", TL, 9, False, False, "fwd_tc2", "tc"),
     ("fp32_br", (37, 70), (50, 70), 4, 2, 64, "fp32", BR, 0, True, True, "fwd_simt", "simt"),
 ]
 
@@ -56,7 +56,8 @@ def test_bias_tensor_fwd_bwd(case):
                               seed=62, dead_rows=3)
     slopes = inputs.bias_slopes(hq) if with_slopes else None
     (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias, slopes)
-    assert "_btab" in fplan and "_btab" in bplan and kernel in fplan and bkernel in bplan, (fplan, bplan)
+    assert "_btab" in fplan and "_btab" in bplan and kernel in fplan and \
+        (tc_backward(bplan) if bkernel == "tc" else bkernel in bplan), (fplan, bplan)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
                                          x["cu_seqlens_k"], w.scale, mask, window=window,
                                          slopes=None if slopes is None else slopes.double().numpy(),
@@ -111,7 +112,7 @@ def test_bias_tensor_mixed_broadcast(shape):
     b, hb = (1, 4) if shape == "heads_only" else (w.batch, 1)
     bias = inputs.bias_tensor(b, hb, w.max_q, w.max_k, seed=67, dead_rows=2)
     (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias)
-    assert "fwd_tc2" in fplan and "dq_tc" in bplan, (fplan, bplan)
+    assert "fwd_tc2" in fplan and tc_backward(bplan), (fplan, bplan)
     rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
                                          x["cu_seqlens_k"], w.scale, BR, bias=bias)
     compare.check_close("o", o, ro)
@@ -148,7 +149,7 @@ def test_bias_tensor_train_full_size_sampled():
     x = inputs.make_inputs(w)
     bias = inputs.bias_tensor(w.batch, 1, w.max_q, w.max_k, w.seed + 1)
     (o, lse, dq, dk, dv), (fplan, bplan) = run(x, bias)
-    assert "fwd_tc2" in fplan and "dq_tc" in bplan, (fplan, bplan)
+    assert "fwd_tc2" in fplan and tc_backward(bplan), (fplan, bplan)
     qrows = sample_rows(w, 8, seed=72)
     krows = np.array([(0, 0), (8191, 3), (8192, 1), (16383, 2)], np.int64)
     rdq, rdk, rdv = oracle.bwd_sampled(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],

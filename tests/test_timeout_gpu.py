@@ -17,6 +17,7 @@ import torch
 import oracle
 from exact_tiled_attention_online_gb300 import attn, inputs
 from tests import compare
+from tests.gpu_cases import backward_form
 
 pytestmark = pytest.mark.gpu
 TL, BR = inputs.MASK_TOP_LEFT, inputs.MASK_BOTTOM_RIGHT
@@ -25,15 +26,21 @@ TIMEOUT = 5
 CALLS = [  # (name, lq, lk, hq, hkv, mask, backward, plan substring)
     ("prefill", (300, 129), (300, 129), 8, 2, TL, False, "fwd_tc2"),
     ("decode_split", (1,) * 4, (9000, 4097, 300, 6000), 32, 8, BR, False, "splits="),
-    ("backward", (300, 129), (300, 129), 8, 2, TL, True, "bwd_dkdv_tc"),
+    ("backward", (300, 129), (300, 129), 8, 2, TL, True, "bwd_fused_tc"),
+    ("backward_two_kernel", (300, 129), (300, 129), 8, 2, TL, "two_kernel", "bwd_dkdv_tc"),
     ("backward_plain", (300, 129), (300, 129), 8, 2, TL, "plain", "fwd_tc2_delta"),
 ]
 
 
 def _call(x, backward):
+    with backward_form(backward == "two_kernel"):
+        return _call_form(x, backward)
+
+
+def _call_form(x, backward):
     w = x["workload"]
     d = x
-    keep = backward is True
+    keep = backward is True or backward == "two_kernel"
     res = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
                    w.max_k, w.mask, w.scale, want_o_f32=keep)
     grads = None

@@ -15,7 +15,10 @@ that are already resident in HBM:
   bias_tensor_train    the train_fwd_bwd shape with such a tensor, forward +
                   backward;
   train_fwd_bwd_plain  train_fwd_bwd without keeping the forward's fp32
-                  output, so the backward recomputes it for its D term.
+                  output, so the backward recomputes it for its D term;
+  train_fwd_bwd_det    train_fwd_bwd with the two-kernel backward, whose
+                  gradients are reproducible bit for bit (the default
+                  fused backward sums dQ with reductions).
 
 Every workload is timed with CUDA events on the launching stream after an L2
 flush (a 256 MiB write), W warm-up steps first, K timed steps, medians and
@@ -203,7 +206,12 @@ class Runner:
         from exact_tiled_attention_online_gb300 import attn
         self.attn = attn
         self.name = name
-        self.w = inputs.WORKLOADS[name[:-len("_plain")] if name.endswith("_plain") else name]
+        base = name
+        for suffix in ("_plain", "_det"):
+            if base.endswith(suffix):
+                base = base[:-len(suffix)]
+        self.w = inputs.WORKLOADS[base]
+        self.two_kernel = name.endswith("_det")
         if batch_div > 1:  # a smaller case of the same kernels, for profiler captures
             w = self.w
             b = max(1, w.batch // batch_div)
@@ -240,11 +248,15 @@ class Runner:
               window=w.window, bias_slopes=self.slopes, bias=self.btab)
         plans = [a.last_plan()]
         if w.backward:
-            a.bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["dout"], x["cu_seqlens_q"],
-                  x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, dq=self.dq, dk=self.dk,
-                  dv=self.dv, workspace=self.bws, o_f32=self.o32, window=w.window,
-                  bias_slopes=self.slopes, bias=self.btab)
-            plans.append(a.last_plan())
+            a.set_deterministic(self.two_kernel)
+            try:
+                a.bwd(x["q"], x["k"], x["v"], self.o, self.lse, x["dout"], x["cu_seqlens_q"],
+                      x["cu_seqlens_k"], w.max_q, w.max_k, w.mask, w.scale, dq=self.dq,
+                      dk=self.dk, dv=self.dv, workspace=self.bws, o_f32=self.o32,
+                      window=w.window, bias_slopes=self.slopes, bias=self.btab)
+                plans.append(a.last_plan())
+            finally:
+                a.set_deterministic(False)
         self.plans = plans
 
     def kernels_per_run(self):
@@ -587,7 +599,7 @@ def main():
     ap.add_argument("--workloads",
                     default="gqa_prefill,decode_q1,decode_q16,train_fwd_bwd,varlen_causal,"
                             "window_prefill,bias_prefill,bias_tensor_prefill,bias_tensor_train,"
-                            "train_fwd_bwd_plain")
+                            "train_fwd_bwd_plain,train_fwd_bwd_det")
     ap.add_argument("--skip-validate", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

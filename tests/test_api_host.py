@@ -77,6 +77,27 @@ def test_bwd_workspace_covers_rows_and_fp16_copies(lib):
     copies = 2 * 200 * 4 * 128 * 2 + 2 * 200 * 2 * 128 * 2   # q, dout, k, v in fp16
     assert n >= rows + copies
     assert lib.attn_bwd_workspace_size(2, 100, 100, 200, 200, 4, 2, 128, 1) >= rows
+    # head_dim 128 bf16 also holds the fused backward's fp32 dQ accumulator
+    assert n >= rows + copies + 200 * 4 * 128 * 4
+    n64 = lib.attn_bwd_workspace_size(2, 100, 100, 200, 200, 4, 2, 64, 0)
+    copies64 = copies // 2
+    assert rows + copies64 <= n64 < rows + copies64 + 200 * 4 * 64 * 4  # head_dim 64: no accumulator
+
+
+def test_deterministic_switch_round_trips(lib):
+    """The backward-form switch is process-wide host state: set, read back,
+    restored (no device needed)."""
+    prev = attn.get_deterministic()
+    try:
+        attn.set_deterministic(True)
+        assert attn.get_deterministic() is True
+        assert lib.attn_get_deterministic() == 1
+        attn.set_deterministic(False)
+        assert attn.get_deterministic() is False
+        lib.attn_set_deterministic(7)  # any nonzero value selects the two-kernel form
+        assert lib.attn_get_deterministic() == 1
+    finally:
+        attn.set_deterministic(prev)
 
 
 def test_bwd_rejects_missing_workspace(lib):

@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&b->v_empty[s], 1);
       mbar_init(&b->s_full[s], 1);
       mbar_init(&b->p_full[s], 128);
-      mbar_init(&b->b_full[s], 128);
+      // kTab with heads2: each tile's threads store half of every row's
+      // bias into both tiles' S columns, so both tiles arrive on both
+      mbar_init(&b->b_full[s], kTab && a.heads2 ? 256 : 128);
       mbar_init(&b->pv_done[s], 1);
     }
     mbar_init(&b->drain, 1);
@@ -420,10 +422,55 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_before();
       mbar_arrive(&b->b_full[x]);
     };
+    // With heads2 the tiles hold the same rows of two heads, and a bias
+    // shared by the heads is the same for both: tile X's threads load keys
+    // [64 X, 64 X + 64) of their row and store them into both tiles' S
+    // columns, so every row's entries cross L2 once per CTA, not twice.
+    const bool share = kTab && a.heads2;
+    auto load_bias_half = [&](int n, uint32_t (&bv)[kTileKeys / 2]) {
+      const int j0 = n * kTileKeys + x * (kTileKeys / 2);
+      const bool vec = brow && j0 + kTileKeys / 2 <= g.nk &&
+                       ((reinterpret_cast<uintptr_t>(brow + j0) & 15) == 0);
+      if (vec) {
+#pragma unroll
+        for (int e = 0; e < kTileKeys / 2; e += 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4 *>(brow + j0 + e));
+          bv[e] = __float_as_uint(f.x * inv_scale);
+          bv[e + 1] = __float_as_uint(f.y * inv_scale);
+          bv[e + 2] = __float_as_uint(f.z * inv_scale);
+          bv[e + 3] = __float_as_uint(f.w * inv_scale);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kTileKeys / 2; e++) {
+          const int j = j0 + e;
+          bv[e] = __float_as_uint(brow && j < g.nk ? __ldg(brow + j) * inv_scale : 0.f);
+        }
+      }
+    };
+    auto store_bias_shared = [&](const uint32_t (&bv)[kTileKeys / 2]) {
+      const uint32_t half_col = t_lane + (uint32_t)(x * (kTileKeys / 2));
+#pragma unroll
+      for (int y = 0; y < 2; y++)
+#pragma unroll
+        for (int c = 0; c < kTileKeys / 64; c++)
+          tmem_st32(half_col + (uint32_t)(y * kTileKeys) + c * 32,
+                    *reinterpret_cast<const uint32_t(*)[32]>(bv + 32 * c));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&b->b_full[0]);
+      mbar_arrive(&b->b_full[1]);
+    };
     if (kTab && n_mine > 0) {
-      uint32_t bv[kTileKeys];
-      load_bias(kr.n_begin, bv);
-      store_bias(bv);
+      if (share) {
+        uint32_t bv[kTileKeys / 2];
+        load_bias_half(kr.n_begin, bv);
+        store_bias_shared(bv);
+      } else {
+        uint32_t bv[kTileKeys];
+        load_bias(kr.n_begin, bv);
+        store_bias(bv);
+      }
     }
     for (int it = 0; it < n_mine; it++) {
       const int n = kr.n_begin + it;  // key tile in the sequence
@@ -535,16 +582,29 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_before();
       mbar_arrive(&b->p_full[x]);
       if (kTab && it + 1 < n_mine) {
-        // the next tile's bias may overwrite S once P V has read P
-        uint32_t bv[kTileKeys];
-        load_bias(n + 1, bv);
-        ok = wait2(b, &b->pv_done[x], it & 1, p.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
+        // the next tile's bias may overwrite S once P V has read P (with
+        // share, both tiles' P: both tiles' S columns are written)
+        if (share) {
+          uint32_t bv[kTileKeys / 2];
+          load_bias_half(n + 1, bv);
+          ok = wait2(b, &b->pv_done[0], it & 1, p.err) && wait2(b, &b->pv_done[1], it & 1, p.err);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          store_bias_shared(bv);
+        } else {
+          uint32_t bv[kTileKeys];
+          load_bias(n + 1, bv);
+          ok = wait2(b, &b->pv_done[x], it & 1, p.err);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          store_bias(bv);
         }
-        tc_fence_after();
-        store_bias(bv);
       }
     }
     if (ok && n_mine > 0) {
@@ -673,7 +733,9 @@ inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorM
                       CUtensorMap *mv, long long *ctas, int *rows_per_cta) {
   a->p = p;
   a->group = p.hq / p.hkv;
-  a->heads2 = a->group % 2 == 0 && !p.btab ? 1 : 0;
+  // a bias tensor pairs heads only when the heads share it (then the two
+  // tiles share its entries too)
+  a->heads2 = a->group % 2 == 0 && (!p.btab || p.bhs == 0) ? 1 : 0;
   *rows_per_cta = a->heads2 ? kTileRows : 2 * kTileRows;
   a->n_pairs = (p.max_q + *rows_per_cta - 1) / *rows_per_cta;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

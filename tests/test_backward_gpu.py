@@ -33,6 +33,7 @@ CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask)
     ("br_empty_rows", (64, 10), (32, 300), 4, 1, 128, "bf16", BR),
     ("noncausal_d64", (100, 37), (50, 260), 4, 4, 64, "bf16", NONE),
     ("zero_length", (0, 33, 0), (5, 33, 0), 2, 1, 64, "bf16", TL),
+    ("zero_length_d128", (0, 33, 0, 130), (5, 33, 0, 7), 4, 2, 128, "bf16", BR),
 ]
 
 

@@ -232,7 +232,10 @@ size_t attn_bwd_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
  *            head_dim]; type `dtype`.  Fully overwritten (rows no query
  *            reaches get zeros).
  * For bf16, an infinity or NaN in q, k, v or dout sets ATTN_ERR_DEVICE_RANGE
- * on the device flag.  dq, dk and dv must be 16-byte aligned.
+ * on the device flag.  dq, dk and dv must be 16-byte aligned.  For bf16 with
+ * head_dim 128, dq is summed over key tiles with fp32 reductions (its last
+ * bits can vary from call to call) unless attn_set_deterministic(1) selects
+ * the two-kernel form; dk and dv are reproducible in both forms.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v,
                      const void *o, const float *lse, const float *o_f32,

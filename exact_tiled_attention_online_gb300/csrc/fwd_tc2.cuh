@@ -195,6 +195,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int lo_b = act_b ? krb.n_begin - n0 : 0, hi_b = act_b ? krb.n_end - n0 : 0;
   const int N = hi_a > hi_b ? hi_a : hi_b;
   const int hk = h / a.group;
+  // Plain scores (no bias in the softmax): a watcher warp certifies the K / V
+  // tiles through the P barriers (measured 1.6% faster for the prefill; with
+  // a bias the softmax is the longer leg and P(n) then waits for K(n + 1),
+  // 9% slower, so the biased instances test the tiles in the MMA thread).
+  constexpr bool kWatch = !kTab && !kBias;
 
   if (threadIdx.x == 0) {
     mbar_init(&b->q_full, 1);
@@ -204,7 +209,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&b->k_empty[s], 1);
       mbar_init(&b->v_empty[s], 1);
       mbar_init(&b->s_full[s], 1);
-      mbar_init(&b->p_full[s], 128);
+      // kWatch: warp 2 adds one arrival per product (see below)
+      mbar_init(&b->p_full[s], kWatch ? 129 : 128);
       // kTab with heads2: each tile's threads store half of every row's
       // bias into both tiles' S columns, so both tiles arrive on both
       mbar_init(&b->b_full[s], kTab && a.heads2 ? 256 : 128);
@@ -263,6 +269,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
       b->filled_k = filled_k;
       b->filled_v = filled_v;
     }
+    } else if (warp == 2) {
+    // --------------------------------------------------------- TMA watcher
+    // kWatch: for each key tile n, once V(n) and K(n + 1) have landed,
+    // one more arrival on p_full of each tile with a product n (after that
+    // tile's previous phase has completed, so the arrival counts toward the
+    // phase of product n).
+    if (kWatch && lane == 0 && N > 0) {
+      bool ok = true;
+      for (int n = 0; ok && n < N; n++) {
+        ok = wait2(b, &b->v_full[n & 1], (n >> 1) & 1, p.err);
+        if (ok && n + 1 < N) ok = wait2(b, &b->k_full[(n + 1) & 1], ((n + 1) >> 1) & 1, p.err);
+        for (int x2 = 0; ok && x2 < 2; x2++) {
+          const int lo = x2 ? lo_b : lo_a, hi = x2 ? hi_b : hi_a;
+          if (n < lo || n >= hi) continue;
+          if (n > lo) ok = wait2(b, &b->p_full[x2], (n - 1 - lo) & 1, p.err);
+          if (ok) mbar_arrive(&b->p_full[x2]);
+        }
+      }
+    }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && N > 0) {
@@ -311,13 +336,19 @@ __global__ void __launch_bounds__(kThreads2, 1)
         mma_commit(&b->s_full[1]);
       }
       if (ok) mma_commit(&b->k_empty[0]);
+      // kWatch: phase c of p_full[X] (tile X's product n = lo_X + c)
+      // also certifies that V(n) and K(n + 1) have landed (warp 2 arrives on
+      // it only then), so the MMA thread tests those barriers only where no
+      // such phase covers them: a barrier test stalls the issuing thread long
+      // enough for the tensor pipe's short queue to run dry.
       for (int n = 0; ok && n < N; n++) {
         const int st = n & 1, n1 = n + 1, st1 = n1 & 1;
         bool v_ready = false, k1_ready = false;
         if (in_a(n)) {
           if (!(ok = wait2(b, &b->p_full[0], (n - lo_a) & 1, p.err))) break;
-          if (!(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
+          if (!kWatch && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
           v_ready = true;
+          k1_ready = kWatch;
           tc_fence_after();
           issue_pv(0, st, n > lo_a);
           mma_commit(&b->pv_done[0]);
@@ -325,7 +356,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // kTab: tile A's next Q K^T waits for its bias, which waits for
         // P_A V: tile B's P V goes first
         if (!kTab && in_a(n1)) {
-          if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
+          if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           k1_ready = true;
           tc_fence_after();
           issue_qk(0, st1);
@@ -333,7 +364,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         if (in_b(n)) {
           if (!(ok = wait2(b, &b->p_full[1], (n - lo_b) & 1, p.err))) break;
-          if (!v_ready && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
+          if (!kWatch && !v_ready && !(ok = wait2(b, &b->v_full[st], (n >> 1) & 1, p.err))) break;
+          if (kWatch) k1_ready = true;
           tc_fence_after();
           issue_pv(1, st, n > lo_b);
           mma_commit(&b->pv_done[1]);

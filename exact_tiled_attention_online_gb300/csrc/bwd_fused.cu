@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   const int m_end = (row_end(g.mask, g.window, j_last, g.nq, g.nk) + kRowsA - 1) / kRowsA;
   const int n_m = m_end > m_begin ? m_end - m_begin : 0;
   const int n_it = n_m * a.group;
+  // Unbiased scores: warp 2 certifies the Q / dO tiles through ps_full
+  // (measured 1.5% faster on training; with a bias the math is the longer
+  // leg and ps_full would then wait for tiles two steps ahead, 5% slower).
+  constexpr bool kWatch = !kBias && !kTab;
 
   if (threadIdx.x == 0) {
     mbar_init(&b->kv_full, 1);
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
     for (int s = 0; s < 2; s++) {
       mbar_init(&b->st_full[s], 1);
-      mbar_init(&b->ps_full[s], 256);
+      mbar_init(&b->ps_full[s], kWatch ? 256 + 1 : 256);  // math warps (+ the tile watcher)
       mbar_init(&b->dq_full[s], 1);
       mbar_init(&b->dq_free[s], 128);
     }
@@ -184,6 +188,20 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       b->sync.filled_one = 1;
       b->sync.filled_a = filled;
+    } else if (kWatch && warp == 2 && lane == 0 && n_it > 0) {
+      // Tile watcher: one more arrival on ps_full of step i once step
+      // i + 2's Q / dO tiles have landed (and step i - 2's phase of the same
+      // barrier has completed, so the arrival counts toward step i), so the
+      // MMA thread, which issues step i + 2's S^T right after that barrier,
+      // tests no TMA barrier: each test stalls it long enough for the
+      // tensor pipe's short queue to drain.
+      bool ok = true;
+      for (int it = 0; ok && it < n_it; it++) {
+        if (it + 2 < n_it)
+          ok = wait_bar(&b->sync, &b->qdo_full[(it + 2) % kStagesA], ((it + 2) / kStagesA) & 1, p.err);
+        if (ok && it >= 2) ok = wait_bar(&b->sync, &b->ps_full[it & 1], ((it - 2) >> 1) & 1, p.err);
+        if (ok) mbar_arrive(&b->ps_full[it & 1]);
+      }
     } else if (warp == 1 && lane == 0 && n_it > 0) {
       b->sync.mma_issued = 1;
       constexpr uint32_t idesc_s = idesc_f16_f32(128, kRowsA, 0, 0);
@@ -250,9 +268,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         issue_grad(kColS + tb * kRowsA + 16, dQm + qoff(qs), kColDK, it > 0);
         if (it + 1 == n_it) mma_commit(&b->mm_done);
         if (it + kStagesA < n_it) mma_commit(&b->qdo_empty[qs]);  // a later step refills it
-        if (it + 2 < n_it) {
+        if (it + 2 < n_it) {  // kWatch: step it + 2's Q / dO landed, certified by ps_full
           const int q2 = (it + 2) % kStagesA, u2 = (it + 2) / kStagesA;
-          if (!wait_bar(&b->sync, &b->qdo_full[q2], u2 & 1, p.err)) break;
+          if (!kWatch && !wait_bar(&b->sync, &b->qdo_full[q2], u2 & 1, p.err)) break;
           tc_fence_after();
           issue_st(dK0, dQk + qoff(q2), kColS + tb * kRowsA);
           if (!wait_bar(&b->sync, &b->dq_free[tb], (it >> 1) & 1, p.err)) break;

@@ -42,7 +42,8 @@ int internal_sm_count();
 
 namespace {
 
-// warps 0 TMA, 1 MMA + TMEM, 2-3 idle (warpgroup 0); 4-11 math, two per TMEM
+// warps 0 TMA, 1 MMA + TMEM, 2 tile watcher (unbiased instances), 3 idle
+// (warpgroup 0); 4-11 math, two per TMEM
 // lane quarter (warpgroups 1-2); 12-15 dQ readout, one per lane quarter
 constexpr int kThreadsF = 512;
 constexpr uint32_t kTmemColsF = 512;

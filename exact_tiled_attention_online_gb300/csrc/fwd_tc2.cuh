@@ -245,11 +245,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int filled_k = 0, filled_v = 0;
+      // Q is read by this CTA alone; each K / V tile by every row block of
+      // the KV group: Q may leave L2 first so K / V stay for the others
+      const uint64_t pol_once = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
       mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
       for (int t2 = 0; t2 < 2; t2++)
         for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full, c * 64,
-                      t2 ? h_b : h, g.q0 + i0 + t2 * rows_b);
+          tma_load_3d_hint(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full,
+                           c * 64, t2 ? h_b : h, g.q0 + i0 + t2 * rows_b, pol_once);
       for (int n = 0; n < N; n++) {
         const int st = n & 1, u = n >> 1;
         const int key_row = g.k0 + (n0 + n) * kTileKeys;
@@ -257,14 +260,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
         mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
         filled_k++;
         for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
-                      hk, key_row);
+          tma_load_3d_hint(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st],
+                           c * 64, hk, key_row, pol_kv);
         if (n >= 2 && !wait2(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
         filled_v++;
         for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st], c * 64,
-                      hk, key_row);
+          tma_load_3d_hint(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st],
+                           c * 64, hk, key_row, pol_kv);
       }
       b->filled_q = 1;  // for a drain after an early exit
       b->filled_k = filled_k;
@@ -692,7 +695,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             w.y = have ? pack_bf16x2(__uint_as_float(o32[e + 2]) * inv, __uint_as_float(o32[e + 3]) * inv) : 0u;
             w.z = have ? pack_bf16x2(__uint_as_float(o32[e + 4]) * inv, __uint_as_float(o32[e + 5]) * inv) : 0u;
             w.w = have ? pack_bf16x2(__uint_as_float(o32[e + 6]) * inv, __uint_as_float(o32[e + 7]) * inv) : 0u;
-            *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+            __stcs(reinterpret_cast<uint4 *>(dst + c * 32 + e), w);  // written once: streaming
           }
           if (p.o_f32) {
             float *df = p.o_f32 + ((size_t)t * p.hq + hx) * D + c * 32;
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
               f.y = have ? __uint_as_float(o32[e + 1]) * inv : 0.f;
               f.z = have ? __uint_as_float(o32[e + 2]) * inv : 0.f;
               f.w = have ? __uint_as_float(o32[e + 3]) * inv : 0.f;
-              *reinterpret_cast<float4 *>(df + e) = f;
+              __stcs(reinterpret_cast<float4 *>(df + e), f);
             }
           }
         }

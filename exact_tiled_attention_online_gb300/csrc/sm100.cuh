@@ -124,6 +124,29 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
       : "memory");
 }
 
+// The same with an L2 eviction-priority policy (from l2_policy_*): tiles
+// read once can leave L2 first, tiles other CTAs read again stay longer.
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m, uint64_t *bar,
+                                                 int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core operand reads) after this fence plus a thread sync.
 __device__ __forceinline__ void fence_proxy_async_smem() {

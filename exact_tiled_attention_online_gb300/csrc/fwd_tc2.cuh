@@ -38,6 +38,8 @@
 #include "tma_map.h"
 
 namespace attn {
+
+int internal_sm_count();
 using namespace sm100;
 
 namespace {
@@ -72,6 +74,8 @@ struct Tc2Args {
   int n_pairs;    // CTAs per (sequence, head), or per (sequence, head pair) with heads2
   int heads2;     // 1: tiles A and B are the same 128 rows of two heads of one KV head
   int compact;    // 1: the grid is the compact work list of compact_item()
+  int ahead;      // > 0: near its end a CTA prefetches into L2 the Q tiles of the
+                  // CTA this many blocks later (the one likely to start next)
 };
 
 // Compact work list for packed batches of at most 32 sequences.  Work item c
@@ -268,6 +272,24 @@ __global__ void __launch_bounds__(kThreads2, 1)
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d_hint(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st],
                            c * 64, hk, key_row, pol_kv);
+      }
+      // The grid runs one CTA per SM at a time, so a CTA's start waits on its
+      // Q tiles; warm L2 with those of the CTA `ahead` blocks later (about
+      // one wave on), which starts when some SM frees up.
+      if (!a.compact && a.ahead > 0) {
+        const long long nb = (long long)blockIdx.x + a.ahead;
+        if (nb < (long long)gridDim.x) {
+          const int per_rank = units * p.batch;
+          const int rank2 = (int)(nb / per_rank), unit2 = (int)(nb % units);
+          const int seq2 = (int)((nb % per_rank) / units);
+          const int q0_2 = __ldg(p.cu_q + seq2), nq2 = __ldg(p.cu_q + seq2 + 1) - q0_2;
+          const int i0_2 = (a.n_pairs - 1 - rank2) * (kTileRows + rows_b);
+          const int h2 = unit2 * (a.heads2 ? 2 : 1), hb2 = a.heads2 ? h2 + 1 : h2;
+          if (i0_2 < nq2)
+            for (int t2 = 0; t2 < 2; t2++)
+              for (int c = 0; c < L::kChunks; c++)
+                tma_prefetch_3d(&tm_q, c * 64, t2 ? hb2 : h2, q0_2 + i0_2 + t2 * rows_b);
+        }
       }
       b->filled_q = 1;  // for a drain after an early exit
       b->filled_k = filled_k;
@@ -785,6 +807,7 @@ inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorM
   // it is shorter: sum_s ceil(nq_s / R) <= (total_q + batch (R - 1)) / R
   // items per head unit, against n_pairs per sequence and unit otherwise.
   a->compact = 0;
+  a->ahead = internal_sm_count();
   if (p.batch <= 32) {
     const long long R = *rows_per_cta;
     const long long items = ((long long)p.total_q + p.batch * (R - 1)) / R * units;

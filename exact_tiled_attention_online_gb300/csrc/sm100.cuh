@@ -135,6 +135,15 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// Warm L2 with a box of a tensor map (no shared-memory destination, no
+// barrier; coordinates past the tensor are ignored like a load's).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -23,12 +23,17 @@
 // With the extra registers a softmax thread loads its whole 128-score row
 // from TMEM with one wait, takes the max, and writes the 64 packed
 // probabilities back.  Instances add the linear positional bias in the softmax (kBias)
-// or an explicit bias tensor that the softmax warps store into S before
-// Q K^T accumulates onto it (kTab; then tile A's next Q K^T follows tile B's
-// P V, since A's bias waits for A's P V to finish reading P).
+// or an explicit bias tensor, in one of two ways (kTab): 1, the softmax warps
+// load their rows' entries and store them into S before Q K^T accumulates
+// onto it (then tile A's next Q K^T follows tile B's P V, since A's bias
+// waits for A's P V to finish reading P); 2, for a tensor the two heads of a
+// CTA share, warp 2 streams each key tile's entries into shared memory with
+// TMA and the softmax adds them to the scores it loads (the schedule stays
+// the plain one; with D = 128 the V ring then has one stage, for room).
 #pragma once
 
 #include <stdio.h>
+#include <string.h>
 
 #include <type_traits>
 
@@ -55,17 +60,26 @@ static_assert(kThreads2 * kRegsLaunch <= 65536, "register file");
 constexpr float kRescale2 = 8.0f;
 constexpr uint32_t kCols2 = 512;
 
-template <int D>
+// kStaged: room for one key tile of fp32 bias entries (128 rows x 128 keys
+// as four 128-byte-swizzled boxes of 32 keys), the V ring shrinking to one
+// stage when two do not fit beside it.
+template <int D, bool kStaged = false>
 struct Layout2 {
   static constexpr int kChunk = 128 * 128;
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;
+  static constexpr int kTabBox = 128 * 32 * 4;
+  static constexpr int kTabBytes = kStaged ? 4 * kTabBox : 0;
+  static constexpr int kMaxSmem = 227 * 1024;
+  static constexpr int kVStages = 6 * kTile + kTabBytes + 256 + 1024 <= kMaxSmem ? 2 : 1;
   static constexpr int kQA = 0;
   static constexpr int kK = 2 * kTile;      // [2] stages
-  static constexpr int kV = kK + 2 * kTile;  // [2] stages
-  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kV = kK + 2 * kTile;  // [kVStages] stages
+  static constexpr int kT = kV + kVStages * kTile;
+  static constexpr int kBar = kT + kTabBytes;
   static constexpr int kUsed = kBar + 256;
   static constexpr int kAlloc = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
+  static_assert(kUsed + 1024 <= kMaxSmem, "shared memory");
 };
 
 struct Tc2Args {
@@ -76,6 +90,7 @@ struct Tc2Args {
   int compact;    // 1: the grid is the compact work list of compact_item()
   int ahead;      // > 0: near its end a CTA prefetches into L2 the Q tiles of the
                   // CTA this many blocks later (the one likely to start next)
+  int staged;     // 1: the bias tensor goes through shared memory (kTab 2; heads2 set)
 };
 
 // Compact work list for packed batches of at most 32 sequences.  Work item c
@@ -112,14 +127,16 @@ __device__ __forceinline__ bool compact_item(const int32_t *cu_q, int batch, int
 struct Bars2 {
   uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];  // [tile A, tile B]
-  uint64_t b_full[2];  // kTab: the next tile's bias is in the tile's S columns
+  uint64_t b_full[2];  // kTab 1: the next tile's bias is in the tile's S columns
+  uint64_t t_full[4];  // kTab 2: box c of the key tile's entries has landed
+  uint64_t t_empty;    // kTab 2: both tiles have added the entries
   uint64_t drain;      // the MMA thread's products have all completed
   uint64_t limit_ns;   // bound of every wait of this call
   uint32_t tmem_base;
   int abort;
   // for a drain after an early exit: Q fills, K / V ring fills (stage =
   // fill % 2) the producer issued, and whether the MMA thread issued any
-  int filled_q, filled_k, filled_v, mma_issued;
+  int filled_q, filled_k, filled_v, filled_t, mma_issued;
 };
 
 static_assert(sizeof(Bars2) <= 256, "barrier block fits its shared-memory slot");
@@ -139,18 +156,28 @@ __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, 
 // keeps that output for the backward); without it O is normalised by the
 // fp32 sum.  kBias: add the linear positional bias (with kPosScale false:
 // the bias must be in the logits before the max).  kTab: add an explicit
-// bias tensor, which the softmax warps write (divided by the positive scale)
-// into the tile's S columns before Q K^T accumulates onto it, so the scores
-// arrive biased and the softmax itself is unchanged.
+// bias tensor, divided by the positive scale so that c2 times the biased
+// raw score is the logit in log2 units.  kTab 1: the softmax warps write
+// the entries into the tile's S columns before Q K^T accumulates onto them,
+// so the scores arrive biased.  kTab 2 (heads2, a tensor shared by the two
+// heads, tm_t its map): the entries of each key tile arrive in shared memory
+// and each softmax thread adds its row's to the scores it loads.
 // kDelta: the backward's per-row term instead of the outputs: the epilogue
 // forms D_i = dO_i . O_i from the fp32 output (with kRoundedSum, an exact
 // convex combination of V rows) and the row of dO, writes D_i to p.delta
 // and stores neither O nor lse.
-template <int D, bool kPosScale, bool kRoundedSum, bool kBias, bool kTab, bool kDelta>
+template <int D, bool kPosScale, bool kRoundedSum, bool kBias, int kTab, bool kDelta>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const Tc2Args a) {
-  using L = Layout2<D>;
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+                   const Tc2Args a) {
+  constexpr bool kTabReg = kTab == 1, kTabSmem = kTab == 2;
+  using L = Layout2<D, kTabSmem>;
+  // V ring: fill n uses barriers v_full / v_empty[n & 1] (phase (n >> 1) & 1)
+  // and shared-memory slot n % kVSt; with one slot, fill n also waits for
+  // fill n - 1 to be released (a one-stage ring behind the two-stage
+  // barrier pattern, which keeps the MMA thread's code as it is)
+  constexpr int kVSt = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
@@ -216,15 +243,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&b->s_full[s], 1);
       // kWatch: warp 2 adds one arrival per product (see below)
       mbar_init(&b->p_full[s], kWatch ? 129 : 128);
-      // kTab with heads2: each tile's threads store half of every row's
+      // kTab 1 with heads2: each tile's threads store half of every row's
       // bias into both tiles' S columns, so both tiles arrive on both
-      mbar_init(&b->b_full[s], kTab && a.heads2 ? 256 : 128);
+      mbar_init(&b->b_full[s], kTabReg && a.heads2 ? 256 : 128);
       mbar_init(&b->pv_done[s], 1);
     }
+    for (int c = 0; c < 4; c++) mbar_init(&b->t_full[c], 1);
+    mbar_init(&b->t_empty, 256);  // every softmax thread of both tiles
     mbar_init(&b->drain, 1);
     b->limit_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     b->abort = 0;
-    b->filled_q = b->filled_k = b->filled_v = b->mma_issued = 0;
+    b->filled_q = b->filled_k = b->filled_v = b->filled_t = b->mma_issued = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -266,12 +295,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
         for (int c = 0; c < L::kChunks; c++)
           tma_load_3d_hint(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st],
                            c * 64, hk, key_row, pol_kv);
-        if (n >= 2 && !wait2(b, &b->v_empty[st], (u - 1) & 1, p.err)) break;
+        if (n >= kVSt &&
+            !wait2(b, &b->v_empty[(n - kVSt) & 1], ((n - kVSt) >> 1) & 1, p.err))
+          break;
         mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
         filled_v++;
         for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d_hint(smem + L::kV + st * L::kTile + c * L::kChunk, &tm_v, &b->v_full[st],
-                           c * 64, hk, key_row, pol_kv);
+          tma_load_3d_hint(smem + L::kV + (n % kVSt) * L::kTile + c * L::kChunk, &tm_v,
+                           &b->v_full[st], c * 64, hk, key_row, pol_kv);
       }
       // The grid runs one CTA per SM at a time, so a CTA's start waits on its
       // Q tiles; warm L2 with those of the CTA `ahead` blocks later (about
@@ -314,6 +345,26 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
       }
     }
+    // ------------------------------------------------- bias entries (kTab 2)
+    // Key tile n0 + u's entries for the CTA's 128 rows (both tiles' heads
+    // share them), as four boxes of 32 keys, once both tiles have added the
+    // previous tile's.  Rows and keys past the tensor's extent read as 0
+    // (their scores are masked or never stored).
+    if (kTabSmem && lane == 0 && N > 0) {
+      tma_prefetch_desc(&tm_t);
+      const int tz = p.bss ? seq : 0;
+      int filled_t = 0;
+      for (int u = 0; u < N; u++) {
+        if (u > 0 && !wait2(b, &b->t_empty, (u - 1) & 1, p.err)) break;
+        const int j0 = (n0 + u) * kTileKeys;
+        filled_t++;
+        for (int c = 0; c < 4; c++) {
+          mbar_arrive_expect_tx(&b->t_full[c], L::kTabBox);
+          tma_load_3d(smem + L::kT + c * L::kTabBox, &tm_t, &b->t_full[c], j0 + 32 * c, i0, tz);
+        }
+      }
+      b->filled_t = filled_t;
+    }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && N > 0) {
@@ -332,11 +383,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++) {
           const uint64_t off = (uint64_t)((((kk >> 2) * L::kChunk) + (kk & 3) * 32) >> 4);
-          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, (kTab || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(d_tmem, dq + off, dk + off, idesc_qk, (kTabReg || kk > 0) ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int x, int st, bool acc) {  // O_x += P V, P in tensor memory
-        const uint64_t dv = dV0 + (uint64_t)((st * L::kTile) >> 4);
+        uint64_t dv = dV0 + (uint64_t)(((kVSt == 2 ? st : 0) * L::kTile) >> 4);
+        // one V slot: the descriptors would be loop-invariant, and holding
+        // them between products costs the control warps more registers than
+        // they have; an opaque copy keeps them computed per product
+        if constexpr (kVSt == 1) asm volatile("" : "+l"(dv));
         const uint32_t d_tmem = tmem + 256u + (uint32_t)(x * D);
         const uint32_t a_tmem = tmem + (uint32_t)(x * kTileKeys + 64);  // P: S columns [64, 128)
 #pragma unroll
@@ -348,15 +403,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // s_full / p_full / pv_done barriers.
       auto in_a = [&](int n) { return n >= lo_a && n < hi_a; };
       auto in_b = [&](int n) { return n >= lo_b && n < hi_b; };
-      // kTab: Q K^T of tile X's c-th product accumulates onto the bias its
+      // kTab 1: Q K^T of tile X's c-th product accumulates onto the bias its
       // softmax warps stored, announced by phase c of b_full[X]
       bool ok = wait2(b, &b->q_full, 0, p.err) && wait2(b, &b->k_full[0], 0, p.err);
-      if (ok && in_a(0) && (!kTab || (ok = wait2(b, &b->b_full[0], 0, p.err)))) {
+      if (ok && in_a(0) && (!kTabReg || (ok = wait2(b, &b->b_full[0], 0, p.err)))) {
         tc_fence_after();
         issue_qk(0, 0);
         mma_commit(&b->s_full[0]);
       }
-      if (ok && in_b(0) && (!kTab || (ok = wait2(b, &b->b_full[1], 0, p.err)))) {
+      if (ok && in_b(0) && (!kTabReg || (ok = wait2(b, &b->b_full[1], 0, p.err)))) {
         tc_fence_after();
         issue_qk(1, 0);
         mma_commit(&b->s_full[1]);
@@ -379,9 +434,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
           issue_pv(0, st, n > lo_a);
           mma_commit(&b->pv_done[0]);
         }
-        // kTab: tile A's next Q K^T waits for its bias, which waits for
+        // kTab 1: tile A's next Q K^T waits for its bias, which waits for
         // P_A V: tile B's P V goes first
-        if (!kTab && in_a(n1)) {
+        if (!kTabReg && in_a(n1)) {
           if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           k1_ready = true;
           tc_fence_after();
@@ -397,7 +452,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           mma_commit(&b->pv_done[1]);
         }
         mma_commit(&b->v_empty[st]);
-        if (kTab && in_a(n1)) {
+        if (kTabReg && in_a(n1)) {
           if (!(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
           k1_ready = true;
           if (!(ok = wait2(b, &b->b_full[0], (n1 - lo_a) & 1, p.err))) break;
@@ -407,7 +462,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         if (in_b(n1)) {
           if (!k1_ready && !(ok = wait2(b, &b->k_full[st1], (n1 >> 1) & 1, p.err))) break;
-          if (kTab && !(ok = wait2(b, &b->b_full[1], (n1 - lo_b) & 1, p.err))) break;
+          if (kTabReg && !(ok = wait2(b, &b->b_full[1], (n1 - lo_b) & 1, p.err))) break;
           tc_fence_after();
           issue_qk(1, st1);
           mma_commit(&b->s_full[1]);
@@ -443,11 +498,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const float bound = (float)(i + causal_offset(g.mask, g.nq, g.nk));  // the row's causal bound
     float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
-    // kTab: this row's bias entries for key tile n, divided by the positive
+    // kTab 1: this row's bias entries for key tile n, divided by the positive
     // scale (so that c2 times the accumulated score is the biased logit in
     // log2 units), into the tile's S columns; keys past the sequence and rows
     // past it get 0 (their lanes are masked or never stored).
-    const float *brow = kTab && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, hx, i) : nullptr;
+    const float *brow = kTabReg && row_in ? btab_row(p.btab, p.bss, p.bhs, p.brs, seq, hx, i) : nullptr;
     const float inv_scale = kTab ? 1.f / p.scale : 0.f;
     // the loads are issued before the wait that gates the store, so their
     // latency overlaps it
@@ -484,7 +539,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     // shared by the heads is the same for both: tile X's threads load keys
     // [64 X, 64 X + 64) of their row and store them into both tiles' S
     // columns, so every row's entries cross L2 once per CTA, not twice.
-    const bool share = kTab && a.heads2;
+    const bool share = kTabReg && a.heads2;
     auto load_bias_half = [&](int n, uint32_t (&bv)[kTileKeys / 2]) {
       const int j0 = n * kTileKeys + x * (kTileKeys / 2);
       const bool vec = brow && j0 + kTileKeys / 2 <= g.nk &&
@@ -519,7 +574,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_arrive(&b->b_full[0]);
       mbar_arrive(&b->b_full[1]);
     };
-    if (kTab && n_mine > 0) {
+    if (kTabReg && n_mine > 0) {
       if (share) {
         uint32_t bv[kTileKeys / 2];
         load_bias_half(kr.n_begin, bv);
@@ -544,6 +599,37 @@ __global__ void __launch_bounds__(kThreads2, 1)
       static_assert(kTileKeys == 128, "one 128-column load");
       tmem_ld128(s_col, v);
       tmem_wait_ld();
+      if constexpr (kTabSmem) {
+        // fill `it` of the entries (both tiles run the same key tiles): box c
+        // holds keys [32 c, 32 c + 32) for the 128 rows, row r's 16-byte
+        // chunk k at 128 r + 16 (k ^ (r & 7)) (the 128-byte swizzle), so a
+        // warp's 32 rows read distinct banks.  Added before the mask below,
+        // which overwrites masked lanes whatever they hold.
+        const uint64_t is2 = f2(inv_scale, inv_scale);
+        const uint8_t *t_row = smem + L::kT + r * 128;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+          if (!wait2(b, &b->t_full[c], it & 1, p.err)) ok = false;
+#pragma unroll
+          for (int k = 0; k < 8; k++) {
+            const float4 f =
+                *reinterpret_cast<const float4 *>(t_row + c * L::kTabBox + ((k ^ (r & 7)) << 4));
+            const int e = 32 * c + 4 * k;
+            float y0, y1, y2, y3;
+            f2_split(ffma2(f2(f.x, f.y), is2, f2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]))), y0, y1);
+            f2_split(ffma2(f2(f.z, f.w), is2, f2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]))), y2, y3);
+            v[e] = __float_as_uint(y0);
+            v[e + 1] = __float_as_uint(y1);
+            v[e + 2] = __float_as_uint(y2);
+            v[e + 3] = __float_as_uint(y3);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive(&b->t_empty);
+      }
       if (!kr.full(n)) {
         // lanes outside [first, limit) of this row: first <= limit, so one
         // unsigned compare tests both ends
@@ -639,7 +725,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tmem_wait_st();  // P (S columns [64, 128)) and any rescaled O are in place
       tc_fence_before();
       mbar_arrive(&b->p_full[x]);
-      if (kTab && it + 1 < n_mine) {
+      if (kTabReg && it + 1 < n_mine) {
         // the next tile's bias may overwrite S once P V has read P (with
         // share, both tiles' P: both tiles' S columns are written)
         if (share) {
@@ -750,6 +836,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
       for (int st = 0; st < 2; st++)
         drained = drain_phase(&b->k_full[st], ring_armed(b->filled_k, st, 2)) &&
                   drain_phase(&b->v_full[st], ring_armed(b->filled_v, st, 2)) && drained;
+      for (int c = 0; c < 4; c++)  // every fill arms each box's barrier once
+        drained = drain_phase(&b->t_full[c], b->filled_t) && drained;
       if (!drained) raise_error(p.err, ATTN_ERR_DEVICE_TIMEOUT);
     }
     if (threadIdx.x == 32 && b->mma_issued && !drain_mma(&b->drain))
@@ -763,20 +851,21 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-template <int D, bool kPos, bool kRs, bool kBias, bool kTab = false, bool kDelta = false>
+// mt: the bias tensor's map (used by kTab 2 only).
+template <int D, bool kPos, bool kRs, bool kBias, int kTab = 0, bool kDelta = false>
 cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                    const CUtensorMap &mv, unsigned ctas, cudaStream_t st) {
+                    const CUtensorMap &mv, const CUtensorMap &mt, unsigned ctas, cudaStream_t st) {
+  constexpr int smem = Layout2<D, kTab == 2>::kAlloc;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(fwd_tc2_kernel<D, kPos, kRs, kBias, kTab, kDelta>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Layout2<D>::kAlloc);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab, kDelta><<<ctas, kThreads2, Layout2<D>::kAlloc, st>>>(mq, mk, mv, a);
+  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab, kDelta><<<ctas, kThreads2, smem, st>>>(mq, mk, mv, mt, a);
   return cudaGetLastError();
 }
 
@@ -785,15 +874,25 @@ cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &
 // head per CTA when the group pairs up: both tiles then have the same key
 // range, no idle diagonal tile (windowed prefill 2%, linear bias 1.5%
 // faster, causal unchanged); with a bias tensor it measured 7% slower, so
-// those keep two row blocks of one head) and the tensor maps of q, k, v.
-// false when a map is rejected or the grid is too large.
+// those keep two row blocks of one head) and the tensor maps of q, k, v and,
+// when the bias tensor goes through shared memory, of the bias (mt; zeroed
+// otherwise).  false when a map of q, k or v is rejected or the grid is too
+// large.
 inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorMap *mk,
-                      CUtensorMap *mv, long long *ctas, int *rows_per_cta) {
+                      CUtensorMap *mv, CUtensorMap *mt, long long *ctas, int *rows_per_cta) {
   a->p = p;
   a->group = p.hq / p.hkv;
   // a bias tensor pairs heads only when the heads share it (then the two
   // tiles share its entries too)
   a->heads2 = a->group % 2 == 0 && (!p.btab || p.bhs == 0) ? 1 : 0;
+  // Shared entries of d = 128 heads stream through shared memory when TMA
+  // can address them (16-byte aligned base and strides); otherwise the
+  // softmax warps load them (kTab 1).
+  memset(mt, 0, sizeof(*mt));
+  a->staged = a->heads2 && p.btab && p.d == 128 &&
+                      make_bias_map(mt, p.btab, p.max_k, p.max_q, p.batch, p.brs, p.bss)
+                  ? 1
+                  : 0;
   *rows_per_cta = a->heads2 ? kTileRows : 2 * kTileRows;
   a->n_pairs = (p.max_q + *rows_per_cta - 1) / *rows_per_cta;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -46,4 +46,28 @@ inline bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int 
   return r == CUDA_SUCCESS;
 }
 
+// An fp32 bias tensor seen as 3-D (key, row, sequence), element strides
+// row_stride and seq_stride (0: the sequences share one set of entries),
+// loaded in boxes of 32 keys x 128 rows with the 128-byte swizzle.  Entries
+// past `keys`, `rows` or `seqs` read as 0.  false when the encoder rejects
+// it (the base or a stride not a multiple of 16 bytes).
+inline bool make_bias_map(CUtensorMap *m, const float *base, int keys, int rows, int seqs,
+                          long long row_stride, long long seq_stride) {
+  auto enc = tensor_map_encoder();
+  if (!enc || !base || keys <= 0 || rows <= 0 || seqs <= 0 || row_stride <= 0 || seq_stride < 0)
+    return false;
+  if (seq_stride == 0) {
+    seqs = 1;
+    seq_stride = row_stride * rows;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)keys, (cuuint64_t)rows, (cuuint64_t)seqs};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride * 4, (cuuint64_t)seq_stride * 4};
+  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace attn

@@ -55,6 +55,9 @@ CASES = [  # (name, lq, lk, hq, hkv, d, mask, v shift per sequence, window, bias
     ("window_shift10", (300, 129), None, 8, 2, 128, TL, 10.0, 64, None),
     ("slopes_shift10", (300, 50), (700, 40), 4, 2, 128, BR, 10.0, 0, "slopes"),
     ("bias_tensor_shift10", (63, 129, 1, 200), None, 8, 2, 128, TL, 10.0, 0, "tensor"),
+    # one set of entries per sequence shared by the heads: staged through
+    # shared memory in the recomputing forward
+    ("bias_shared_shift10", (63, 129, 1, 200), None, 8, 2, 128, TL, 10.0, 0, "shared"),
 ]
 
 
@@ -67,8 +70,8 @@ def test_backward_without_o_f32(case):
                       v_shift_per_seq=shift, window=window)
     x = inputs.make_inputs(w)
     slopes = inputs.bias_slopes(hq) if kind == "slopes" else None
-    bias = inputs.bias_tensor(w.batch, hq, w.max_q, w.max_k, seed=72, dead_rows=2) \
-        if kind == "tensor" else None
+    bias = inputs.bias_tensor(w.batch, 1 if kind == "shared" else hq, w.max_q, w.max_k, seed=72,
+                              dead_rows=2) if kind in ("tensor", "shared") else None
     (o, lse, dq, dk, dv), plan = run(x, False, slopes, bias)
     assert "fwd_tc2_delta" in plan and tc_backward(plan), plan
     rdq, rdk, rdv, ro, rlse = oracle.bwd(

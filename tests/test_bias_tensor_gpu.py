@@ -43,6 +43,16 @@ CASES = [  # (name, lq, lk, hq, hkv, d, dtype, mask, window, bias broadcast, slo
     ("bf16_none_slopes", (50, 77), (70, 20), 4, 4, 128, "bf16", NONE, 0, False, True, "fwd_simt", "simt"),
     ("bf16_tl_window", (90, 333), None, 4, 2, 64, "bf16", TL, 9, False, False, "fwd_tc2", "tc"),
     ("fp32_br", (37, 70), (50, 70), 4, 2, 64, "fp32", BR, 0, True, True, "fwd_simt", "simt"),
+    # d = 128 with the entries shared by the heads of a CTA: staged through
+    # shared memory (key extent a multiple of 4 entries, 16-byte rows)
+    ("bf16_tl_bcast_d128", (63, 129, 1, 200), None, 8, 2, 128, "bf16", TL, 0, True, False,
+     "_btab_smem", "tc"),
+    ("bf16_tl_window_bcast_d128", (90, 332, 260), None, 4, 2, 128, "bf16", TL, 9, True, False,
+     "_btab_smem", "tc"),
+    ("bf16_none_bcast_d128", (200, 77), (150, 300), 4, 2, 128, "bf16", NONE, 0, True, False,
+     "_btab_smem", "tc"),
+    ("bf16_br_bcast_d128", (40, 9, 130), (100, 300, 140), 8, 4, 128, "bf16", BR, 0, True, False,
+     "_btab_smem", "tc"),
 ]
 
 
@@ -101,6 +111,26 @@ def test_zero_bias_tensor_matches_no_bias_oracle():
     compare.check_close("dv", dv, rdv)
 
 
+@pytest.mark.parametrize("keys,staged", [(200, True), (131, False), (70, False)])
+def test_bias_tensor_staging_choice(keys, staged):
+    """Entries shared by a CTA's two heads go through shared memory when TMA
+    can address them (rows a multiple of 16 bytes); otherwise the softmax
+    warps load them.  Both routes meet the oracle."""
+    w = inputs.custom("bstage", (keys, keys - 50), (keys, keys - 50), 4, 2, 128, "bf16", TL,
+                      seed=68, backward=True)
+    x = inputs.make_inputs(w)
+    bias = inputs.bias_tensor(1, 1, w.max_q, w.max_k, seed=69, dead_rows=1)
+    (o, lse, dq, dk, dv), (fplan, _) = run(x, bias)
+    assert "_btab" in fplan and ("_btab_smem" in fplan) == staged, fplan
+    rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], w.scale, TL, bias=bias)
+    compare.check_close("o", o, ro)
+    compare.check_lse("lse", lse, rlse)
+    compare.check_close("dq", dq, rdq)
+    compare.check_close("dk", dk, rdk)
+    compare.check_close("dv", dv, rdv)
+
+
 @pytest.mark.parametrize("shape", ["heads_only", "sequences_only"])
 def test_bias_tensor_mixed_broadcast(shape):
     """A tensor with one entry per head shared by every sequence, or one per
@@ -131,7 +161,7 @@ def test_bias_tensor_prefill_full_size_sampled():
     d = {k: (t.cuda() if hasattr(t, "cuda") else t) for k, t in x.items()}
     o, lse = attn.fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], w.max_q,
                       w.max_k, w.mask, w.scale, bias=bias.cuda())
-    assert "fwd_tc2" in attn.last_plan() and "_btab" in attn.last_plan()
+    assert "fwd_tc2" in attn.last_plan() and "_btab_smem" in attn.last_plan()
     torch.cuda.synchronize()
     assert attn.get_device_error() == 0
     rows = sample_rows(w, 24, seed=71)

@@ -166,7 +166,10 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o,
  * -inf removes the pair (an explicit mask); a row without any finite logit
  * is an empty row (O = 0, lse = -inf).  +inf and NaN entries are not
  * allowed.  The caller owns the device memory, which must cover every entry
- * of every allowed pair and stay valid until the call's kernels finish.
+ * of the [batch, n_heads_q, max_seqlen_q, max_seqlen_k] box the strides
+ * describe (the tensor-core forward may read entries outside the allowed
+ * pairs, and then ignores them) and stay valid until the call's kernels
+ * finish.
  */
 typedef struct {
   const float *data;
@@ -179,8 +182,11 @@ typedef struct {
  * none; both NULL is exactly attn_fwd).  Same results; ATTN_ERR_INVALID_ARG
  * for a stride that breaks the rules above, a negative bias stride or a bias
  * without data.  bf16 calls with a bias tensor, a positive scale and no
- * bias_slopes run on the tensor-core prefill kernel (the entries are stored
- * into the score buffer before Q K^T accumulates onto them); other calls
+ * bias_slopes run on the tensor-core prefill kernel: with head_dim 128, an
+ * even GQA group, head_stride 0 and a 16-byte aligned base, row and
+ * sequence stride, the entries stream through shared memory by TMA and the
+ * softmax adds them; otherwise they are stored into the score buffer before
+ * Q K^T accumulates onto them; other calls
  * with a bias tensor (fp32, a non-positive scale, or slopes as well) run on
  * the CUDA-core kernels (one warp per query row and head).
  */

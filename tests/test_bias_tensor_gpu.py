@@ -131,6 +131,46 @@ def test_bias_tensor_staging_choice(keys, staged):
     compare.check_close("dv", dv, rdv)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_bias_tensor_staged_random_shapes(seed):
+    """Random packed batches on the staged forward (head_dim 128, even GQA
+    group, entries shared by the heads): 1-4 sequences of 0-300 queries, keys
+    as many (top-left) or independent (bottom-right, no mask), a window half
+    of the time with a causal rule, a tensor per sequence or one for all, its
+    key dimension padded to a multiple of 4 entries (16-byte rows), about a
+    fifth of the entries and a few whole rows -inf; forward and backward
+    against the oracle."""
+    rng = np.random.default_rng(100 + seed)
+    batch = int(rng.integers(1, 5))
+    mask = [TL, BR, NONE][int(rng.integers(3))]
+    lq = [int(x) for x in rng.integers(0, 301, size=batch)]
+    lk = lq if mask == TL else [int(x) for x in rng.integers(1, 301, size=batch)]
+    hkv = int(rng.choice([1, 2]))
+    hq = hkv * int(rng.choice([2, 4]))
+    window = int(rng.integers(1, 200)) if mask != NONE and rng.random() < 0.5 else 0
+    w = inputs.custom(f"bsrand{seed}", lq, lk, hq, hkv, 128, "bf16", mask, seed=110 + seed,
+                      backward=True, v_shift_per_seq=2.0, window=window)
+    x = inputs.make_inputs(w)
+    per_seq = bool(rng.random() < 0.5)
+    keys = max(4, (w.max_k + 3) // 4 * 4)
+    bias = inputs.bias_tensor(w.batch if per_seq else 1, 1, max(1, w.max_q), keys, seed=120 + seed,
+                              dead_rows=2)
+    (o, lse, dq, dk, dv), (fplan, _) = run(x, bias)
+    if w.max_q > 0:
+        assert "_btab_smem" in fplan, fplan
+    rdq, rdk, rdv, ro, rlse = oracle.bwd(x["q"], x["k"], x["v"], x["dout"], x["cu_seqlens_q"],
+                                         x["cu_seqlens_k"], w.scale, mask, window=window,
+                                         bias=bias)
+    tag = f"seed {seed}: lq {lq} lk {lk} hq {hq} hkv {hkv} mask {mask} window {window}"
+    compare.check_close(f"o ({tag})", o, ro)
+    compare.check_lse(f"lse ({tag})", lse, rlse)
+    compare.check_close(f"dq ({tag})", dq, rdq)
+    compare.check_close(f"dk ({tag})", dk, rdk)
+    compare.check_close(f"dv ({tag})", dv, rdv)
+    for h, t in np.argwhere(np.isneginf(rlse)):
+        assert np.all(compare.to_np(o)[t, h] == 0.0)
+
+
 @pytest.mark.parametrize("shape", ["heads_only", "sequences_only"])
 def test_bias_tensor_mixed_broadcast(shape):
     """A tensor with one entry per head shared by every sequence, or one per

@@ -7,24 +7,22 @@ namespace attn {
 namespace {
 
 template <int D>
-cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                      const CUtensorMap &mv, const CUtensorMap &mt, unsigned ctas,
-                      cudaStream_t st) {
+cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap (&m)[5], unsigned ctas, cudaStream_t st) {
   const bool pos = a.p.scale_log2 > 0.f, rs = a.p.o_f32 != nullptr;
   if (a.p.btab) {  // the caller routes a bias tensor here only with a positive scale, no slopes
     if constexpr (D == 128)
       if (a.staged)
-        return rs ? launch2<D, true, true, false, 2>(a, mq, mk, mv, mt, ctas, st)
-                  : launch2<D, true, false, false, 2>(a, mq, mk, mv, mt, ctas, st);
-    return rs ? launch2<D, true, true, false, 1>(a, mq, mk, mv, mt, ctas, st)
-              : launch2<D, true, false, false, 1>(a, mq, mk, mv, mt, ctas, st);
+        return rs ? launch2<D, true, true, false, 2>(a, m, ctas, st)
+                  : launch2<D, true, false, false, 2>(a, m, ctas, st);
+    return rs ? launch2<D, true, true, false, 1>(a, m, ctas, st)
+              : launch2<D, true, false, false, 1>(a, m, ctas, st);
   }
-  if (a.p.slopes) return rs ? launch2<D, false, true, true>(a, mq, mk, mv, mt, ctas, st)
-                            : launch2<D, false, false, true>(a, mq, mk, mv, mt, ctas, st);
-  if (pos) return rs ? launch2<D, true, true, false>(a, mq, mk, mv, mt, ctas, st)
-                     : launch2<D, true, false, false>(a, mq, mk, mv, mt, ctas, st);
-  return rs ? launch2<D, false, true, false>(a, mq, mk, mv, mt, ctas, st)
-            : launch2<D, false, false, false>(a, mq, mk, mv, mt, ctas, st);
+  if (a.p.slopes) return rs ? launch2<D, false, true, true>(a, m, ctas, st)
+                            : launch2<D, false, false, true>(a, m, ctas, st);
+  if (pos) return rs ? launch2<D, true, true, false>(a, m, ctas, st)
+                     : launch2<D, true, false, false>(a, m, ctas, st);
+  return rs ? launch2<D, false, true, false>(a, m, ctas, st)
+            : launch2<D, false, false, false>(a, m, ctas, st);
 }
 
 }  // namespace
@@ -33,16 +31,16 @@ cudaError_t launch2_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap
 cudaError_t launch_fwd_tc2(const FwdParams &p, cudaStream_t st, char *desc, size_t desc_len) {
   snprintf(desc, desc_len, "fwd_tc2_d%d (tensor map or grid size rejected)", p.d);
   Tc2Args a;
-  CUtensorMap mq, mk, mv, mt;
+  CUtensorMap m[5];
   long long ctas = 0;
   int rows_per_cta = 0;
-  if (!setup_tc2(p, &a, &mq, &mk, &mv, &mt, &ctas, &rows_per_cta)) return cudaErrorInvalidValue;
+  if (!setup_tc2(p, &a, m, &ctas, &rows_per_cta)) return cudaErrorInvalidValue;
   snprintf(desc, desc_len, "fwd_tc2_d%d%s ctas=%lld rows_per_cta=%d heads_per_cta=%d", p.d,
            p.btab ? (a.staged ? "_btab_smem" : "_btab") : "", ctas, rows_per_cta,
            a.heads2 ? 2 : 1);
   if (ctas == 0) return cudaSuccess;
-  if (p.d == 64) return launch2_d<64>(a, mq, mk, mv, mt, (unsigned)ctas, st);
-  return launch2_d<128>(a, mq, mk, mv, mt, (unsigned)ctas, st);
+  if (p.d == 64) return launch2_d<64>(a, m, (unsigned)ctas, st);
+  return launch2_d<128>(a, m, (unsigned)ctas, st);
 }
 
 }  // namespace attn

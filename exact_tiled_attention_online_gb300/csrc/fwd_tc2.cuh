@@ -91,6 +91,7 @@ struct Tc2Args {
   int ahead;      // > 0: near its end a CTA prefetches into L2 the Q tiles of the
                   // CTA this many blocks later (the one likely to start next)
   int staged;     // 1: the bias tensor goes through shared memory (kTab 2; heads2 set)
+  int tma_o;      // 1: tm_o maps O; full tiles leave through shared memory and TMA
 };
 
 // Compact work list for packed batches of at most 32 sequences.  Work item c
@@ -162,6 +163,10 @@ __device__ __forceinline__ bool wait2(Bars2 *b, uint64_t *bar, uint32_t parity, 
 // so the scores arrive biased.  kTab 2 (heads2, a tensor shared by the two
 // heads, tm_t its map): the entries of each key tile arrive in shared memory
 // and each softmax thread adds its row's to the scores it loads.
+// tm_o (a.tma_o): O's map; a tile whose 128 rows all lie in its sequence
+// writes its bf16 rows into its Q buffer (the 128-byte swizzle of the Q
+// load) and one thread stores the tile with TMA: full 128-byte lines instead
+// of 16-byte pieces of 32 rows 8 KB apart per warp store.
 // kDelta: the backward's per-row term instead of the outputs: the epilogue
 // forms D_i = dO_i . O_i from the fp32 output (with kRoundedSum, an exact
 // convex combination of V rows) and the row of dO, writes D_i to p.delta
@@ -170,7 +175,7 @@ template <int D, bool kPosScale, bool kRoundedSum, bool kBias, int kTab, bool kD
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-                   const Tc2Args a) {
+                   const __grid_constant__ CUtensorMap tm_o, const Tc2Args a) {
   constexpr bool kTabReg = kTab == 1, kTabSmem = kTab == 2;
   using L = Layout2<D, kTabSmem>;
   // V ring: fill n uses barriers v_full / v_empty[n & 1] (phase (n >> 1) & 1)
@@ -788,6 +793,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
       if (row_in) p.delta[(size_t)hx * p.total_q + t] = have ? dsum * inv : 0.f;
     } else {
       __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + toff(p.so, t, hx);
+      // the same for the tile's 128 threads: rows all in the sequence, and
+      // products run (so the Q load into the buffer has landed and every
+      // product that read it has completed)
+      // (not in the bias-tensor instances, whose softmax warps it would push
+      // past their registers)
+      const bool via_tma =
+          !kTab && a.tma_o && n_mine > 0 && i0 + x * rows_b + kTileRows <= g.nq;
+      uint8_t *so = smem + L::kQA + x * L::kTile;
   #pragma unroll
       for (int c = 0; c < D / 32; c++) {
         uint32_t o32[32];
@@ -803,7 +816,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             w.y = have ? pack_bf16x2(__uint_as_float(o32[e + 2]) * inv, __uint_as_float(o32[e + 3]) * inv) : 0u;
             w.z = have ? pack_bf16x2(__uint_as_float(o32[e + 4]) * inv, __uint_as_float(o32[e + 5]) * inv) : 0u;
             w.w = have ? pack_bf16x2(__uint_as_float(o32[e + 6]) * inv, __uint_as_float(o32[e + 7]) * inv) : 0u;
-            __stcs(reinterpret_cast<uint4 *>(dst + c * 32 + e), w);  // written once: streaming
+            if (via_tma) {  // feature f = 32 c + e: chunk f / 64, 16-byte unit (f % 64) / 8
+              const int f = c * 32 + e, k = (f % 64) / 8;
+              st_shared_v4(smem_u32(so + (f / 64) * L::kChunk + r * 128 + ((k ^ (r & 7)) << 4)),
+                           w.x, w.y, w.z, w.w);
+            } else {
+              __stcs(reinterpret_cast<uint4 *>(dst + c * 32 + e), w);  // written once: streaming
+            }
           }
           if (p.o_f32) {
             float *df = p.o_f32 + ((size_t)t * p.hq + hx) * D + c * 32;
@@ -817,6 +836,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
               __stcs(reinterpret_cast<float4 *>(df + e), f);
             }
           }
+        }
+      }
+      if (via_tma) {
+        fence_proxy_async_smem();    // the rows are visible to the TMA unit
+        named_bar_sync(1 + x, 128);  // once the tile's 128 rows are written
+        if (wq == 0 && lane == 0) {
+          const uint64_t pol = l2_policy_evict_first();  // written once
+          for (int ch = 0; ch < L::kChunks; ch++)
+            tma_store_3d_hint(&tm_o, so + ch * L::kChunk, ch * 64, hx, g.q0 + i0 + x * rows_b, pol);
+          bulk_commit();
+          bulk_wait_read();  // the buffer stays allocated until the copies have read it
         }
       }
       if (row_in && p.lse) p.lse[(size_t)hx * p.total_q + t] = have ? lse2 * kLn2 : -INFINITY;
@@ -851,10 +881,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-// mt: the bias tensor's map (used by kTab 2 only).
+// Maps: q, k, v, the bias tensor (m[3], kTab 2 only) and O (m[4], with a.tma_o).
 template <int D, bool kPos, bool kRs, bool kBias, int kTab = 0, bool kDelta = false>
-cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                    const CUtensorMap &mv, const CUtensorMap &mt, unsigned ctas, cudaStream_t st) {
+cudaError_t launch2(const Tc2Args &a, const CUtensorMap (&m)[5], unsigned ctas, cudaStream_t st) {
   constexpr int smem = Layout2<D, kTab == 2>::kAlloc;
   static bool configured[64] = {false};
   int dev = 0;
@@ -865,7 +894,8 @@ cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab, kDelta><<<ctas, kThreads2, smem, st>>>(mq, mk, mv, mt, a);
+  fwd_tc2_kernel<D, kPos, kRs, kBias, kTab, kDelta><<<ctas, kThreads2, smem, st>>>(m[0], m[1], m[2],
+                                                                                  m[3], m[4], a);
   return cudaGetLastError();
 }
 
@@ -874,12 +904,13 @@ cudaError_t launch2(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &
 // head per CTA when the group pairs up: both tiles then have the same key
 // range, no idle diagonal tile (windowed prefill 2%, linear bias 1.5%
 // faster, causal unchanged); with a bias tensor it measured 7% slower, so
-// those keep two row blocks of one head) and the tensor maps of q, k, v and,
-// when the bias tensor goes through shared memory, of the bias (mt; zeroed
-// otherwise).  false when a map of q, k or v is rejected or the grid is too
-// large.
-inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorMap *mk,
-                      CUtensorMap *mv, CUtensorMap *mt, long long *ctas, int *rows_per_cta) {
+// those keep two row blocks of one head) and the tensor maps m: q, k, v,
+// the bias tensor when it goes through shared memory (zeroed otherwise) and
+// O when there is one and TMA can address it (zeroed otherwise).  false
+// when a map of q, k or v is rejected or the grid is too large.
+inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap (&m)[5], long long *ctas,
+                      int *rows_per_cta) {
+  CUtensorMap *mq = &m[0], *mk = &m[1], *mv = &m[2], *mt = &m[3], *mo = &m[4];
   a->p = p;
   a->group = p.hq / p.hkv;
   // a bias tensor pairs heads only when the heads share it (then the two
@@ -900,6 +931,10 @@ inline bool setup_tc2(const FwdParams &p, Tc2Args *a, CUtensorMap *mq, CUtensorM
       !make_map(mk, p.k, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sk.hs, p.sk.ts) ||
       !make_map(mv, p.v, p.d, p.hkv, p.total_k, 1, kTileKeys, bf, p.sv.hs, p.sv.ts))
     return false;
+  memset(mo, 0, sizeof(*mo));
+  a->tma_o = p.o && make_map(mo, p.o, p.d, p.hq, p.total_q, 1, kTileRows, bf, p.so.hs, p.so.ts)
+                 ? 1
+                 : 0;
   const int units = a->heads2 ? p.hq / 2 : p.hq;
   *ctas = (long long)a->n_pairs * units * p.batch;
   // A packed batch of at most 32 sequences takes the compact work list when

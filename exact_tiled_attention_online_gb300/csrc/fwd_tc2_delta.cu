@@ -14,18 +14,17 @@ namespace attn {
 namespace {
 
 template <int D>
-cudaError_t launch_delta_d(const Tc2Args &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                           const CUtensorMap &mv, const CUtensorMap &mt, unsigned ctas,
+cudaError_t launch_delta_d(const Tc2Args &a, const CUtensorMap (&m)[5], unsigned ctas,
                            cudaStream_t st) {
   const bool pos = a.p.scale_log2 > 0.f;
   if (a.p.btab) {  // a bias tensor comes here only with a positive scale, no slopes
     if constexpr (D == 128)
-      if (a.staged) return launch2<D, true, true, false, 2, true>(a, mq, mk, mv, mt, ctas, st);
-    return launch2<D, true, true, false, 1, true>(a, mq, mk, mv, mt, ctas, st);
+      if (a.staged) return launch2<D, true, true, false, 2, true>(a, m, ctas, st);
+    return launch2<D, true, true, false, 1, true>(a, m, ctas, st);
   }
-  if (a.p.slopes) return launch2<D, false, true, true, 0, true>(a, mq, mk, mv, mt, ctas, st);
-  if (pos) return launch2<D, true, true, false, 0, true>(a, mq, mk, mv, mt, ctas, st);
-  return launch2<D, false, true, false, 0, true>(a, mq, mk, mv, mt, ctas, st);
+  if (a.p.slopes) return launch2<D, false, true, true, 0, true>(a, m, ctas, st);
+  if (pos) return launch2<D, true, true, false, 0, true>(a, m, ctas, st);
+  return launch2<D, false, true, false, 0, true>(a, m, ctas, st);
 }
 
 }  // namespace
@@ -34,14 +33,14 @@ cudaError_t launch_delta_d(const Tc2Args &a, const CUtensorMap &mq, const CUtens
 // empty rows); p.dout, p.sdo: the upstream gradient and its layout.
 cudaError_t launch_fwd_tc2_delta(const FwdParams &p, cudaStream_t st) {
   Tc2Args a;
-  CUtensorMap mq, mk, mv, mt;
+  CUtensorMap m[5];
   long long ctas = 0;
   int rows_per_cta = 0;
   if (!p.delta || !p.dout) return cudaErrorInvalidValue;
-  if (!setup_tc2(p, &a, &mq, &mk, &mv, &mt, &ctas, &rows_per_cta)) return cudaErrorInvalidValue;
+  if (!setup_tc2(p, &a, m, &ctas, &rows_per_cta)) return cudaErrorInvalidValue;
   if (ctas == 0) return cudaSuccess;
-  if (p.d == 64) return launch_delta_d<64>(a, mq, mk, mv, mt, (unsigned)ctas, st);
-  return launch_delta_d<128>(a, mq, mk, mv, mt, (unsigned)ctas, st);
+  if (p.d == 64) return launch_delta_d<64>(a, m, (unsigned)ctas, st);
+  return launch_delta_d<128>(a, m, (unsigned)ctas, st);
 }
 
 }  // namespace attn

@@ -156,6 +156,33 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// TMA store of a tile that generic stores wrote into shared memory (after
+// fence_proxy_async_smem and a sync of the writing threads), in the calling
+// thread's bulk group, with an L2 eviction-priority policy; rows past the
+// tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *m, const void *src, int x,
+                                                  int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint "
+      "[%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// This thread's committed bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Barrier `id` (1..15) over `n` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core operand reads) after this fence plus a thread sync.
 __device__ __forceinline__ void fence_proxy_async_smem() {

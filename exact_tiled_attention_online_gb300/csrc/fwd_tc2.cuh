@@ -238,6 +238,32 @@ __global__ void __launch_bounds__(kThreads2, 1)
   // 9% slower, so the biased instances test the tiles in the MMA thread).
   constexpr bool kWatch = !kTab && !kBias;
 
+  // Copies of Q and of key tile n's K and V (ring stage n % 2, V slot
+  // n % kVSt).  Q is read by this CTA alone, each K / V tile by every row
+  // block of the KV group: with the policies below Q may leave L2 first so
+  // that K / V stay for the others.
+  auto load_q = [&](uint64_t pol) {
+    mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
+    for (int t2 = 0; t2 < 2; t2++)
+      for (int c = 0; c < L::kChunks; c++)
+        tma_load_3d_hint(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full, c * 64,
+                         t2 ? h_b : h, g.q0 + i0 + t2 * rows_b, pol);
+  };
+  auto load_k = [&](int n, uint64_t pol) {
+    const int st = n & 1;
+    mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
+    for (int c = 0; c < L::kChunks; c++)
+      tma_load_3d_hint(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st], c * 64,
+                       hk, g.k0 + (n0 + n) * kTileKeys, pol);
+  };
+  auto load_v = [&](int n, uint64_t pol) {
+    const int st = n & 1;
+    mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
+    for (int c = 0; c < L::kChunks; c++)
+      tma_load_3d_hint(smem + L::kV + (n % kVSt) * L::kTile + c * L::kChunk, &tm_v,
+                       &b->v_full[st], c * 64, hk, g.k0 + (n0 + n) * kTileKeys, pol);
+  };
+
   if (threadIdx.x == 0) {
     mbar_init(&b->q_full, 1);
     for (int s = 0; s < 2; s++) {
@@ -260,6 +286,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
     b->abort = 0;
     b->filled_q = b->filled_k = b->filled_v = b->filled_t = b->mma_issued = 0;
     fence_mbar_init();
+    // Thread 0 is the producer: Q and key tile 0 leave before the block-wide
+    // sync, so their latency overlaps the allocation of tensor memory
+    if (N > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint64_t pol_kv = l2_policy_evict_last();
+      load_q(l2_policy_evict_first());
+      load_k(0, pol_kv);
+      load_v(0, pol_kv);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&b->tmem_base, kCols2);
@@ -279,35 +316,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && N > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      int filled_k = 0, filled_v = 0;
-      // Q is read by this CTA alone; each K / V tile by every row block of
-      // the KV group: Q may leave L2 first so K / V stay for the others
-      const uint64_t pol_once = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
-      mbar_arrive_expect_tx(&b->q_full, 2 * L::kTile);
-      for (int t2 = 0; t2 < 2; t2++)
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d_hint(smem + L::kQA + t2 * L::kTile + c * L::kChunk, &tm_q, &b->q_full,
-                           c * 64, t2 ? h_b : h, g.q0 + i0 + t2 * rows_b, pol_once);
-      for (int n = 0; n < N; n++) {
+      int filled_k = 1, filled_v = 1;  // Q and key tile 0: issued before the sync
+      const uint64_t pol_kv = l2_policy_evict_last();
+      for (int n = 1; n < N; n++) {
         const int st = n & 1, u = n >> 1;
-        const int key_row = g.k0 + (n0 + n) * kTileKeys;
         if (n >= 2 && !wait2(b, &b->k_empty[st], (u - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&b->k_full[st], L::kTile);
         filled_k++;
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d_hint(smem + L::kK + st * L::kTile + c * L::kChunk, &tm_k, &b->k_full[st],
-                           c * 64, hk, key_row, pol_kv);
+        load_k(n, pol_kv);
         if (n >= kVSt &&
             !wait2(b, &b->v_empty[(n - kVSt) & 1], ((n - kVSt) >> 1) & 1, p.err))
           break;
-        mbar_arrive_expect_tx(&b->v_full[st], L::kTile);
         filled_v++;
-        for (int c = 0; c < L::kChunks; c++)
-          tma_load_3d_hint(smem + L::kV + (n % kVSt) * L::kTile + c * L::kChunk, &tm_v,
-                           &b->v_full[st], c * 64, hk, key_row, pol_kv);
+        load_v(n, pol_kv);
       }
       // The grid runs one CTA per SM at a time, so a CTA's start waits on its
       // Q tiles; warm L2 with those of the CTA `ahead` blocks later (about

@@ -162,6 +162,23 @@ def test_bad_cu_seqlens_sets_device_flag():
     assert attn.get_device_error() == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_uniform_totals_with_bad_cu_seqlens_set_device_flag(which):
+    """Totals of batch x max with cu_seqlens in which one sequence runs past
+    the max (a broken layout contract the totals alone do not show) are
+    caught on the device and reported; a correct call afterwards is clean."""
+    w = inputs.custom("unif", (128, 128), (128, 128), 4, 2, 128, "bf16", TL)
+    x = inputs.make_inputs(w, device="cuda")
+    bad = torch.tensor([0, 60, 256], dtype=torch.int32, device="cuda")
+    cu_q = bad if which == "q" else x["cu_seqlens_q"]
+    cu_k = bad if which == "k" else x["cu_seqlens_k"]
+    attn.fwd(x["q"], x["k"], x["v"], cu_q, cu_k, 128, 128, TL)
+    assert "fwd_tc2" in attn.last_plan(), attn.last_plan()
+    assert attn.get_device_error() == 6
+    attn.fwd(x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], 128, 128, TL)
+    assert attn.get_device_error() == 0
+
+
 @pytest.mark.parametrize("scale", [-0.07, 0.0])
 def test_non_positive_scale(scale):
     """scale <= 0 takes the path that scales scores before the row max."""

@@ -66,7 +66,11 @@ struct LayoutF {
   static constexpr int kDS = kDO + kStagesA * kQT;   // dS^T [128 keys][64 rows] fp16, swizzled
   static constexpr int kRow = kDS + kKeysA * kRowsA * 2;  // [2] x {-lse2[64], -D[64]}
   static constexpr int kBar = kRow + 2 * 2 * kRowsA * 4;
-  static constexpr int kUsed = kBar + 512;
+  // dQ^T readout: per readout warp two [16 rows x 32 fp32] tiles for the
+  // TMA reduce-adds into the accumulator
+  static constexpr int kDQ = (kBar + 512 + 1023) / 1024 * 1024;
+  static constexpr int kDQWarp = 2 * 16 * 32 * 4;
+  static constexpr int kUsed = kDQ + 4 * kDQWarp;
   static constexpr int kAlloc = kUsed + 1024;
 };
 static_assert(LayoutF::kAlloc <= 227 * 1024, "shared memory of one CTA");
@@ -83,9 +87,6 @@ struct BarsF {
 };
 static_assert(sizeof(BarsF) <= 512, "barrier block fits its shared-memory slot");
 
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
 
 // kBias: linear positional bias; kTab: explicit bias tensor (entries added
 // to the exponent argument in registers, loaded a step ahead), as in the
@@ -94,7 +95,7 @@ template <bool kBias, bool kTab>
 __global__ void __launch_bounds__(kThreadsF, 1)
     bwd_fused_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                        const BwdTcArgs a) {
+                        const __grid_constant__ CUtensorMap tm_dq, const BwdTcArgs a) {
   constexpr int D = kDF;
   using L = LayoutF;
   extern __shared__ uint8_t smem_raw[];
@@ -455,10 +456,16 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
   } else {
     reg_dealloc<kRegOut>();
-    // dQ readout: thread = head-dim index (TMEM lane), 64 rows per step
+    // dQ readout: thread = head-dim index (TMEM lane), 64 rows per step.
+    // Each warp reduces its 32 features into the fp32 accumulator by TMA:
+    // 32 rows at a time (two [16 rows x 32 fp32] shared tiles, row c of a
+    // tile at 128 c bytes, one reduce-add each) once the tiles' previous
+    // reduce-adds have read them; rows past the sequence add 0 (a 16-row
+    // group wholly past it is skipped).  Only the warp itself syncs, so an
+    // early exit cannot strand another warp.
     const int wq = warp & 3;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-    const size_t rs = (size_t)p.hq * D;  // accumulator row stride (floats)
+    float *sdq = reinterpret_cast<float *>(smem + L::kDQ + wq * L::kDQWarp);
     bool ok = true;
     for (int it = 0; it < n_it; it++) {
       const int tb = it & 1;
@@ -466,22 +473,36 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32(t_lane + kColDP + tb * kRowsA, v0);
-      tmem_ld32(t_lane + kColDP + tb * kRowsA + 32, v1);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&b->dq_free[tb]);
       const int i0 = it_row0(it);
-      const int rows = g.nq - i0 < kRowsA ? g.nq - i0 : kRowsA;  // rows past the sequence: skipped
-      float *dst = p.dqacc + ((size_t)(g.q0 + i0) * p.hq + it_head(it)) * D + wq * 32 + lane;
+      const int rows = g.nq - i0 < kRowsA ? g.nq - i0 : kRowsA;
+      const int head = it_head(it);
 #pragma unroll
-      for (int c = 0; c < 32; c++)
-        if (c < rows) red_add_f32(dst + c * rs, __uint_as_float(v0[c]));
+      for (int hf = 0; hf < 2; hf++) {  // rows [32 hf, 32 hf + 32) of the step
+        uint32_t v[32];
+        tmem_ld32(t_lane + kColDP + tb * kRowsA + 32 * hf, v);
+        tmem_wait_ld();
+        if (hf == 1) {  // the step's dQ^T is out of tensor memory
+          tc_fence_before();
+          mbar_arrive(&b->dq_free[tb]);
+        }
+        if (32 * hf >= rows) continue;  // warp-uniform
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 32; c++)
-        if (32 + c < rows) red_add_f32(dst + (32 + c) * rs, __uint_as_float(v1[c]));
+        for (int c = 0; c < 32; c++)
+          sdq[c * 32 + lane] = 32 * hf + c < rows ? __uint_as_float(v[c]) : 0.f;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, sdq, wq * 32, head, g.q0 + i0 + 32 * hf);
+          if (32 * hf + 16 < rows)
+            tma_reduce_add_3d(&tm_dq, sdq + 16 * 32, wq * 32, head, g.q0 + i0 + 32 * hf + 16);
+          bulk_commit();
+        }
+      }
     }
+    // the shared tiles stay allocated until the last reduce-adds have read them
+    if (lane == 0) bulk_wait_read();
   }
 
   tc_fence_before();
@@ -539,18 +560,20 @@ template <bool kBias, bool kTab>
 cudaError_t launch_fused_t(const BwdTcArgs &a, cudaStream_t st) {
   const BwdParams &p = a.p;
   const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap q64, do64, mk, mv;
+  CUtensorMap q64, do64, mk, mv, mdq;
   if (!make_map(&q64, p.q16, kDF, p.hq, p.total_q, 1, kRowsA, f16) ||
       !make_map(&do64, p.do16, kDF, p.hq, p.total_q, 1, kRowsA, f16) ||
       !make_map(&mk, p.k16, kDF, p.hkv, p.total_k, 1, kTileKeys, f16) ||
-      !make_map(&mv, p.v16, kDF, p.hkv, p.total_k, 1, kTileKeys, f16))
+      !make_map(&mv, p.v16, kDF, p.hkv, p.total_k, 1, kTileKeys, f16) ||
+      !make_map_f32(&mdq, p.dqacc, kDF, p.hq, p.total_q, 32, 16))
     return cudaErrorInvalidValue;
   static bool conf[64] = {false};
   cudaError_t e = set_smem(bwd_fused_tc_kernel<kBias, kTab>, LayoutF::kAlloc, conf);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.n_key_tiles * p.hkv * p.batch;
   if (grid >= (1LL << 31)) return cudaErrorInvalidValue;
-  bwd_fused_tc_kernel<kBias, kTab><<<(unsigned)grid, kThreadsF, LayoutF::kAlloc, st>>>(q64, do64, mk, mv, a);
+  bwd_fused_tc_kernel<kBias, kTab><<<(unsigned)grid, kThreadsF, LayoutF::kAlloc, st>>>(q64, do64, mk, mv,
+                                                                                        mdq, a);
   return cudaGetLastError();
 }
 

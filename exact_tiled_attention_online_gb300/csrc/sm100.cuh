@@ -169,6 +169,24 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *m, const vo
       : "memory");
 }
 
+// TMA reduce-add of a shared tile into global memory (the element type is
+// the map's), in the calling thread's bulk group; rows past the tensor's
+// extent are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, const void *src, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group "
+      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// All but the newest of this thread's committed bulk groups have read their
+// shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -46,6 +46,22 @@ inline bool make_map(CUtensorMap *m, const void *base, int D, int H, int T, int 
   return r == CUDA_SUCCESS;
 }
 
+// A contiguous [T, H, D] fp32 tensor seen as 3-D (d, head, token), boxes of
+// box_d features x 1 head x box_t tokens, no swizzle (rows of box_d floats
+// packed in shared memory).
+inline bool make_map_f32(CUtensorMap *m, float *base, int D, int H, int T, int box_d, int box_t) {
+  auto enc = tensor_map_encoder();
+  if (!enc || !base || T <= 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_t};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // An fp32 bias tensor seen as 3-D (key, row, sequence), element strides
 // row_stride and seq_stride (0: the sequences share one set of entries),
 // loaded in boxes of 32 keys x 128 rows with the 128-byte swizzle.  Entries

@@ -11,9 +11,10 @@
 // paragraphs: the gradients of every input, GQA sums over shared heads).
 // dQ^T takes K from the same shared-memory tile as S^T (read d-major) and
 // dS^T from a shared-memory copy the math warps write beside the tensor-memory
-// one; a readout warpgroup moves each step's dQ^T from tensor memory to an
-// fp32 accumulator in global memory with reductions, since the rows' other
-// key tiles belong to other CTAs.  A last kernel scales the accumulator back
+// one; a readout warpgroup moves each step's dQ^T from tensor memory through
+// shared memory into an fp32 accumulator in global memory with TMA
+// reduce-adds, since the rows' other key tiles belong to other CTAs.  A last
+// kernel scales the accumulator back
 // (the fp16 copies' power-of-two factors and the softmax scale) and writes
 // dQ in bf16.  The summation order of dQ then depends on the CTAs' timing:
 // the two-kernel backward stays available for bit-reproducible gradients.

@@ -13,12 +13,14 @@
 // so that while one softmax warpgroup turns its S into P, the tensor core is
 // busy with the other tile.  Warpgroups: the first holds warp 0 (TMA
 // producer), warp 1 (TMEM allocation and MMA issue) and warp 2 (without a
-// bias, a watcher that folds the K / V arrivals into the P barriers) and
-// gives most of its registers to the other two, which run the softmax of
-// tile A (warps 4..7) and tile B (warps 8..11), thread = row = TMEM lane.  TMEM: S_A, S_B, O_A,
+// bias, a watcher that folds the K / V arrivals into the P barriers; with a
+// staged bias tensor, the copies of its entries) and gives most of its
+// registers to the other two, which run the softmax of tile A (warps 4..7)
+// and tile B (warps 8..11), thread = row = TMEM lane.  TMEM: S_A, S_B, O_A,
 // O_B; each tile's bf16 P overwrites the second half of its S and feeds P V
 // from tensor memory, so P never passes through shared memory.  Shared
-// memory: Q_A, Q_B and a 2-stage K/V ring.
+// memory: Q_A, Q_B (which also stage full O tiles for their TMA stores) and
+// a 2-stage K/V ring.
 //
 // With the extra registers a softmax thread loads its whole 128-score row
 // from TMEM with one wait, takes the max, and writes the 64 packed

@@ -105,3 +105,29 @@ def test_many_expired_calls_leave_the_device_usable():
     on, ln = compare.to_np(o), compare.to_np(lse)
     compare.check_close("o", on[rows[:, 0], rows[:, 1]], ro)
     compare.check_lse("lse", ln[rows[:, 1], rows[:, 0]], rlse)
+
+
+def test_expired_wait_staged_bias_reports_and_recovers():
+    """The prefill with a head-shared bias tensor streamed through shared
+    memory (warp 2 copying each key tile's entries): the same expiry, drain
+    (the entries' copies included) and recovery."""
+    w = inputs.custom("tmo_bias", (300, 129), (300, 129), 8, 2, 128, "bf16", TL, seed=82)
+    x = inputs.make_inputs(w, device="cuda")
+    bias = inputs.bias_tensor(w.batch, 1, w.max_q, w.max_k, seed=83).cuda()
+    args = (x["q"], x["k"], x["v"], x["cu_seqlens_q"], x["cu_seqlens_k"], w.max_q, w.max_k, TL,
+            w.scale)
+    assert attn.get_device_error() == 0
+    attn.set_wait_limit_ns(1)
+    try:
+        attn.fwd(*args, bias=bias)
+        assert "_btab_smem" in attn.last_plan(), attn.last_plan()
+        assert attn.get_device_error() == TIMEOUT
+    finally:
+        attn.set_wait_limit_ns(0)
+    o, lse = attn.fwd(*args, bias=bias)
+    assert attn.get_device_error() == 0
+    host = {k: (t.cpu() if hasattr(t, "cpu") else t) for k, t in x.items()}
+    ro, rlse = oracle.fwd(host["q"], host["k"], host["v"], host["cu_seqlens_q"],
+                          host["cu_seqlens_k"], w.scale, TL, bias=bias.cpu())
+    compare.check_close("o", o, ro)
+    compare.check_lse("lse", lse, rlse)
